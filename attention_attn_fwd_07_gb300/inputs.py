@@ -1,0 +1,85 @@
+"""Seeded synthetic inputs and the named workloads.
+
+This module is shared by the CUDA path's callers and by the oracle's callers.
+It holds no attention arithmetic: only shapes, seeds and random draws.
+
+Every tensor is drawn i.i.d. N(0, 1) in float32 from a seeded
+``torch.Generator`` and rounded to bfloat16 (round-to-nearest-even); those
+bfloat16 bits are the common input of both sides.  The long-prefill workload
+additionally multiplies K by 4 on exactly ceil(0.01 * Nk) key rows per
+(batch, head), chosen by ``randperm`` from the same generator; x4 is exact in
+bfloat16.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    k_boost_frac: float = 0.0
+    splits: tuple = field(default=())
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d), rounded to float32 as the library receives it."""
+        return float(torch.tensor(1.0 / math.sqrt(self.d), dtype=torch.float32))
+
+
+# The five workloads of the fused attention forward (seeds 1000 + index).
+TINY = Workload("tiny B1 H1 N128 d64 non-causal", 1, 1, 128, 128, 64, False, 1000)
+RAGGED_LENGTHS = (1, 31, 32, 33, 1003)
+RAGGED_SPLITS = (1, 3, 16)
+PREFILL = Workload("prefill B4 H16 N2048 d64 causal", 4, 16, 2048, 2048, 64, True, 1002)
+LONG_PREFILL_CAUSAL = Workload("long prefill B2 H32 N8192 d128 causal, K x4 on 1% rows",
+                               2, 32, 8192, 8192, 128, True, 1003, k_boost_frac=0.01)
+LONG_PREFILL_NONCAUSAL = Workload("long prefill B2 H32 N8192 d128 non-causal, K x4 on 1% rows",
+                                  2, 32, 8192, 8192, 128, False, 1003, k_boost_frac=0.01)
+DECODE = Workload("decode B16 H32 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768, 128, False,
+                  1004, splits=(16, 32, 64))
+
+
+def ragged(n: int, causal: bool) -> Workload:
+    """Ragged-length edge case: B=3, H=4, d=64, Nq=Nk=n (seed 1001 + n)."""
+    tag = "causal" if causal else "non-causal"
+    return Workload(f"ragged B3 H4 N{n} d64 {tag}", 3, 4, n, n, 64, causal, 1001 + n)
+
+
+def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = None,
+             Nk: int | None = None):
+    """Draw (q, k, v) as contiguous bfloat16 [B, H, N, d] tensors on ``device``.
+
+    ``Nq``/``Nk`` override the workload's lengths (smaller parity cases that
+    keep the same distribution).
+    """
+    Nq = w.Nq if Nq is None else Nq
+    Nk = w.Nk if Nk is None else Nk
+    g = torch.Generator(device=device).manual_seed(w.seed)
+
+    def draw(n):
+        out = torch.empty((w.B, w.H, n, w.d), dtype=torch.bfloat16, device=device)
+        for b in range(w.B):  # per batch keeps the float32 temporary small
+            out[b] = torch.randn((w.H, n, w.d), generator=g, device=device,
+                                 dtype=torch.float32).to(torch.bfloat16)
+        return out
+
+    q, k, v = draw(Nq), draw(Nk), draw(Nk)
+    if w.k_boost_frac > 0.0:
+        n_boost = math.ceil(w.k_boost_frac * Nk)
+        for b in range(w.B):
+            for h in range(w.H):
+                rows = torch.randperm(Nk, generator=g, device=device)[:n_boost]
+                k[b, h, rows] = k[b, h, rows] * 4
+    return q, k, v
+
