@@ -1,0 +1,258 @@
+// api.cu -- the C ABI declared in include/attn.h: argument validation,
+// TMA descriptor encoding, workspace layout and kernel launches.  No device
+// memory is allocated here and no work runs anywhere but in this library's
+// kernels.  Validation happens before any CUDA call, so argument errors are
+// reported identically with or without a GPU.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "internal.cuh"
+
+namespace attn {
+
+// The library's own status word, one per device (used when the caller does
+// not pass attn_params.dev_status).  Bit 0: some kernel gave up a wait.
+__device__ int g_status_word;
+
+cudaError_t default_status_word(int** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_status_word);
+}
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;  // TMA coordinates and grid size
+constexpr int64_t kMaxOffset = int64_t{1} << 40;
+constexpr int kMaxSplits = 256;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [BH][N][d] bf16 viewed as a 3-D tensor (d fastest); 64 x 128 x 1 boxes with
+// the 128-byte swizzle the MMA descriptors expect; out-of-range rows read 0.
+bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* ptr,
+                int64_t N, int64_t BH, int64_t d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(N * d * 2)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by both forward entry points.
+int validate(const attn_params* p) {
+  if (p == nullptr) return ATTN_ERR_INVALID;
+  if (!p->q || !p->k || !p->v || !p->o || !p->lse) return ATTN_ERR_INVALID;
+  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1) return ATTN_ERR_INVALID;
+  if (!std::isfinite(p->scale) || !(p->scale > 0.0f)) return ATTN_ERR_INVALID;
+  if (p->query_offset < -kMaxOffset || p->query_offset > kMaxOffset) return ATTN_ERR_INVALID;
+  if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
+  if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
+      p->Nk > kMaxDim)
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->v, 16) || !aligned(p->o, 16) ||
+      !aligned(p->lse, 4))
+    return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
+int64_t keys_per_split(int64_t Nk, int splits) {
+  const int64_t per = (Nk + splits - 1) / splits;
+  return (per + 127) / 128 * 128;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
+  int rc = validate(p);
+  if (rc != ATTN_OK) return rc;
+  const int64_t BH = p->B * p->H;
+  const int64_t blocks = BH * ((p->Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta);
+  if (blocks > kMaxDim) return ATTN_ERR_UNSUPPORTED;
+
+  int* status = p->dev_status;
+  if (status == nullptr && default_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d) || !encode_map(enc, &tk, p->k, p->Nk, BH, p->d) ||
+      !encode_map(enc, &tv, p->v, p->Nk, BH, p->d))
+    return ATTN_ERR_CUDA;
+
+  FwdArgs a;
+  a.o = p->o;
+  a.lse = p->lse;
+  a.status = status;
+  a.BH = BH;
+  a.Nq = p->Nq;
+  a.Nk = p->Nk;
+  a.query_offset = p->query_offset;
+  a.d = static_cast<int>(p->d);
+  a.causal = p->causal ? 1 : 0;
+  a.scale = p->scale;
+  a.flags = p->flags;
+  a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
+  return launch_fwd_tcgen05(a, tq, tk, tv, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                        float scale, cudaStream_t stream) {
+  attn_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.d = d;
+  p.causal = causal;
+  p.scale = scale;
+  return attn_fwd_ex(&p, stream);
+}
+
+extern "C" size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
+                                               int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
+  if (num_splits < 1 || num_splits > kMaxSplits) return 0;
+  if (B > kMaxDim || H > kMaxDim || Nq > kMaxDim || B * H > kMaxDim) return 0;
+  const unsigned __int128 rows =
+      static_cast<unsigned __int128>(B * H) * static_cast<unsigned>(num_splits) *
+      static_cast<uint64_t>(Nq);
+  const unsigned __int128 bytes = rows * static_cast<uint64_t>(d) * 4u + 256u + rows * 4u;
+  if (bytes > (static_cast<unsigned __int128>(1) << 62)) return 0;
+  const size_t r = static_cast<size_t>(rows);
+  return align256(r * static_cast<size_t>(d) * 4) + r * 4;
+}
+
+extern "C" int attn_combine(const float* o_part, const float* lse_part, void* o, float* lse,
+                            int64_t B, int64_t H, int64_t Nq, int64_t d, int num_splits,
+                            cudaStream_t stream) {
+  if (!o_part || !lse_part || !o || !lse) return ATTN_ERR_INVALID;
+  if (B < 1 || H < 1 || Nq < 1 || num_splits < 1 || num_splits > kMaxSplits)
+    return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (B > kMaxDim || H > kMaxDim || Nq > kMaxDim || B * H > kMaxDim ||
+      (B * H * Nq + 7) / 8 > kMaxDim)
+    return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_ALIGN;
+  return launch_combine(o_part, lse_part, o, lse, B * H, Nq, static_cast<int>(d), num_splits,
+                        stream) == cudaSuccess
+             ? ATTN_OK
+             : ATTN_ERR_CUDA;
+}
+
+extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  int rc = validate(p);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
+  const size_t need = attn_splitkv_workspace_bytes(p->B, p->H, p->Nq, p->d, num_splits);
+  if (need == 0) return ATTN_ERR_UNSUPPORTED;
+  if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return ATTN_ERR_ALIGN;
+  const int64_t BH = p->B * p->H;
+  const int64_t qb = p->Nq == 1 ? 1 : 4;  // query rows per partial CTA
+  if (BH * ((p->Nq + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
+
+  const size_t rows = static_cast<size_t>(BH) * num_splits * static_cast<size_t>(p->Nq);
+  SplitArgs a;
+  a.q = p->q;
+  a.k = p->k;
+  a.v = p->v;
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        align256(rows * static_cast<size_t>(p->d) * 4));
+  a.BH = BH;
+  a.Nq = p->Nq;
+  a.Nk = p->Nk;
+  a.query_offset = p->query_offset;
+  a.keys_per_split = keys_per_split(p->Nk, num_splits);
+  a.d = static_cast<int>(p->d);
+  a.splits = num_splits;
+  a.causal = p->causal ? 1 : 0;
+  a.scale = p->scale;
+  if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_combine(a.o_part, a.lse_part, p->o, p->lse, BH, p->Nq, a.d, num_splits, stream) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                                int causal, float scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  attn_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.d = d;
+  p.causal = causal;
+  p.scale = scale;
+  return attn_fwd_splitkv_ex(&p, num_splits, workspace, workspace_bytes, stream);
+}
+
+extern "C" int attn_get_device_status(int* dev_status_host, cudaStream_t stream) {
+  if (dev_status_host == nullptr) return ATTN_ERR_INVALID;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  int* word = nullptr;
+  if (default_status_word(&word) != cudaSuccess) return ATTN_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  *dev_status_host = value;
+  return ATTN_OK;
+}
+
+extern "C" const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID: return "ATTN_ERR_INVALID: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported head dim or size";
+    case ATTN_ERR_ALIGN: return "ATTN_ERR_ALIGN: misaligned pointer";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call failed";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT: a kernel gave up a wait";
+    default: return "unknown attn status";
+  }
+}

@@ -1,0 +1,472 @@
+// fwd_tcgen05.cu -- fused attention forward (prefill) for sm_103a.
+//
+// Computes, per (batch*head, query row), O = softmax(scale * Q K^T [causal]) V
+// and LSE = ln sum exp(scores), by the online-softmax recurrence of
+// "GPU Engineering: Correctness, Throughput, and Attention" (section 22.5:
+// running maximum m, normaliser l, unnormalised accumulator o; old state is
+// rescaled by exp(m - m_new) when the maximum grows; output o / l), with the
+// section 22.7 lab's conventions (causal rule j > i + query_offset applied
+// before maxima and sums, "safe" exponent reference 0 for a row that is still
+// fully masked, output 0 and LSE -inf for a row with no admissible key,
+// LSE = m + ln l).  The score tile lives only in tensor memory; nothing of
+// size Nq x Nk touches device memory.
+//
+// One CTA owns 256 query rows of one (b,h) as two 128-row tiles A and B that
+// share every K/V tile (prior art: the producer/consumer, TMA-fed, on-chip
+// accumulator pipeline described for FlashAttention-3 on H100; here rebuilt
+// on tcgen05 with TMEM accumulators):
+//   warp 9      TMA producer: Q_A, Q_B once, then K0 V0 K1 V1 ... through an
+//               NS-stage shared-memory ring (full/empty mbarriers).
+//   warp 8      MMA issuer (one thread): S_X = Q_X K^T into TMEM (SS MMA), and
+//               O_X += P_X V (TS MMA, P read from TMEM) for X in {A, B},
+//               ordered so that the tensor core works on one tile while the
+//               other tile's softmax runs (ping-pong).
+//   warps 0-3   softmax of tile A; warps 4-7 softmax of tile B.  One thread
+//               per query row (TMEM lane = row): tcgen05.ld of the 128-score
+//               row, mask, row max, exp2, row sum, bf16 P written back into the
+//               S columns with tcgen05.st; O rescaled in TMEM only when the
+//               row maximum grew by more than 2^8 (otherwise the stale
+//               reference is kept; o and l share it, so o / l is unchanged).
+//               Epilogue: O / l -> bf16 global, LSE -> f32 global.
+// TMEM (512 columns): S_A [0,128) S_B [128,256) O_A [256,256+d) O_B [256+d, 256+2d).
+//
+// Every mbarrier wait is bounded (globaltimer budget); on expiry the CTA
+// records a timeout in the status word, all roles leave their loops, pending
+// TMA loads and MMAs are awaited (bounded), TMEM is freed and the CTA exits.
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "attn.h"
+
+namespace attn {
+namespace {
+
+constexpr int BM = 128;            // query rows per tile (= TMEM lanes)
+constexpr int BN = 128;            // keys per K/V tile
+constexpr int kThreads = 320;      // 8 softmax warps + MMA warp + TMA warp
+constexpr int kWarpMma = 8;
+constexpr int kWarpLoad = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows by > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int kAtoms = D / 64;                     // 128-byte swizzle atoms per row
+  static constexpr uint32_t kAtomBytes = 128u * 128u;       // one [128 rows][64 bf16] box
+  static constexpr uint32_t kQBytes = BM * D * 2;           // one Q tile
+  static constexpr uint32_t kKVBytes = BN * D * 2;          // one K or V tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffKV = 2 * kQBytes;
+  static constexpr uint32_t kOffBar = kOffKV + kStages * kKVBytes;
+  // barriers: full[S], empty[S], q_full, s_full[2], p_ready[2], o_full[2], drain
+  static constexpr int kBarFull = 0;
+  static constexpr int kBarEmpty = kStages;
+  static constexpr int kBarQ = 2 * kStages;
+  static constexpr int kBarS = kBarQ + 1;
+  static constexpr int kBarP = kBarS + 2;
+  static constexpr int kBarO = kBarP + 2;
+  static constexpr int kBarDrain = kBarO + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
+  static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + 1 KiB alignment slack
+  static constexpr uint32_t kColS = 0;      // + 128 * tile
+  static constexpr uint32_t kColO = 256;    // + D * tile
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSmemBytes > 232448 / 2, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
+};
+
+struct KParams {
+  __nv_bfloat16* o;
+  float* lse;
+  int* status;
+  int64_t Nq, Nk, qoff;
+  int n_qblk;
+  int causal;
+  float sc_log2;  // scale * log2(e)
+  uint32_t flags;
+  uint64_t timeout_ns;
+};
+
+struct Waiter {
+  volatile int* abort_flag;
+  int* status;
+  uint64_t timeout_ns;
+
+  // Bounded wait for the phase of `bar` with parity `parity`.  Returns false
+  // when the CTA is aborting (another role timed out) or this wait timed out.
+  __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((spin & 31u) == 0) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+          *abort_flag = 1;
+          atomicOr(status, 1);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+// Number of K/V tiles query tile `row0` (128 rows) must visit; 0 if the tile
+// is past Nq or (negative offsets only) no row of it sees any key.
+__device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
+  if (row0 >= p.Nq) return 0;
+  const int64_t n_all = (p.Nk + BN - 1) / BN;
+  if (!p.causal) return static_cast<int>(n_all);
+  const int64_t last_row = min(row0 + BM - 1, p.Nq - 1);
+  const int64_t last_key = last_row + p.qoff;
+  if (last_key < 0) return 0;
+  return static_cast<int>(min(n_all, last_key / BN + 1));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tcgen05_kernel(const __grid_constant__ CUtensorMap tq,
+                            const __grid_constant__ CUtensorMap tk,
+                            const __grid_constant__ CUtensorMap tv, const KParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // CTA -> (bh, query block); causal grids start with the heaviest blocks.
+  const int64_t bh = blockIdx.x / p.n_qblk;
+  const int qi = static_cast<int>(blockIdx.x % p.n_qblk);
+  const int qb = p.causal ? (p.n_qblk - 1 - qi) : qi;
+  const int64_t q0 = static_cast<int64_t>(qb) * (2 * BM);
+  int ntile[2];
+  ntile[0] = tiles_for(q0, p);
+  ntile[1] = tiles_for(q0 + BM, p);
+  const int n_kv = max(ntile[0], ntile[1]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(C::kBarFull + s), 1);
+      mbar_init(bar(C::kBarEmpty + s), 1);
+    }
+    mbar_init(bar(C::kBarQ), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(C::kBarS + x), 1);
+      mbar_init(bar(C::kBarP + x), 128);
+      mbar_init(bar(C::kBarO + x), 1);
+    }
+    mbar_init(bar(C::kBarDrain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpLoad && lane == 0) {
+    tma_prefetch_map(&tq);
+    tma_prefetch_map(&tk);
+    tma_prefetch_map(&tv);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter wait{abort_flag, p.status, p.timeout_ns};
+
+  const uint32_t sQ = sbase + C::kOffQ;
+  const uint32_t sKV = sbase + C::kOffKV;
+
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kv > 0) {
+      uint32_t qbytes = 0;
+      for (int x = 0; x < 2; ++x) qbytes += ntile[x] > 0 ? C::kQBytes : 0u;
+      mbar_arrive_expect_tx(bar(C::kBarQ), qbytes);
+      for (int x = 0; x < 2; ++x) {
+        if (ntile[x] == 0) continue;
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d(sQ + x * C::kQBytes + a * C::kAtomBytes, &tq, bar(C::kBarQ), a * 64,
+                      static_cast<int>(q0 + x * BM), static_cast<int>(bh));
+      }
+      // Ring position t: K(t/2) for even t, V(t/2) for odd t.
+      int last_t[C::kStages];
+      for (int s = 0; s < C::kStages; ++s) last_t[s] = -1;
+      int skipped = -1;
+      bool ok = true;
+      for (int t = 0; t < 2 * n_kv && ok; ++t) {
+        const int s = t % C::kStages;
+        if (t >= C::kStages) ok = wait(bar(C::kBarEmpty + s), ((t / C::kStages) - 1) & 1);
+        if (!ok) break;
+        last_t[s] = t;
+        if ((p.flags & ATTN_FLAG_TEST_SKIP_LOAD) && t == 1) {  // fault injection
+          skipped = t;
+          continue;
+        }
+        mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kKVBytes);
+        const CUtensorMap* map = (t & 1) ? &tv : &tk;
+        const int key0 = (t >> 1) * BN;
+        for (int a = 0; a < C::kAtoms; ++a)
+          tma_load_3d(sKV + s * C::kKVBytes + a * C::kAtomBytes, map, bar(C::kBarFull + s),
+                      a * 64, key0, static_cast<int>(bh));
+      }
+      // Every issued load must land before the CTA can exit.  Only this
+      // thread arrives on the full barriers, so the phase of the last load
+      // into a stage stays complete once it lands.  These waits ignore the
+      // abort flag (they cover copies in flight) but are still bounded.
+      volatile int no_abort = 0;
+      const Waiter own{&no_abort, p.status, p.timeout_ns};
+      own(bar(C::kBarQ), 0);
+      for (int s = 0; s < C::kStages; ++s)
+        if (last_t[s] >= 0 && last_t[s] != skipped)
+          own(bar(C::kBarFull + s), (last_t[s] / C::kStages) & 1);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_kv > 0) {
+      auto qk = [&](int x, int stage) {
+        const uint32_t d_tmem = tmem + C::kColS + 128 * x;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes + off, 16, 1024);
+          const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes + off, 16, 1024);
+          mma_ss(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto pv = [&](int x, int stage, bool acc) {
+        const uint32_t d_tmem = tmem + C::kColO + D * x;
+        const uint32_t p_tmem = tmem + C::kColS + 128 * x;
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t b =
+              sdesc_sw128(sKV + stage * C::kKVBytes + kk * 16 * 128, C::kAtomBytes, 1024);
+          mma_ts(d_tmem, p_tmem + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait(bar(C::kBarQ), 0);
+      if (ok) ok = wait(bar(C::kBarFull + 0), 0);
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x) {
+          if (ntile[x] > 0) {
+            qk(x, 0);
+            mma_commit(bar(C::kBarS + x));
+          }
+        }
+        mma_commit(bar(C::kBarEmpty + 0));
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int tV = 2 * j + 1, sV = tV % C::kStages;
+        const int tK = 2 * j + 2, sK = tK % C::kStages;
+        const bool next = j + 1 < n_kv;
+        bool k_ready = false;
+        ok = wait(bar(C::kBarFull + sV), (tV / C::kStages) & 1);
+        if (!ok) break;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (j >= ntile[x]) continue;
+          ok = wait(bar(C::kBarP + x), j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          pv(x, sV, j > 0);
+          if (j == ntile[x] - 1) mma_commit(bar(C::kBarO + x));
+          if (j + 1 < ntile[x]) {
+            if (!k_ready) {
+              ok = wait(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            qk(x, sK);
+            mma_commit(bar(C::kBarS + x));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kBarEmpty + sV));
+        if (next) {
+          if (!k_ready) {  // K(j+1) is used by no tile: still consume it in order
+            ok = wait(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
+            if (!ok) break;
+          }
+          mma_commit(bar(C::kBarEmpty + sK));
+        }
+      }
+      // All issued MMAs must complete before TMEM is released (bounded wait
+      // that ignores the abort flag).
+      mma_commit(bar(C::kBarDrain));
+      volatile int no_abort = 0;
+      const Waiter own{&no_abort, p.status, p.timeout_ns};
+      own(bar(C::kBarDrain), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = warp >> 2;  // query tile
+    const int row_in_tile = ((warp & 3) << 5) + lane;
+    const int64_t row0 = q0 + x * BM;
+    const int64_t row = row0 + row_in_tile;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::kColS + 128 * x;
+    const uint32_t tO = tmem + lane_off + C::kColO + D * x;
+    const int n = ntile[x];
+    // Last admissible key of this row and of the tile's first row.
+    const int64_t lim = p.causal ? min(p.Nk - 1, row + p.qoff) : p.Nk - 1;
+    const int64_t lim_tile = p.causal ? min(p.Nk - 1, row0 + p.qoff) : p.Nk - 1;
+
+    float m_run = -INFINITY;  // running maximum of scaled scores (log2 units)
+    float m_ref = -INFINITY;  // exponent reference shared by o and l
+    float l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      // tcgen05.ld/st below are warp-collective: the warp leaves together.
+      ok = __all_sync(0xffffffffu, wait(bar(C::kBarS + x), j & 1));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld_x128(tS, sr);
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      const int64_t k0 = static_cast<int64_t>(j) * BN;
+      if (k0 + BN - 1 > lim_tile) {  // edge or diagonal tile (uniform per tile)
+        const int64_t rel64 = lim - k0;
+        const int rel = static_cast<int>(rel64 < -1 ? -1 : (rel64 > BN ? BN : rel64));
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = (c > rel) ? -INFINITY : s[c];
+      }
+      float mx[8];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        mx[g] = s[g];
+#pragma unroll
+        for (int c = g + 8; c < 128; c += 8) mx[g] = fmaxf(mx[g], s[c]);
+      }
+      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m_run, tmax * p.sc_log2);
+      m_run = m_new;
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (m_new > m_ref + kRescaleThreshold) {
+        alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
+        rescale = (m_ref != -INFINITY);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float neg_ref = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+      uint32_t pk[64];
+      float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(s[2 * c], p.sc_log2, neg_ref));
+        const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.sc_log2, neg_ref));
+        sum0 += p0;
+        sum1 += p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+      l += sum0 + sum1;
+      tmem_st_x64(tS, pk);
+      if (__any_sync(0xffffffffu, rescale) && j > 0) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + cc * 32, o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_x32(tO + cc * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarP + x));
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, wait(bar(C::kBarO + x), 0));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool valid = row < p.Nq;
+      const bool empty = (n == 0) || !(l > 0.0f);
+      if (n > 0) {
+        const float inv = empty ? 0.0f : 1.0f / l;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * D);
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(tO + cc * 32, o);
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+              if (empty) w = make_uint4(0u, 0u, 0u, 0u);
+              dst[cc * 4 + v4] = w;
+            }
+          }
+        }
+      } else if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * D);
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (valid)
+        p.lse[bh * p.Nq + row] =
+            empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                   const CUtensorMap& tv, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static_assert(C::kSmemBytes < (1u << 20), "");
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::kSmemBytes));
+  if (err != cudaSuccess) return err;
+  KParams p;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lse = a.lse;
+  p.status = a.status;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.qoff = a.query_offset;
+  p.n_qblk = static_cast<int>((a.Nq + 2 * BM - 1) / (2 * BM));
+  p.causal = a.causal;
+  p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.flags = a.flags;
+  p.timeout_ns = a.timeout_ns;
+  const int64_t blocks = a.BH * p.n_qblk;
+  attn_fwd_tcgen05_kernel<D><<<dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
+                               C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, cudaStream_t stream) {
+  if (a.d == 64) return launch<64>(a, tq, tk, tv, stream);
+  return launch<128>(a, tq, tk, tv, stream);
+}
+
+}  // namespace attn

@@ -1,0 +1,52 @@
+// internal.cuh -- launch interfaces between the C-ABI layer (api.cu) and the
+// kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace attn {
+
+// Arguments of one prefill (tcgen05) launch, already validated.
+struct FwdArgs {
+  void* o;             // bf16 [B][H][Nq][d]
+  float* lse;          // f32  [B][H][Nq]
+  int* status;         // device status word (bit 0 = wait timeout)
+  int64_t BH, Nq, Nk, query_offset;
+  int d;
+  int causal;
+  float scale;
+  uint32_t flags;
+  uint64_t timeout_ns;
+};
+
+// Arguments of one split-KV decode launch pair, already validated.
+struct SplitArgs {
+  const void *q, *k, *v;  // bf16 [B][H][N][d]
+  float* o_part;          // f32 [BH][S][Nq][d]
+  float* lse_part;        // f32 [BH][S][Nq]
+  int64_t BH, Nq, Nk, query_offset;
+  int64_t keys_per_split;
+  int d;
+  int splits;
+  int causal;
+  float scale;
+};
+
+// Query rows per CTA of the prefill kernel (two 128-row tiles).
+constexpr int kFwdRowsPerCta = 256;
+
+cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                               const CUtensorMap& tv, cudaStream_t stream);
+
+cudaError_t launch_splitkv_partial(const SplitArgs& a, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, void* o, float* lse,
+                           int64_t BH, int64_t Nq, int d, int splits, cudaStream_t stream);
+
+// Address of the library's own device status word on the current device.
+cudaError_t default_status_word(int** ptr);
+
+}  // namespace attn

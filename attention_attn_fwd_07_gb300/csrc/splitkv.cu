@@ -1,0 +1,333 @@
+// splitkv.cu -- memory-bound split-KV attention for short queries (decode)
+// and the log-sum-exp combine.
+//
+// Partial kernel: one CTA per (batch*head, query block of QB rows, key split
+// s).  The split's keys [s*L, min((s+1)*L, Nk)) are streamed once from device
+// memory with 16-byte read-only loads: a key row of d bf16 is read by d/8
+// adjacent lanes, so a warp reads 32/(d/8) whole rows per instruction and the
+// CTA's 8 warps read consecutive rows.  Each lane group keeps the online
+// softmax state of section 22.5 of "GPU Engineering: Correctness, Throughput,
+// and Attention" (running maximum m, normaliser l, unnormalised o, rescale
+// by exp2(m - m_new)) for its keys, in log2 units (q is pre-multiplied by
+// scale * log2(e)); group, warp and CTA states are merged by the same
+// rescaling.  Output per (row, split): the normalised o (f32) and its
+// natural-log LSE; an empty or fully masked split gives o = 0, lse = -inf.
+//
+// Combine kernel: one warp per (batch*head, query row) merges the splits:
+// M = max lse_s, w_s = exp(lse_s - M), O = sum w_s o_s / sum w_s (-> bf16),
+// LSE = M + ln sum w_s; M = -inf gives O = +0.0, LSE = -inf (the section 22.7
+// lab's policy for a row with no admissible key).
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr float kLog2e = 1.4426950408889634074f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct PartialParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  float* o_part;
+  float* lse_part;
+  int64_t Nq, Nk, qoff, L;
+  int S, n_qb, causal;
+  float sc_log2;
+};
+
+__device__ __forceinline__ uint4 ld_stream(const uint16_t* ptr) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(ptr));
+  return r;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
+  f[0] = bf_lo(r.x); f[1] = bf_hi(r.x);
+  f[2] = bf_lo(r.y); f[3] = bf_hi(r.y);
+  f[4] = bf_lo(r.z); f[5] = bf_hi(r.z);
+  f[6] = bf_lo(r.w); f[7] = bf_hi(r.w);
+}
+
+// Merge state (m2, l2, o2) into (m, l, o); all in log2 units.
+__device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[8], float m2, float l2,
+                                            const float (&o2)[8]) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;  // both empty
+  const float a = ex2_approx(m - mn);
+  const float b = ex2_approx(m2 - mn);
+  l = l * a + l2 * b;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = o[e] * a + o2[e] * b;
+  m = mn;
+}
+
+template <int D, int QB, int U>
+__global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const PartialParams p) {
+  constexpr int LPR = D / 8;      // lanes per key row (16 B each)
+  constexpr int G = 32 / LPR;     // key rows per warp instruction
+  constexpr int STEP = kWarps * G * U;
+
+  __shared__ float sm_m[kWarps][QB];
+  __shared__ float sm_l[kWarps][QB];
+  __shared__ __align__(16) float sm_o[kWarps][QB][D];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPR, sub = lane % LPR;
+  const int64_t lin = blockIdx.x;
+  const int s = static_cast<int>(lin % p.S);
+  const int64_t rest = lin / p.S;
+  const int qb = static_cast<int>(rest % p.n_qb);
+  const int64_t bh = rest / p.n_qb;
+  const int64_t i0 = static_cast<int64_t>(qb) * QB;
+
+  const int64_t k_lo = static_cast<int64_t>(s) * p.L;
+  int64_t k_hi = min(k_lo + p.L, p.Nk);
+  int64_t lim[QB];  // last admissible key per query row
+#pragma unroll
+  for (int qi = 0; qi < QB; ++qi) {
+    const int64_t i = min(i0 + qi, p.Nq - 1);
+    lim[qi] = p.causal ? min(p.Nk - 1, i + p.qoff) : p.Nk - 1;
+  }
+  if (p.causal) {
+    int64_t top = lim[0];
+#pragma unroll
+    for (int qi = 1; qi < QB; ++qi) top = max(top, lim[qi]);
+    k_hi = min(k_hi, top + 1);
+  }
+
+  float qf[QB][8];
+#pragma unroll
+  for (int qi = 0; qi < QB; ++qi) {
+    const int64_t i = min(i0 + qi, p.Nq - 1);
+    const uint4 r = ld_stream(p.q + (bh * p.Nq + i) * D + 8 * sub);
+    unpack8(r, qf[qi]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qf[qi][e] *= p.sc_log2;
+  }
+
+  float m[QB], l[QB], o[QB][8];
+#pragma unroll
+  for (int qi = 0; qi < QB; ++qi) {
+    m[qi] = -INFINITY;
+    l[qi] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[qi][e] = 0.0f;
+  }
+
+  const uint16_t* kbase = p.k + bh * p.Nk * D + 8 * sub;
+  const uint16_t* vbase = p.v + bh * p.Nk * D + 8 * sub;
+  for (int64_t base = k_lo; base < k_hi; base += STEP) {
+    uint4 kr[U], vr[U];
+    int64_t key[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      key[u] = base + u * (kWarps * G) + warp * G + grp;
+      if (key[u] < k_hi) {
+        kr[u] = ld_stream(kbase + key[u] * D);
+        vr[u] = ld_stream(vbase + key[u] * D);
+      } else {
+        kr[u] = make_uint4(0u, 0u, 0u, 0u);
+        vr[u] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float sc[QB][U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float kf[8];
+      unpack8(kr[u], kf);
+#pragma unroll
+      for (int qi = 0; qi < QB; ++qi) {
+        float dot = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dot = fmaf(qf[qi][e], kf[e], dot);
+#pragma unroll
+        for (int off = 1; off < LPR; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        const bool live = key[u] < k_hi && key[u] <= lim[qi];
+        sc[qi][u] = live ? dot : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int qi = 0; qi < QB; ++qi) {
+      float mx = sc[qi][0];
+#pragma unroll
+      for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[qi][u]);
+      const float m_new = fmaxf(m[qi], mx);
+      if (m_new == -INFINITY) continue;  // nothing admissible yet
+      const float alpha = ex2_approx(m[qi] - m_new);
+      l[qi] *= alpha;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[qi][e] *= alpha;
+      m[qi] = m_new;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float pu = ex2_approx(sc[qi][u] - m_new);
+        l[qi] += pu;
+        float vf[8];
+        unpack8(vr[u], vf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[qi][e] = fmaf(pu, vf[e], o[qi][e]);
+      }
+    }
+  }
+
+  // Merge the lane groups of this warp (groups differ in lane / LPR).
+#pragma unroll
+  for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+    for (int qi = 0; qi < QB; ++qi) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[qi], off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l[qi], off);
+      float o2[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[qi][e], off);
+      merge_state(m[qi], l[qi], o[qi], m2, l2, o2);
+    }
+  }
+  if (grp == 0) {
+#pragma unroll
+    for (int qi = 0; qi < QB; ++qi) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm_o[warp][qi][8 * sub + e] = o[qi][e];
+      if (sub == 0) {
+        sm_m[warp][qi] = m[qi];
+        sm_l[warp][qi] = l[qi];
+      }
+    }
+  }
+  __syncthreads();
+
+  // Merge the warps and write the split's normalised output and LSE.
+  for (int idx = threadIdx.x; idx < QB * D; idx += kThreads) {
+    const int qi = idx / D, e = idx % D;
+    const int64_t i = i0 + qi;
+    if (i >= p.Nq) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][qi]);
+    float L = 0.0f, acc = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = ex2_approx(sm_m[w][qi] - M);
+        L = fmaf(sm_l[w][qi], f, L);
+        acc = fmaf(sm_o[w][qi][e], f, acc);
+      }
+    }
+    const bool empty = !(L > 0.0f);
+    const int64_t slot = (bh * p.S + s) * p.Nq + i;
+    p.o_part[slot * D + e] = empty ? 0.0f : acc / L;
+    if (e == 0) p.lse_part[slot] = empty ? -INFINITY : (M + log2f(L)) * kLn2;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o_part,
+                                                      const float* __restrict__ lse_part,
+                                                      uint16_t* __restrict__ o,
+                                                      float* __restrict__ lse, int64_t rows,
+                                                      int64_t Nq, int S) {
+  constexpr int E = D / 32;  // elements per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (row >= rows) return;
+  const int64_t bh = row / Nq, i = row % Nq;
+  const float* lp = lse_part + bh * S * Nq + i;  // split s at lp[s * Nq]
+
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) M = fmaxf(M, lp[static_cast<int64_t>(s) * Nq]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+  float W = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < S; ++s) {
+      const float w = ex2_approx((lp[static_cast<int64_t>(s) * Nq] - M) * kLog2e);
+      W += w;
+      const float* op = o_part + ((bh * S + s) * Nq + i) * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(op);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+        acc[2] = fmaf(w, x.z, acc[2]);
+        acc[3] = fmaf(w, x.w, acc[3]);
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(op);
+        acc[0] = fmaf(w, x.x, acc[0]);
+        acc[1] = fmaf(w, x.y, acc[1]);
+      }
+    }
+  }
+  const bool empty = !(W > 0.0f);
+  const float inv = empty ? 0.0f : 1.0f / W;
+  uint16_t* dst = o + row * D + lane * E;
+  if constexpr (E == 4) {
+    uint2 pk;
+    pk.x = empty ? 0u : pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    pk.y = empty ? 0u : pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = empty ? 0u : pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0) lse[row] = empty ? -INFINITY : M + logf(W);
+}
+
+template <int D, int QB, int U>
+cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
+  PartialParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.k = static_cast<const uint16_t*>(a.k);
+  p.v = static_cast<const uint16_t*>(a.v);
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.qoff = a.query_offset;
+  p.L = a.keys_per_split;
+  p.S = a.splits;
+  p.n_qb = static_cast<int>((a.Nq + QB - 1) / QB);
+  p.causal = a.causal;
+  p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  const int64_t blocks = a.BH * p.n_qb * a.splits;
+  splitkv_partial_kernel<D, QB, U><<<dim3(static_cast<unsigned>(blocks)), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_splitkv_partial(const SplitArgs& a, cudaStream_t stream) {
+  if (a.d == 64) {
+    if (a.Nq == 1) return launch_partial<64, 1, 4>(a, stream);
+    return launch_partial<64, 4, 2>(a, stream);
+  }
+  if (a.Nq == 1) return launch_partial<128, 1, 4>(a, stream);
+  return launch_partial<128, 4, 2>(a, stream);
+}
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, void* o, float* lse,
+                           int64_t BH, int64_t Nq, int d, int splits, cudaStream_t stream) {
+  const int64_t rows = BH * Nq;
+  const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+  if (d == 64)
+    combine_kernel<64><<<blocks, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o),
+                                                    lse, rows, Nq, splits);
+  else
+    combine_kernel<128><<<blocks, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o),
+                                                     lse, rows, Nq, splits);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

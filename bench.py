@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention forward on GB300.
+
+One step = one attn_fwd call (tcgen05 prefill kernel) on the long-prefill
+causal workload: B=2, H=32, Nq=Nk=8192, d=128, bf16, K x4 on 1% of key rows,
+inputs resident in device memory (Q+K+V = 403 MB, larger than the 129 MB L2,
+so no flush is needed between steps).  The line also carries the split-KV
+decode workload (B=16, H=32, Nq=1, Nk=32768, d=128) in GB/s, the other
+prefill workloads, an end-to-end figure through the C ABI with pinned host
+buffers, the roofline of the dominant kernel, and the CPU oracle timed on the
+host's cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one per GPU, launched by torchrun); the
+attention path needs no exchange between GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from attention_attn_fwd_07_gb300 import inputs as W  # noqa: E402
+
+METRIC = "attention fwd TFLOPS (prefill) / HBM GB/s (decode) at 1 GB300, % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TXT = os.path.join(ROOT, "profiles", "fwd_tcgen05_long_prefill_causal.md")
+KERNEL_SOURCES = ["fwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true", help="main workload only (profiling runs)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(w: W.Workload) -> float:
+    f = 4.0 * w.B * w.H * w.Nq * w.Nk * w.d
+    return f / 2 if w.causal else f
+
+
+def decode_bytes(w: W.Workload) -> int:
+    kv = 2 * w.B * w.H * w.Nk * w.d * 2
+    qo = 2 * w.B * w.H * w.Nq * w.d * 2
+    return kv + qo + w.B * w.H * w.Nq * 4
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "attention_attn_fwd_07_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    if not os.path.exists(PROFILE_TXT):
+        return None
+    txt = open(PROFILE_TXT).read()
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    tb = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    if not src or not tb or src.group(1) != kernel_source_hash():
+        return None
+    return int(tb.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        used = inside if len(inside) >= 3 else rows
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": float(np.median([r[1] for r in used])),
+                "sm_max_mhz": float(max(r[2] for r in used)),
+                "reasons": reasons, "samples": len(used),
+                "window": "timed region" if used is inside else "whole run (timed region too short)"}
+
+
+def event_time(fn, steps: int, stream) -> float:
+    """Average ms per call of fn over `steps` calls, CUDA events on `stream`."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def event_time_flushed(fn, steps: int, stream, scratch: torch.Tensor) -> float:
+    """Average ms per call with L2 flushed before each call: a buffer larger
+    than L2 is rewritten outside the timed events."""
+    total = 0.0
+    for _ in range(steps):
+        scratch.add_(1)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        fn()
+        end.record(stream)
+        end.synchronize()
+        total += start.elapsed_time(end)
+    return total / steps
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_sample(w: W.Workload, q, k, v, target_s: float):
+    """Time the oracle on evenly spaced rows of head 0, sized to ~target_s."""
+    import oracle
+    lib = oracle.load()
+    threads = oracle.default_threads()
+
+    def rows_flops(n):
+        rows = np.linspace(0, w.Nq - 1, n).round().astype(np.int64)
+        if w.causal:
+            fl = sum(4.0 * w.d * min(w.Nk, int(i) + 1) for i in rows)
+        else:
+            fl = 4.0 * w.d * w.Nk * n
+        return rows, fl
+
+    n = max(threads, 16)
+    rows, fl = rows_flops(n)
+    t = time.perf_counter()
+    oracle.attention(q, k, v, causal=w.causal, scale=w.scale, rows=rows, threads=threads, lib=lib)
+    dt = time.perf_counter() - t
+    n = int(min(w.Nq, max(n, n * target_s / max(dt, 1e-3))))
+    rows, fl = rows_flops(n)
+    t = time.perf_counter()
+    oracle.attention(q, k, v, causal=w.causal, scale=w.scale, rows=rows, threads=threads, lib=lib)
+    dt = time.perf_counter() - t
+    return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{n} evenly spaced query rows of head (0,0) of {w.name}; "
+                      f"{fl / 1e9:.2f} GFLOP in {dt:.2f} s (fp64, all host threads)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on bounded samples of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = W.LONG_PREFILL_CAUSAL
+    q, k, v = W.make_qkv(w)
+    import oracle
+    threads = oracle.default_threads()
+
+    def pick(n):
+        r = np.linspace(0, w.Nq - 1, n).round().astype(np.int64)
+        return r, sum(4.0 * w.d * (int(i) + 1) for i in r)
+
+    # Size one step to about one second of host work (calibrated once).
+    rows, fl = pick(4 * threads)
+    t = time.perf_counter()
+    oracle.attention(q, k, v, causal=True, scale=w.scale, rows=rows, threads=threads)
+    dt = max(time.perf_counter() - t, 1e-3)
+    rows, fl = pick(int(min(w.Nq, max(4 * threads, 4 * threads * 1.0 / dt))))
+    times = []
+    for step in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        oracle.attention(q, k, v, causal=True, scale=w.scale, rows=rows, threads=threads)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t)
+    ms = 1e3 * float(np.mean(times))
+    value = fl / (ms / 1e3) / 1e12
+    sample = (f"{len(rows)} evenly spaced query rows of head (0,0) per step "
+              f"({fl / 1e9:.3f} GFLOP, fp64)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": True, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU leg
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from attention_attn_fwd_07_gb300 import binding, build
+    build.build()
+    binding.load_library()
+    stream = torch.cuda.current_stream()
+    pk, pk_src = peaks()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    launches = 0
+
+    # ---- main workload: long prefill, causal
+    w = W.LONG_PREFILL_CAUSAL
+    q_h, k_h, v_h = W.make_qkv(w)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+
+    def step():
+        binding.attn_fwd(q, k, v, True, w.scale, o=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    t0 = time.time()
+    ms = event_time(step, args.steps, stream)
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    launches += args.steps
+    ms = max_over_ranks(ms)
+    flops = prefill_flops(w)
+    value = world * flops / (ms / 1e3) / 1e12
+    per_gpu = flops / (ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": per_gpu, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": per_gpu / pk["bf16_tflops"],
+            "peak_source": f"{pk_src} bf16 dense (burst: kernel timed back to back)",
+            "traffic": recorded_traffic(),
+            "algorithmic_flops_per_launch": flops}
+
+    # ---- end to end through the C ABI with pinned host buffers
+    q_p, k_p, v_p = (t.pin_memory() for t in (q_h, k_h, v_h))
+    o_p = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_p = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        binding.fwd_from_host(q_p, k_p, v_p, True, w.scale, q, k, v, o, lse, o_p, lse_p,
+                              stream=stream)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e2e_ms = max_over_ranks(event_time(e2e_step, e2e_steps, stream))
+    launches += e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p))
+    d2h = o_p.numel() * o_p.element_size() + lse_p.numel() * lse_p.element_size()
+    e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "path": "pinned host -> device copies, attn_fwd (C ABI), device -> pinned host copies "
+                   "of O and LSE, one stream"}
+    del q_p, k_p, v_p, o_p, lse_p
+
+    others = []
+    decode = None
+    if not args.quick:
+        # ---- the other prefill workloads
+        for wo in (W.LONG_PREFILL_NONCAUSAL, W.PREFILL):
+            if wo.Nq == w.Nq and wo.d == w.d:
+                qq, kk, vv, oo, ll = q, k, v, o, lse
+            else:
+                qq, kk, vv = (t.to(dev) for t in W.make_qkv(wo))
+                oo = torch.empty_like(qq)
+                ll = torch.empty((wo.B, wo.H, wo.Nq), dtype=torch.float32, device=dev)
+
+            def st(qq=qq, kk=kk, vv=vv, oo=oo, ll=ll, wo=wo):
+                binding.attn_fwd(qq, kk, vv, wo.causal, wo.scale, o=oo, lse=ll, stream=stream)
+
+            for _ in range(args.warmup):
+                st()
+            if wo.Nq >= 8192:
+                n = args.steps
+                m = max_over_ranks(event_time(st, n, stream))
+            else:
+                n = args.steps
+                scratch = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
+                m = max_over_ranks(event_time_flushed(st, n, stream, scratch))
+                del scratch
+            launches += n
+            tf = prefill_flops(wo) / (m / 1e3) / 1e12
+            others.append({"workload": wo.name, "metric": "TFLOPS", "value": world * tf,
+                           "ms_per_step": m, "frac_of_peak": tf / pk["bf16_tflops"],
+                           "l2": "inputs > L2" if wo.Nq >= 8192 else
+                                 "L2 flushed (256 MB rewrite) before each timed launch"})
+
+        # ---- decode (split-KV + combine), memory bound
+        wd = W.DECODE
+        qd, kd, vd = W.make_qkv(wd, device=dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
+        results = []
+        for S in wd.splits:
+            need = binding.attn_splitkv_workspace_bytes(wd.B, wd.H, 1, wd.d, S)
+            ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+
+            def sd(S=S, ws=ws):
+                binding.attn_fwd_splitkv(qd, kd, vd, False, wd.scale, S, workspace=ws, o=od,
+                                         lse=ld, stream=stream)
+
+            for _ in range(args.warmup):
+                sd()
+            n = max(10, args.steps // 4)
+            m = max_over_ranks(event_time(sd, n, stream))
+            launches += 2 * n
+            gbs = decode_bytes(wd) / (m / 1e3) / 1e9
+            results.append({"splits": S, "ms_per_step": m, "GB/s": gbs,
+                            "workspace_bytes": need})
+        best = max(results, key=lambda r: r["GB/s"])
+        decode = {"workload": wd.name, "metric": "HBM GB/s", "unit": "GB/s",
+                  "value": world * best["GB/s"], "ms_per_step": best["ms_per_step"],
+                  "splits": best["splits"], "per_split_count": results,
+                  "algorithmic_bytes_per_step": decode_bytes(wd),
+                  "roofline": {"bound": "hbm", "achieved": best["GB/s"], "peak": pk["hbm_gbs"],
+                               "unit": "GB/s", "frac": best["GB/s"] / pk["hbm_gbs"],
+                               "peak_source": f"{pk_src} copy bandwidth", "traffic": None},
+                  "l2": "inputs 8.6 GB > L2"}
+        del qd, kd, vd
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(w, q_h, k_h, v_h, target_s=10.0)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": True, "flops_convention": "4*B*H*Nq*Nk*d, halved for causal",
+                   "l2": "inputs (403 MB) larger than L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clocks, "decode": decode, "other_workloads": others,
+        "kernel_source_sha256_16": kernel_source_hash(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * Operation (all entry points): for every batch b, head h and query row i,
+ *
+ *   s_j  = scale * <q[b,h,i,:], k[b,h,j,:]>                 j = 0 .. Nk-1
+ *   s_j  = -inf  when causal and j > i + query_offset
+ *   o[b,h,i,:] = sum_j softmax(s)_j * v[b,h,j,:]
+ *   lse[b,h,i] = ln sum_j exp(s_j)                           (natural log)
+ *
+ * computed tile by tile with the online-softmax recurrence (running maximum
+ * m, normaliser l and unnormalised accumulator o, old state rescaled by
+ * exp(m - m_new)), so the Nq x Nk score matrix never reaches device memory.
+ * Definitions follow "GPU Engineering: Correctness, Throughput, and
+ * Attention": section 22.5 (the recurrence and its rescaling; causal masking
+ * before maxima and sums; fully masked rows need explicit semantics) and
+ * section 22.7 (the worked lab: scores scaled after the dot product; key j
+ * excluded when j > i + query_offset; a row with no admissible key has output
+ * 0 and log-normaliser -inf; the log-normaliser is m + ln(l)).  The split-KV
+ * merge is the same rescaling applied to whole partial states.
+ *
+ * Conventions shared by every entry point
+ *  - Q, K, V, O are bfloat16, contiguous [B][H][N][d] (N = Nq for Q and O,
+ *    Nk for K and V); each (b,h) slice is a row-major [N][d] matrix.  LSE is
+ *    float32 [B][H][Nq].  All tensor pointers are DEVICE pointers owned by the
+ *    caller; the library keeps no pointer after a call returns.
+ *  - Q, K, V, O and workspaces must be 16-byte aligned; LSE 4-byte aligned.
+ *  - d must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).
+ *  - B, H, Nq, Nk >= 1 (ATTN_ERR_INVALID otherwise); scale must be finite
+ *    and > 0.  Inputs must be finite (a documented precondition, not checked:
+ *    a check would cost a full pass over the data).
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  The
+ *    return value reports argument validation and launch errors only.  Device
+ *    side wait timeouts are reported through attn_get_device_status().
+ *  - Rows >= Nq of O/LSE and any byte outside [B,H,Nq,d] / [B,H,Nq] are never
+ *    written.  A fully masked row is written as O = +0.0, LSE = -inf.
+ *  - No entry point allocates device memory; the split-KV workspace is the
+ *    caller's.  Entry points are thread-safe.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point (0 = success). */
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID = -1,        /* null pointer, size < 1, bad scale, ...   */
+  ATTN_ERR_UNSUPPORTED = -2,    /* head dim other than 64/128, size limits  */
+  ATTN_ERR_ALIGN = -3,          /* pointer misaligned                       */
+  ATTN_ERR_WORKSPACE = -4,      /* split-KV workspace missing or too small  */
+  ATTN_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed        */
+  ATTN_ERR_DEVICE_TIMEOUT = -6  /* a kernel gave up a bounded wait          */
+} attn_status;
+
+/* attn_params.flags */
+enum {
+  /* Accept query_offset < 0 so that leading rows see no key at all (fully
+   * masked rows).  The pages require query_offset >= 0; this flag exists to
+   * exercise the fully-masked-row policy. */
+  ATTN_FLAG_ALLOW_NEG_OFFSET = 1u << 0,
+  /* Fault injection for the timeout path: the prefill kernel's loader skips
+   * one K/V tile load so that its consumers' bounded waits expire.  The
+   * kernel then records ATTN_ERR_DEVICE_TIMEOUT and returns; no GPU fault. */
+  ATTN_FLAG_TEST_SKIP_LOAD = 1u << 1
+};
+
+/* Full argument set of the prefill entry point (attn_fwd_ex) and of the
+ * split-KV entry point (attn_fwd_splitkv_ex). */
+typedef struct attn_params {
+  const void* q;          /* bf16 [B][H][Nq][d], device                    */
+  const void* k;          /* bf16 [B][H][Nk][d], device                    */
+  const void* v;          /* bf16 [B][H][Nk][d], device                    */
+  void* o;                /* bf16 [B][H][Nq][d], device, written           */
+  float* lse;             /* f32  [B][H][Nq],    device, written           */
+  int64_t B, H, Nq, Nk, d;
+  int causal;             /* nonzero: key j visible to row i iff j <= i + query_offset */
+  float scale;            /* multiplies q.k before masking; finite, > 0    */
+  int64_t query_offset;   /* absolute position of query row 0; >= 0        */
+  int* dev_status;        /* optional device int; timeouts are OR-ed into it
+                             as bit 0; NULL = the library's own status word */
+  uint32_t flags;         /* ATTN_FLAG_* */
+  uint32_t wait_timeout_us; /* per-wait device timeout; 0 = 1,000,000 us   */
+} attn_params;
+
+/*
+ * Prefill / general forward: O and LSE for all rows, query_offset = 0.
+ * tcgen05 (TMEM accumulators) + TMA kernel; any Nq, Nk >= 1.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+             int causal, float scale, cudaStream_t stream);
+
+/* attn_fwd with every option (query_offset, flags, status word, timeout). */
+int attn_fwd_ex(const attn_params* p, cudaStream_t stream);
+
+/*
+ * Bytes of workspace attn_fwd_splitkv needs: float32 partial outputs
+ * [B][H][num_splits][Nq][d] followed (at a 256-byte boundary) by float32
+ * partial log-sum-exps [B][H][num_splits][Nq].  Returns 0 for invalid sizes.
+ */
+size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
+                                    int num_splits);
+
+/*
+ * Split-KV forward for short queries (decode): the keys of every (b,h) are
+ * cut into num_splits contiguous ranges of L = ceil(Nk/num_splits) keys
+ * rounded up to a multiple of 128 (trailing ranges may be empty); each range
+ * yields a partial (normalised o, lse) in `workspace`, then attn_combine
+ * merges them into O and LSE.  1 <= num_splits <= 256.  Two launches on
+ * `stream`; `workspace` (device, 16-byte aligned, caller-owned) must hold
+ * attn_splitkv_workspace_bytes(...) bytes (ATTN_ERR_WORKSPACE otherwise).
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                     int causal, float scale, int num_splits, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream);
+
+/* attn_fwd_splitkv with query_offset and flags from `p` (dev_status,
+ * wait_timeout_us and ATTN_FLAG_TEST_SKIP_LOAD do not apply: the split-KV
+ * kernels have no inter-thread waits beyond block barriers). */
+int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Log-sum-exp merge of num_splits partial states per row:
+ *   M = max_s lse_part[s];  if M = -inf: O = +0.0, LSE = -inf;  otherwise
+ *   w_s = exp(lse_part[s] - M),  LSE = M + ln sum_s w_s,
+ *   O = sum_s (w_s / sum_s w_s) * o_part[s]   (rounded to bf16).
+ * o_part: f32 [B][H][num_splits][Nq][d], lse_part: f32 [B][H][num_splits][Nq]
+ * (device, 16-byte aligned); o: bf16 [B][H][Nq][d]; lse: f32 [B][H][Nq].
+ * 1 <= num_splits <= 256.
+ */
+int attn_combine(const float* o_part, const float* lse_part, void* o, float* lse,
+                 int64_t B, int64_t H, int64_t Nq, int64_t d, int num_splits,
+                 cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, copies the library's own device status word (the
+ * one kernels use when attn_params.dev_status is NULL) on the current device
+ * to *dev_status_host, and clears it.  Bit 0 set = some kernel gave up a
+ * bounded wait (ATTN_ERR_DEVICE_TIMEOUT); its outputs are undefined.
+ */
+int attn_get_device_status(int* dev_status_host, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -1,0 +1,143 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every entry
+point that include/attn.h declares, and rejects bad arguments with the
+documented status codes before touching CUDA."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+from attention_attn_fwd_07_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+# Fake, never-dereferenced device addresses (validation rejects before use).
+A16 = 0x10000
+MIS = 0x10008
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(attn_\w+)\s*\(", text,
+                                 flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_entry_points()
+    assert set(binding.EXPORTED) <= set(names), names
+    assert "attn_fwd" in names and "attn_fwd_splitkv" in names and "attn_combine" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(attn_\w+)$", out, flags=re.M))
+    for name in declared_entry_points():
+        assert name in exported, f"{name} declared in attn.h but not exported"
+        assert hasattr(lib, name)
+
+
+def call_fwd(lib, q=A16, k=A16, v=A16, o=A16, lse=A16, B=1, H=1, Nq=8, Nk=8, d=64, causal=0,
+             scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), binding.ATTN_ERR_INVALID),
+    (dict(lse=0), binding.ATTN_ERR_INVALID),
+    (dict(B=0), binding.ATTN_ERR_INVALID),
+    (dict(H=-1), binding.ATTN_ERR_INVALID),
+    (dict(Nq=0), binding.ATTN_ERR_INVALID),
+    (dict(Nk=0), binding.ATTN_ERR_INVALID),
+    (dict(scale=float("nan")), binding.ATTN_ERR_INVALID),
+    (dict(scale=float("inf")), binding.ATTN_ERR_INVALID),
+    (dict(scale=0.0), binding.ATTN_ERR_INVALID),
+    (dict(scale=-0.5), binding.ATTN_ERR_INVALID),
+    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(Nq=1 << 31), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(B=1 << 20, H=1 << 12), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(q=MIS), binding.ATTN_ERR_ALIGN),
+    (dict(o=MIS + 4), binding.ATTN_ERR_ALIGN),
+    (dict(lse=A16 + 2), binding.ATTN_ERR_ALIGN),
+])
+def test_fwd_rejects(lib, kw, code):
+    assert call_fwd(lib, **kw) == code
+
+
+def _params(**kw):
+    base = dict(q=A16, k=A16, v=A16, o=A16, lse=A16, B=1, H=1, Nq=8, Nk=8, d=64, causal=1,
+                scale=0.125, query_offset=0, dev_status=None, flags=0, wait_timeout_us=0)
+    base.update(kw)
+    return binding.attn_params(**base)
+
+
+def test_negative_offset_needs_flag(lib):
+    p = _params(query_offset=-3)
+    assert lib.attn_fwd_ex(ctypes.byref(p), None) == binding.ATTN_ERR_INVALID
+    p = _params(query_offset=1 << 41, flags=binding.ATTN_FLAG_ALLOW_NEG_OFFSET)
+    assert lib.attn_fwd_ex(ctypes.byref(p), None) == binding.ATTN_ERR_INVALID
+    assert lib.attn_fwd_ex(None, None) == binding.ATTN_ERR_INVALID
+
+
+def test_workspace_bytes(lib):
+    f = lib.attn_splitkv_workspace_bytes
+    rows = 16 * 32 * 64 * 1
+    assert f(16, 32, 1, 128, 64) == math.ceil(rows * 128 * 4 / 256) * 256 + rows * 4
+    rows = 3 * 4 * 3 * 1003
+    assert f(3, 4, 1003, 64, 3) == math.ceil(rows * 64 * 4 / 256) * 256 + rows * 4
+    for bad in [(0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, 0), (1, 1, 1, 64, 257),
+                (1, 1, 0, 64, 1)]:
+        assert f(*bad) == 0
+
+
+def test_splitkv_rejects(lib):
+    need = lib.attn_splitkv_workspace_bytes(1, 1, 8, 64, 4)
+    sk = lib.attn_fwd_splitkv
+    args = [A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, 0, 0.125]
+    assert sk(*args, 0, A16, need, None) == binding.ATTN_ERR_INVALID
+    assert sk(*args, 257, A16, need, None) == binding.ATTN_ERR_INVALID
+    assert sk(*args, 4, 0, need, None) == binding.ATTN_ERR_WORKSPACE
+    assert sk(*args, 4, A16, need - 1, None) == binding.ATTN_ERR_WORKSPACE
+    assert sk(*args, 4, MIS, need, None) == binding.ATTN_ERR_ALIGN
+    bad = list(args)
+    bad[9] = 80
+    assert sk(*bad, 4, A16, need, None) == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_combine_rejects(lib):
+    c = lib.attn_combine
+    assert c(0, A16, A16, A16, 1, 1, 1, 64, 4, None) == binding.ATTN_ERR_INVALID
+    assert c(A16, A16, A16, A16, 1, 1, 1, 64, 0, None) == binding.ATTN_ERR_INVALID
+    assert c(A16, A16, A16, A16, 1, 1, 1, 32, 4, None) == binding.ATTN_ERR_UNSUPPORTED
+    assert c(MIS, A16, A16, A16, 1, 1, 1, 64, 4, None) == binding.ATTN_ERR_ALIGN
+
+
+def test_status_strings(lib):
+    for code in range(-6, 1):
+        s = lib.attn_status_string(code).decode()
+        assert s.startswith("ATTN_")
+    assert "unknown" in lib.attn_status_string(42).decode()
+    assert lib.attn_get_device_status(None, None) == binding.ATTN_ERR_INVALID
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful on a host without a GPU (fake pointers)")
+    assert call_fwd(lib) == binding.ATTN_ERR_CUDA
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.load_library(str(tmp_path / "nope.so"))
