@@ -1,0 +1,113 @@
+// noalloc.cu -- attn_fwd_splitkv_noalloc: the split-KV forward with its
+// scratch (the per-split partial outputs and log-sum-exps) in a fixed
+// device array owned by this library, for callers that cannot allocate
+// device memory themselves.
+//
+// Who needs this: a caller whose device memory is entirely planned and
+// owned by an outer arena (for example a serving process that reserves all
+// memory at start-up and forbids any further cudaMalloc), a plug-in running
+// inside a host program that exposes no allocator, or a latency-critical
+// loop where cudaMalloc/cudaFree may synchronise the device.  Such callers
+// still pass their own q, k, v, o and lse; only the scratch moves here.
+//
+// The array below is ATTN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that
+// loads this library, held until the process exits.  Every call shares it
+// and it keeps the previous call's contents.  Nothing in it needs clearing:
+// the partial kernel writes every slot the combine kernel reads in the same
+// call (an empty split writes o = 0, lse = -inf).  Calls that overlap on the
+// GPU (different streams, or different host threads on one device) race on
+// the array and give undefined results; serialise them.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "internal.cuh"
+
+namespace attn {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};  // device address of the array, per device
+
+// Once per device, with that device current: translate the array's host-side
+// name into its device address.  The name itself is only a host stand-in and
+// must never be passed to a kernel.
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return ATTN_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                        float* lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                                        int64_t d, int causal, float scale, int num_splits,
+                                        cudaStream_t stream) {
+  // The same argument rules as attn_fwd_splitkv.
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_INVALID;
+  if (!(scale > 0.0f) || !(scale < INFINITY)) return ATTN_ERR_INVALID;
+  if (num_splits < 1 || num_splits > 256) return ATTN_ERR_INVALID;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  const int64_t kMaxDim = (int64_t{1} << 31) - 1;
+  if (B > kMaxDim || H > kMaxDim || B * H > kMaxDim || Nq > kMaxDim || Nk > kMaxDim)
+    return ATTN_ERR_UNSUPPORTED;
+  const uintptr_t a16 = 15;
+  if ((reinterpret_cast<uintptr_t>(q) & a16) || (reinterpret_cast<uintptr_t>(k) & a16) ||
+      (reinterpret_cast<uintptr_t>(v) & a16) || (reinterpret_cast<uintptr_t>(o) & a16) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3))
+    return ATTN_ERR_ALIGN;
+  // Sizes beyond the fixed array are refused before anything is launched.
+  const size_t need = attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
+  if (need == 0) return ATTN_ERR_UNSUPPORTED;
+  if (need > static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES)) return ATTN_ERR_WORKSPACE;
+  const int64_t BH = B * H;
+  const int64_t qb = Nq == 1 ? 1 : 4;
+  if (BH * ((Nq + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
+
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != ATTN_OK) return rc;
+
+  const size_t rows = static_cast<size_t>(BH) * num_splits * static_cast<size_t>(Nq);
+  SplitArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o_part = static_cast<float*>(scratch);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                        align256(rows * static_cast<size_t>(d) * 4));
+  a.BH = BH;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.query_offset = 0;
+  const int64_t per = (Nk + num_splits - 1) / num_splits;
+  a.keys_per_split = (per + 127) / 128 * 128;
+  a.d = static_cast<int>(d);
+  a.splits = num_splits;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (launch_combine(a.o_part, a.lse_part, o, lse, BH, Nq, a.d, num_splits, stream) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}

@@ -142,6 +142,33 @@ int attn_combine(const float* o_part, const float* lse_part, void* o, float* lse
                  int64_t B, int64_t H, int64_t Nq, int64_t d, int num_splits,
                  cudaStream_t stream);
 
+/* Size of the library-owned scratch array used by attn_fwd_splitkv_noalloc
+ * (one per GPU that loads the library, kept until the process exits). */
+#define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * attn_fwd_splitkv without a caller-provided workspace, for callers that
+ * cannot allocate device memory: code whose device memory is all planned by
+ * an outer arena that forbids further allocation, plug-ins whose host
+ * program offers no allocator, or latency-critical loops that cannot afford
+ * the device synchronisation cudaMalloc/cudaFree may cause.  The pages have
+ * no counterpart to this entry point; it is a deployment convenience.
+ *
+ * Same arguments, results and rules as attn_fwd_splitkv (query_offset 0).
+ * The scratch lives in a fixed device array of ATTN_NOALLOC_SCRATCH_BYTES
+ * inside the library; calls whose attn_splitkv_workspace_bytes(...) exceed it
+ * return ATTN_ERR_WORKSPACE before launching anything.  Nothing is allocated.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the array: calls that overlap on the GPU (other streams or
+ * host threads on the same device) race and must be serialised by the
+ * caller.  The array keeps the previous call's contents; no call needs it
+ * cleared.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                             int causal, float scale, int num_splits, cudaStream_t stream);
+
 /*
  * Synchronises `stream`, copies the library's own device status word (the
  * one kernels use when attn_params.dev_status is NULL) on the current device

@@ -1,0 +1,74 @@
+"""attn_fwd_splitkv_noalloc against attn_fwd_splitkv, through the C ABI.
+
+The allocation-free entry point exists for callers that cannot allocate
+device memory: code whose device memory is all planned by an outer arena that
+refuses further allocation, plug-ins whose host program exposes no
+allocator, and latency-critical loops that cannot afford the device
+synchronisation cudaMalloc/cudaFree may cause.  It keeps the split-KV
+scratch in a fixed 32 MiB array inside the library instead of a caller
+workspace.  Here it must give the same O and LSE as the workspace entry point
+(within the parity tolerances) on two different problems called one after
+the other, and must refuse a problem whose scratch exceeds the array.
+
+This file is named to be collected last.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from attention_attn_fwd_07_gb300 import binding, build
+from attention_attn_fwd_07_gb300 import inputs as W
+from tests.parity_util import LSE_TOL, O_TOL
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+SCRATCH_BYTES = 32 << 20  # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h
+
+
+def _entry(lib):
+    f = lib.attn_fwd_splitkv_noalloc
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
+                  ctypes.c_int, vp]
+    f.restype = ctypes.c_int
+    return f
+
+
+def _call(f, q, k, v, o, lse, causal, scale, splits):
+    B, H, Nq, d = q.shape
+    return f(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq,
+             k.shape[2], d, int(causal), float(scale), int(splits),
+             torch.cuda.current_stream().cuda_stream)
+
+
+def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    f = _entry(binding.load_library())
+    cases = [(W.Workload("decode-like", 2, 8, 1, 5000, 128, False, 501), 8),
+             (W.Workload("short causal queries", 3, 2, 37, 777, 64, True, 502), 5)]
+    for w, splits in cases:
+        q, k, v = (t.to(DEV) for t in W.make_qkv(w))
+        o_ref, lse_ref = binding.attn_fwd_splitkv(q, k, v, w.causal, w.scale, splits)
+        o = torch.full_like(o_ref, float("nan"))
+        lse = torch.full_like(lse_ref, float("nan"))
+        assert _call(f, q, k, v, o, lse, w.causal, w.scale, splits) == binding.ATTN_OK
+        torch.cuda.synchronize()
+        assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+        assert (o.float() - o_ref.float()).abs().max().item() <= O_TOL, w.name
+        assert (lse - lse_ref).abs().max().item() <= LSE_TOL, w.name
+
+
+def test_noalloc_refuses_scratch_beyond_its_array():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    f = _entry(binding.load_library())
+    B, H, d, splits = 16, 32, 128, 256
+    assert binding.attn_splitkv_workspace_bytes(B, H, 1, d, splits) > SCRATCH_BYTES
+    q = torch.zeros((B, H, 1, d), dtype=torch.bfloat16, device=DEV)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((B, H, 1), dtype=torch.float32, device=DEV)
+    assert _call(f, q, q, q, o, lse, False, 0.125, splits) == binding.ATTN_ERR_WORKSPACE
