@@ -342,15 +342,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = (c > rel) ? -INFINITY : s[c];
       }
+      // Row maximum: eight independent 16-element chains of 3-input maxima.
       float mx[8];
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
-        mx[g] = s[g];
+        mx[g] = fmaxf(s[16 * g], s[16 * g + 1]);
 #pragma unroll
-        for (int c = g + 8; c < 128; c += 8) mx[g] = fmaxf(mx[g], s[c]);
+        for (int c = 2; c < 16; c += 2) mx[g] = fmax3f(mx[g], s[16 * g + c], s[16 * g + c + 1]);
       }
-      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                                fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m_run, tmax * p.sc_log2);
       m_run = m_new;
       float alpha = 1.0f;
@@ -362,17 +363,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = m_new;
       }
       const float neg_ref = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+      // p = 2^(s * scale * log2 e - m_ref), two lanes per instruction; the
+      // row sum uses four independent packed accumulators.
+      const uint64_t scale2 = f2_pack(p.sc_log2, p.sc_log2);
+      const uint64_t bias2 = f2_pack(neg_ref, neg_ref);
+      uint64_t acc2[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc2[i] = 0ull;
       uint32_t pk[64];
-      float sum0 = 0.0f, sum1 = 0.0f;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(s[2 * c], p.sc_log2, neg_ref));
-        const float p1 = ex2_approx(fmaf(s[2 * c + 1], p.sc_log2, neg_ref));
-        sum0 += p0;
-        sum1 += p1;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, bias2), x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
         pk[c] = pack_bf16x2(p0, p1);
       }
-      l += sum0 + sum1;
+      float sum_lo, sum_hi;
+      f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
+      l += sum_lo + sum_hi;
       tmem_st_x64(tS, pk);
       if (__any_sync(0xffffffffu, rescale) && j > 0) {
 #pragma unroll 1
