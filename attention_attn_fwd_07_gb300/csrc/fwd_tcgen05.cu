@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kBarQ), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::kBarS + x), 1);
-      mbar_init(bar(C::kBarP + x), 128);
+      mbar_init(bar(C::kBarP + x), 4);  // one arrival per softmax warp
       mbar_init(bar(C::kBarO + x), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
@@ -396,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::kBarP + x));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarP + x));
     }
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, wait(bar(C::kBarO + x), 0));
