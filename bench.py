@@ -40,6 +40,8 @@ METRIC = "attention fwd TFLOPS (prefill) / HBM GB/s (decode) at 1 GB300, % of ro
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_TXT = os.path.join(ROOT, "profiles", "fwd_tcgen05_long_prefill_causal.md")
 KERNEL_SOURCES = ["fwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
+DECODE_PROFILE_TXT = os.path.join(ROOT, "profiles", "splitkv_decode.md")
+DECODE_SOURCES = ["splitkv.cu", "ptx.cuh", "internal.cuh"]
 
 
 def parse_args():
@@ -50,6 +52,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true", help="main workload only (profiling runs)")
+    ap.add_argument("--decode-profile-batch", type=int, default=0,
+                    help="run only the split-KV decode workload with this batch size "
+                         "(smaller cases for ncu captures) and print its GB/s")
     return ap.parse_args()
 
 
@@ -74,23 +79,23 @@ def decode_bytes(w: W.Workload) -> int:
     return kv + qo + w.B * w.H * w.Nq * 4
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "attention_attn_fwd_07_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    if not os.path.exists(PROFILE_TXT):
+def recorded_traffic(path=PROFILE_TXT, sources=KERNEL_SOURCES):
+    """DRAM bytes per launch (full-size workload) from a committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
+    if not os.path.exists(path):
         return None
-    txt = open(PROFILE_TXT).read()
+    txt = open(path).read()
     src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
     tb = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
-    if not src or not tb or src.group(1) != kernel_source_hash():
+    if not src or not tb or src.group(1) != kernel_source_hash(sources):
         return None
     return int(tb.group(1))
 
@@ -183,32 +188,36 @@ def event_time_flushed(fn, steps: int, stream, scratch: torch.Tensor) -> float:
 
 # ------------------------------------------------------------------ CPU oracle legs
 def oracle_sample(w: W.Workload, q, k, v, target_s: float):
-    """Time the oracle on evenly spaced rows of head 0, sized to ~target_s."""
+    """Time the oracle on a bounded sample of the workload's query rows.
+
+    The sample is every query row of the first few (b, h) heads, as many
+    heads as take about ``target_s`` seconds on all host threads (calibrated
+    on a small sample first); FLOPs are counted per row (4*d*visible keys).
+    """
     import oracle
     lib = oracle.load()
     threads = oracle.default_threads()
+    BH = w.B * w.H
 
-    def rows_flops(n):
-        rows = np.linspace(0, w.Nq - 1, n).round().astype(np.int64)
-        if w.causal:
-            fl = sum(4.0 * w.d * min(w.Nk, int(i) + 1) for i in rows)
-        else:
-            fl = 4.0 * w.d * w.Nk * n
-        return rows, fl
+    def rows_flops(n_rows):
+        flat = np.arange(n_rows, dtype=np.int64)
+        i = flat % w.Nq
+        keys = np.minimum(w.Nk, i + 1) if w.causal else np.full_like(i, w.Nk)
+        return flat, float(4.0 * w.d * keys.sum())
 
-    n = max(threads, 16)
-    rows, fl = rows_flops(n)
-    t = time.perf_counter()
-    oracle.attention(q, k, v, causal=w.causal, scale=w.scale, rows=rows, threads=threads, lib=lib)
-    dt = time.perf_counter() - t
-    n = int(min(w.Nq, max(n, n * target_s / max(dt, 1e-3))))
-    rows, fl = rows_flops(n)
-    t = time.perf_counter()
-    oracle.attention(q, k, v, causal=w.causal, scale=w.scale, rows=rows, threads=threads, lib=lib)
-    dt = time.perf_counter() - t
+    heads = 1
+    while True:
+        rows, fl = rows_flops(heads * w.Nq)
+        t = time.perf_counter()
+        oracle.attention(q, k, v, causal=w.causal, scale=w.scale, rows=rows, threads=threads,
+                         lib=lib)
+        dt = time.perf_counter() - t
+        if dt >= 0.5 * target_s or heads == BH:
+            break
+        heads = int(min(BH, max(heads + 1, round(heads * target_s / max(dt, 1e-3)))))
     return {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-            "sample": f"{n} evenly spaced query rows of head (0,0) of {w.name}; "
-                      f"{fl / 1e9:.2f} GFLOP in {dt:.2f} s (fp64, all host threads)"}
+            "sample": f"all {w.Nq} query rows of the first {heads} of {BH} (b,h) heads of "
+                      f"{w.name}; {fl / 1e9:.1f} GFLOP in {dt:.1f} s (fp64, all host threads)"}
 
 
 def run_reference(args):
@@ -291,6 +300,29 @@ def main():
         return float(t.item())
 
     launches = 0
+
+    if args.decode_profile_batch > 0:
+        # Decode only, smaller batch: the case the ncu captures run on.
+        wd = W.Workload(W.DECODE.name.replace("B16", f"B{args.decode_profile_batch}"),
+                        args.decode_profile_batch, W.DECODE.H, 1, W.DECODE.Nk, W.DECODE.d,
+                        False, W.DECODE.seed)
+        qd, kd, vd = W.make_qkv(wd, device=dev)
+        od = torch.empty_like(qd)
+        ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
+        S = 16
+        ws = torch.empty((binding.attn_splitkv_workspace_bytes(wd.B, wd.H, 1, wd.d, S),),
+                         dtype=torch.uint8, device=dev)
+
+        def sd():
+            binding.attn_fwd_splitkv(qd, kd, vd, False, wd.scale, S, workspace=ws, o=od, lse=ld,
+                                     stream=stream)
+
+        for _ in range(args.warmup):
+            sd()
+        m = event_time(sd, args.steps, stream)
+        print(json.dumps({"workload": wd.name, "splits": S, "ms_per_step": m,
+                          "GB/s": decode_bytes(wd) / (m / 1e3) / 1e9}), flush=True)
+        return 0
 
     # ---- main workload: long prefill, causal
     w = W.LONG_PREFILL_CAUSAL
@@ -407,7 +439,8 @@ def main():
                   "algorithmic_bytes_per_step": decode_bytes(wd),
                   "roofline": {"bound": "hbm", "achieved": best["GB/s"], "peak": pk["hbm_gbs"],
                                "unit": "GB/s", "frac": best["GB/s"] / pk["hbm_gbs"],
-                               "peak_source": f"{pk_src} copy bandwidth", "traffic": None},
+                               "peak_source": f"{pk_src} copy bandwidth",
+                               "traffic": recorded_traffic(DECODE_PROFILE_TXT, DECODE_SOURCES)},
                   "l2": "inputs 8.6 GB > L2"}
         del qd, kd, vd
 
