@@ -70,7 +70,7 @@ def _declare(lib) -> None:
     f = lib.oracle_attention
     f.restype = ctypes.c_int
     i64, vp = ctypes.c_int64, ctypes.c_void_p
-    f.argtypes = [vp, vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64,
+    f.argtypes = [vp, vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i64,
                   ctypes.c_int, i64, ctypes.c_double, i64, i64, vp, i64, vp,
                   vp, ctypes.c_int]
     lib.oracle_plant.restype = ctypes.c_int
@@ -109,6 +109,9 @@ def attention(q, k, v, *, causal: bool, scale: float, query_offset: int = 0,
               threads: int | None = None, lib=None):
     """Dense fp64 softmax attention over 4-D [B, H, N, dim] inputs.
 
+    K and V may have fewer heads than Q (grouped K/V heads): query head h
+    reads K/V head h // (H // Hkv).
+
     Returns ``(o, lse)`` as float64 numpy arrays.  With ``rows`` = None, o has
     shape [B, H, Nq, dv] and lse [B, H, Nq]; with ``rows`` (flattened indices
     (b*H + h)*Nq + i) they have shapes [len(rows), dv] and [len(rows)].
@@ -123,8 +126,8 @@ def attention(q, k, v, *, causal: bool, scale: float, query_offset: int = 0,
     if qa.ndim != 4 or ka.ndim != 4 or va.ndim != 4:
         raise ValueError("expected [B, H, N, dim] inputs")
     B, H, Nq, d = qa.shape
-    Bk, Hk, Nk, dk = ka.shape
-    if (Bk, Hk, dk) != (B, H, d) or va.shape[:3] != (B, H, Nk):
+    Bk, Hkv, Nk, dk = ka.shape
+    if (Bk, dk) != (B, d) or va.shape[:3] != (B, Hkv, Nk) or Hkv < 1 or H % Hkv != 0:
         raise ValueError("incompatible q, k, v shapes")
     dv = va.shape[3]
     lo, hi = key_range if key_range is not None else (0, Nk)
@@ -139,7 +142,7 @@ def attention(q, k, v, *, causal: bool, scale: float, query_offset: int = 0,
     o = np.empty((n_out, dv), dtype=np.float64)
     lse = np.empty((n_out,), dtype=np.float64)
     rc = lib.oracle_attention(
-        qa.ctypes.data, ka.ctypes.data, va.ctypes.data, qe, B, H, Nq, Nk, d, dv,
+        qa.ctypes.data, ka.ctypes.data, va.ctypes.data, qe, B, H, Hkv, Nq, Nk, d, dv,
         int(bool(causal)), int(query_offset), float(scale), int(lo), int(hi),
         rows_p, n_out if rows_a is not None else 0, o.ctypes.data,
         lse.ctypes.data, int(threads or default_threads()))

@@ -25,6 +25,11 @@
  *                  o[i][c] = sum_j w_j * v[j][c] / Z
  *                  lse[i]  = M + log(Z)              (natural logarithm)
  *
+ * Grouped K/V heads (GQA/MQA, named among FlashAttention's production
+ * features in "GPU Kernels: CUDA, HIP & Triton", section 7.6): K and V have
+ * Hkv heads; query head h of batch b reads K/V head b*Hkv + h / (H / Hkv).
+ * Hkv = H is ordinary multi-head attention.
+ *
  * Inputs are either IEEE doubles or bfloat16 bit patterns; a bfloat16 value
  * is widened exactly (its 16 bits are the top half of an IEEE single).
  * The key range [key_lo, key_hi) defaults to every key; a narrower range is
@@ -51,7 +56,7 @@ enum { ORACLE_F64 = 0, ORACLE_BF16 = 1 };
 typedef struct {
   const void *q, *k, *v;
   int elem;
-  int64_t B, H, Nq, Nk, d, dv;
+  int64_t B, H, Hkv, Nq, Nk, d, dv;
   int causal;
   int64_t query_offset;
   double scale;
@@ -76,7 +81,12 @@ static void one_row(const job_t *J, int64_t flat_row, double *s, double *o_out,
   const int64_t bh = flat_row / J->Nq;
   const int64_t i = flat_row % J->Nq;
   const int64_t q_base = flat_row * J->d;
-  const int64_t kv_head = bh * J->Nk;
+  const int64_t b = bh / J->H, h = bh % J->H;
+#if ORACLE_PLANT == 7 /* grouped heads mapped round-robin instead of in blocks */
+  const int64_t kv_head = (b * J->Hkv + h % J->Hkv) * J->Nk;
+#else
+  const int64_t kv_head = (b * J->Hkv + h / (J->H / J->Hkv)) * J->Nk;
+#endif
 
   double M = -INFINITY;
   for (int64_t j = J->key_lo; j < J->key_hi; ++j) {
@@ -146,17 +156,19 @@ static void *worker(void *arg) {
 
 /*
  * Returns 0 on success, -1 on invalid arguments, -2 on allocation failure.
- * q: [B][H][Nq][d], k: [B][H][Nk][d], v: [B][H][Nk][dv] (contiguous).
+ * q: [B][H][Nq][d], k: [B][Hkv][Nk][d], v: [B][Hkv][Nk][dv] (contiguous);
+ * H must be a multiple of Hkv.
  * o: [n_out][dv], lse: [n_out] where n_out = n_rows if rows != NULL else B*H*Nq.
  */
 int oracle_attention(const void *q, const void *k, const void *v, int elem,
-                     int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                     int64_t B, int64_t H, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d,
                      int64_t dv, int causal, int64_t query_offset, double scale,
                      int64_t key_lo, int64_t key_hi, const int64_t *rows,
                      int64_t n_rows, double *o, double *lse, int n_threads) {
   if (!q || !k || !v || !o || !lse) return -1;
   if (elem != ORACLE_F64 && elem != ORACLE_BF16) return -1;
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || dv < 1) return -1;
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0) return -1;
   if (key_lo < 0 || key_hi > Nk || key_lo > key_hi) return -1;
   if (!isfinite(scale)) return -1;
   const int64_t total_rows = B * H * Nq;
@@ -169,7 +181,7 @@ int oracle_attention(const void *q, const void *k, const void *v, int elem,
   if (n_threads > 256) n_threads = 256;
   if (n_out < n_threads) n_threads = n_out > 0 ? (int)n_out : 1;
 
-  job_t base = {q, k, v, elem, B, H, Nq, Nk, d, dv, causal, query_offset,
+  job_t base = {q, k, v, elem, B, H, Hkv, Nq, Nk, d, dv, causal, query_offset,
                 scale, key_lo, key_hi, rows, n_rows, o, lse, 0, 0};
   job_t jobs[256];
   pthread_t tids[256];

@@ -309,4 +309,21 @@ def pin_split_merge(lib):
             _close(lse, full[1], 1e-12, f"merge LSE {cuts}")
 
 
+def pin_grouped_heads_equal_replicated_heads(lib):
+    """GQA/MQA: K/V heads shared by groups of query heads give exactly the
+    result of multi-head attention with each K/V head repeated for its group."""
+    rng = np.random.default_rng(14)
+    B, H, Nq, Nk, d = 2, 6, 9, 13, 8
+    q = _bf16_like(rng, (B, H, Nq, d))
+    for hkv in (1, 2, 3, 6):
+        k = _bf16_like(rng, (B, hkv, Nk, d), 2.0)
+        v = _bf16_like(rng, (B, hkv, Nk, d))
+        kr = np.repeat(k, H // hkv, axis=1)
+        vr = np.repeat(v, H // hkv, axis=1)
+        for causal in (False, True):
+            o1, l1 = _att(lib, q, k, v, causal, 0.4, offset=2)
+            o2, l2 = _att(lib, q, kr, vr, causal, 0.4, offset=2)
+            assert np.array_equal(o1, o2) and np.array_equal(l1, l2), f"Hkv={hkv}"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -11,7 +11,8 @@ import oracle
 from tests import oracle_pins
 
 PLANTS = {1: "causal mask dropped", 2: "mask off by one", 3: "exponent sign",
-          4: "no normalisation", 5: "transposed K", 6: "LSE without max"}
+          4: "no normalisation", 5: "transposed K", 6: "LSE without max",
+          7: "grouped K/V heads mapped round-robin"}
 
 
 @pytest.mark.parametrize("plant", sorted(PLANTS), ids=lambda p: PLANTS[p])
