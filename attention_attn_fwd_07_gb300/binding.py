@@ -47,7 +47,8 @@ class attn_params(ctypes.Structure):
                 ("Nk", ctypes.c_int64), ("d", ctypes.c_int64),
                 ("causal", ctypes.c_int), ("scale", ctypes.c_float),
                 ("query_offset", ctypes.c_int64), ("dev_status", ctypes.c_void_p),
-                ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
+                ("Hkv", ctypes.c_int64)]
 
 
 def load_library(path: str | None = None):
@@ -120,13 +121,18 @@ def _require(t, dtype, name):
 
 
 def _shape(q, k, v=None):
+    """(B, H, Nq, Nk, d) of q [B, H, Nq, d] and k, v [B, Hkv, Nk, d]."""
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("expected [B, H, N, d] tensors")
     _require(q, torch.bfloat16, "q")
     _require(k, torch.bfloat16, "k")
     if v is not None:
         _require(v, torch.bfloat16, "v")
+        if tuple(v.shape) != tuple(k.shape):
+            raise ValueError("k and v must have the same shape")
     B, H, Nq, d = q.shape
+    if k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("k must be [B, Hkv, Nk, d] with the batch and head dim of q")
     return B, H, Nq, k.shape[2], d
 
 
@@ -142,8 +148,12 @@ def _outputs(q, o, lse):
 
 
 def attn_fwd(q, k, v, causal: bool, scale: float, o=None, lse=None, stream=None):
-    """Prefill forward: returns (o bf16 [B,H,Nq,d], lse f32 [B,H,Nq])."""
+    """Prefill forward: returns (o bf16 [B,H,Nq,d], lse f32 [B,H,Nq]).
+
+    K/V with fewer heads than Q (grouped K/V heads) go through attn_fwd_ex."""
     B, H, Nq, Nk, d = _shape(q, k, v)
+    if k.shape[1] != H:
+        return attn_fwd_ex(q, k, v, causal, scale, o=o, lse=lse, stream=stream)
     o, lse = _outputs(q, o, lse)
     rc = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                                  int(bool(causal)), float(scale), _stream(stream))
@@ -156,7 +166,7 @@ def make_params(q, k, v, o, lse, causal, scale, query_offset=0, flags=0, dev_sta
     B, H, Nq, Nk, d = _shape(q, k, v)
     return attn_params(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                        int(bool(causal)), float(scale), int(query_offset), _ptr(dev_status),
-                       int(flags), int(wait_timeout_us))
+                       int(flags), int(wait_timeout_us), int(k.shape[1]))
 
 
 def attn_fwd_ex(q, k, v, causal: bool, scale: float, query_offset: int = 0, flags: int = 0,
@@ -182,8 +192,13 @@ def _workspace(q, num_splits, workspace):
 
 def attn_fwd_splitkv(q, k, v, causal: bool, scale: float, num_splits: int, workspace=None,
                      o=None, lse=None, stream=None):
-    """Split-KV forward (partial + combine).  ``workspace``: caller's uint8 tensor."""
+    """Split-KV forward (partial + combine).  ``workspace``: caller's uint8 tensor.
+
+    K/V with fewer heads than Q (grouped K/V heads) go through attn_fwd_splitkv_ex."""
     B, H, Nq, Nk, d = _shape(q, k, v)
+    if k.shape[1] != H:
+        return attn_fwd_splitkv_ex(q, k, v, causal, scale, num_splits, workspace=workspace,
+                                   o=o, lse=lse, stream=stream)
     o, lse = _outputs(q, o, lse)
     ws, ws_bytes = _workspace(q, num_splits, workspace)
     rc = load_library().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq,

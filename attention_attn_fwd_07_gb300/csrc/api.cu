@@ -67,6 +67,7 @@ int validate(const attn_params* p) {
   if (!std::isfinite(p->scale) || !(p->scale > 0.0f)) return ATTN_ERR_INVALID;
   if (p->query_offset < -kMaxOffset || p->query_offset > kMaxOffset) return ATTN_ERR_INVALID;
   if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
+  if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
       p->Nk > kMaxDim)
@@ -100,9 +101,12 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   if (status == nullptr && default_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (enc == nullptr) return ATTN_ERR_CUDA;
+  const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
+  const int64_t BHkv = p->B * Hkv;
   CUtensorMap tq, tk, tv;
-  if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d) || !encode_map(enc, &tk, p->k, p->Nk, BH, p->d) ||
-      !encode_map(enc, &tv, p->v, p->Nk, BH, p->d))
+  if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d) ||
+      !encode_map(enc, &tk, p->k, p->Nk, BHkv, p->d) ||
+      !encode_map(enc, &tv, p->v, p->Nk, BHkv, p->d))
     return ATTN_ERR_CUDA;
 
   FwdArgs a;
@@ -113,6 +117,8 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   a.Nq = p->Nq;
   a.Nk = p->Nk;
   a.query_offset = p->query_offset;
+  a.H = p->H;
+  a.group = p->H / Hkv;
   a.d = static_cast<int>(p->d);
   a.causal = p->causal ? 1 : 0;
   a.scale = p->scale;
@@ -182,18 +188,22 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return ATTN_ERR_ALIGN;
   const int64_t BH = p->B * p->H;
-  const int64_t qb = p->Nq == 1 ? 1 : 4;  // query rows per partial CTA
-  if (BH * ((p->Nq + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
+  const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
+  const int64_t rows = (p->H / Hkv) * p->Nq;  // query rows sharing one K/V head
+  const int64_t qb = splitkv_rows_per_cta(rows);
+  if (p->B * Hkv * ((rows + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
 
-  const size_t rows = static_cast<size_t>(BH) * num_splits * static_cast<size_t>(p->Nq);
+  const size_t part_rows = static_cast<size_t>(BH) * num_splits * static_cast<size_t>(p->Nq);
   SplitArgs a;
   a.q = p->q;
   a.k = p->k;
   a.v = p->v;
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        align256(rows * static_cast<size_t>(p->d) * 4));
+                                        align256(part_rows * static_cast<size_t>(p->d) * 4));
   a.BH = BH;
+  a.H = p->H;
+  a.Hkv = Hkv;
   a.Nq = p->Nq;
   a.Nk = p->Nk;
   a.query_offset = p->query_offset;

@@ -12,7 +12,8 @@
 // size Nq x Nk touches device memory.
 //
 // One CTA owns 256 query rows of one (b,h) as two 128-row tiles A and B that
-// share every K/V tile (prior art: the producer/consumer, TMA-fed, on-chip
+// share every K/V tile, read from the query head's K/V head when K/V heads
+// are grouped (prior art: the producer/consumer, TMA-fed, on-chip
 // accumulator pipeline described for FlashAttention-3 on H100; here rebuilt
 // on tcgen05 with TMEM accumulators):
 //   warp 9      TMA producer: Q_A, Q_B once, then K0 V0 K1 V1 ... through an
@@ -84,6 +85,7 @@ struct KParams {
   float* lse;
   int* status;
   int64_t Nq, Nk, qoff;
+  int64_t H, group;  // query heads per batch; query heads per K/V head
   int n_qblk;
   int causal;
   float sc_log2;  // scale * log2(e)
@@ -150,6 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int qi = static_cast<int>(blockIdx.x % p.n_qblk);
   const int qb = p.causal ? (p.n_qblk - 1 - qi) : qi;
   const int64_t q0 = static_cast<int64_t>(qb) * (2 * BM);
+  // K/V head of this query head (grouped K/V heads: H / group per batch).
+  const int64_t bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
   int ntile[2];
   ntile[0] = tiles_for(q0, p);
   ntile[1] = tiles_for(q0 + BM, p);
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key0 = (t >> 1) * BN;
         for (int a = 0; a < C::kAtoms; ++a)
           tma_load_3d(sKV + s * C::kKVBytes + a * C::kAtomBytes, map, bar(C::kBarFull + s),
-                      a * 64, key0, static_cast<int>(bh));
+                      a * 64, key0, static_cast<int>(bkv));
       }
       // Every issued load must land before the CTA can exit.  Only this
       // thread arrives on the full barriers, so the phase of the last load
@@ -461,6 +465,8 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.qoff = a.query_offset;
+  p.H = a.H;
+  p.group = a.group;
   p.n_qblk = static_cast<int>((a.Nq + 2 * BM - 1) / (2 * BM));
   p.causal = a.causal;
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);

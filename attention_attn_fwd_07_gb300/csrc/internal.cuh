@@ -15,6 +15,7 @@ struct FwdArgs {
   float* lse;          // f32  [B][H][Nq]
   int* status;         // device status word (bit 0 = wait timeout)
   int64_t BH, Nq, Nk, query_offset;
+  int64_t H, group;    // query heads per batch; query heads per K/V head
   int d;
   int causal;
   float scale;
@@ -24,10 +25,11 @@ struct FwdArgs {
 
 // Arguments of one split-KV decode launch pair, already validated.
 struct SplitArgs {
-  const void *q, *k, *v;  // bf16 [B][H][N][d]
+  const void *q, *k, *v;  // bf16 q [B][H][Nq][d], k/v [B][Hkv][Nk][d]
   float* o_part;          // f32 [BH][S][Nq][d]
   float* lse_part;        // f32 [BH][S][Nq]
-  int64_t BH, Nq, Nk, query_offset;
+  int64_t BH, Nq, Nk, query_offset;  // BH: batch x query heads
+  int64_t H, Hkv;                     // query heads and K/V heads per batch
   int64_t keys_per_split;
   int d;
   int splits;
@@ -37,6 +39,12 @@ struct SplitArgs {
 
 // Query rows per CTA of the prefill kernel (two 128-row tiles).
 constexpr int kFwdRowsPerCta = 256;
+
+// Query rows one split-KV partial CTA serves, out of the rows that share one
+// K/V head (query heads of the group x query positions).
+inline int64_t splitkv_rows_per_cta(int64_t rows_per_kv_head) {
+  return rows_per_kv_head == 1 ? 1 : (rows_per_kv_head <= 4 ? 4 : 8);
+}
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream);

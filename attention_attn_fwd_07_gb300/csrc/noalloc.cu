@@ -80,7 +80,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   if (need == 0) return ATTN_ERR_UNSUPPORTED;
   if (need > static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES)) return ATTN_ERR_WORKSPACE;
   const int64_t BH = B * H;
-  const int64_t qb = Nq == 1 ? 1 : 4;
+  const int64_t qb = splitkv_rows_per_cta(Nq);
   if (BH * ((Nq + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
 
   void* scratch = nullptr;
@@ -96,6 +96,8 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                         align256(rows * static_cast<size_t>(d) * 4));
   a.BH = BH;
+  a.H = H;
+  a.Hkv = H;
   a.Nq = Nq;
   a.Nk = Nk;
   a.query_offset = 0;

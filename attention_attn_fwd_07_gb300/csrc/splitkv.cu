@@ -1,8 +1,10 @@
 // splitkv.cu -- memory-bound split-KV attention for short queries (decode)
 // and the log-sum-exp combine.
 //
-// Partial kernel: one CTA per (batch*head, query block of QB rows, key split
-// s).  The split's keys [s*L, min((s+1)*L, Nk)) are streamed once from device
+// Partial kernel: one CTA per (batch * K/V head, block of QB query rows, key
+// split s).  The query rows of a K/V head are those of every query head in
+// its group (grouped-query / multi-query attention) at every query position,
+// so a split's K/V slice is read from memory once for the whole group.  The split's keys [s*L, min((s+1)*L, Nk)) are streamed once from device
 // memory with 16-byte read-only loads: a key row of d bf16 is read by d/8
 // adjacent lanes, so a warp reads 32/(d/8) whole rows per instruction and the
 // CTA's 8 warps read consecutive rows.  Each lane group keeps the online
@@ -37,6 +39,7 @@ struct PartialParams {
   float* o_part;
   float* lse_part;
   int64_t Nq, Nk, qoff, L;
+  int64_t H, Hkv, G, R;  // query heads, K/V heads, group size, rows per K/V head
   int S, n_qb, causal;
   float sc_log2;
 };
@@ -72,8 +75,8 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[8], f
   m = mn;
 }
 
-template <int D, int QB, int U>
-__global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const PartialParams p) {
+template <int D, int QB, int U, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const PartialParams p) {
   constexpr int LPR = D / 8;      // lanes per key row (16 B each)
   constexpr int G = 32 / LPR;     // key rows per warp instruction
   constexpr int STEP = kWarps * G * U;
@@ -88,17 +91,24 @@ __global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const Part
   const int s = static_cast<int>(lin % p.S);
   const int64_t rest = lin / p.S;
   const int qb = static_cast<int>(rest % p.n_qb);
-  const int64_t bh = rest / p.n_qb;
-  const int64_t i0 = static_cast<int64_t>(qb) * QB;
+  const int64_t bkv = rest / p.n_qb;  // batch * Hkv + K/V head
+  const int64_t r0 = static_cast<int64_t>(qb) * QB;
+  // Row r of this K/V head: query head (group member r / Nq), position r % Nq.
+  int64_t qrow[QB], pos[QB];
+#pragma unroll
+  for (int qi = 0; qi < QB; ++qi) {
+    const int64_t r = min(r0 + qi, p.R - 1);
+    const int64_t g = r / p.Nq;
+    pos[qi] = r % p.Nq;
+    const int64_t h = (bkv % p.Hkv) * p.G + g;
+    qrow[qi] = ((bkv / p.Hkv) * p.H + h) * p.Nq + pos[qi];
+  }
 
   const int64_t k_lo = static_cast<int64_t>(s) * p.L;
   int64_t k_hi = min(k_lo + p.L, p.Nk);
   int64_t lim[QB];  // last admissible key per query row
 #pragma unroll
-  for (int qi = 0; qi < QB; ++qi) {
-    const int64_t i = min(i0 + qi, p.Nq - 1);
-    lim[qi] = p.causal ? min(p.Nk - 1, i + p.qoff) : p.Nk - 1;
-  }
+  for (int qi = 0; qi < QB; ++qi) lim[qi] = p.causal ? min(p.Nk - 1, pos[qi] + p.qoff) : p.Nk - 1;
   if (p.causal) {
     int64_t top = lim[0];
 #pragma unroll
@@ -109,8 +119,7 @@ __global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const Part
   float qf[QB][8];
 #pragma unroll
   for (int qi = 0; qi < QB; ++qi) {
-    const int64_t i = min(i0 + qi, p.Nq - 1);
-    const uint4 r = ld_stream(p.q + (bh * p.Nq + i) * D + 8 * sub);
+    const uint4 r = ld_stream(p.q + qrow[qi] * D + 8 * sub);
     unpack8(r, qf[qi]);
 #pragma unroll
     for (int e = 0; e < 8; ++e) qf[qi][e] *= p.sc_log2;
@@ -125,8 +134,8 @@ __global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const Part
     for (int e = 0; e < 8; ++e) o[qi][e] = 0.0f;
   }
 
-  const uint16_t* kbase = p.k + bh * p.Nk * D + 8 * sub;
-  const uint16_t* vbase = p.v + bh * p.Nk * D + 8 * sub;
+  const uint16_t* kbase = p.k + bkv * p.Nk * D + 8 * sub;
+  const uint16_t* vbase = p.v + bkv * p.Nk * D + 8 * sub;
   for (int64_t base = k_lo; base < k_hi; base += STEP) {
     uint4 kr[U], vr[U];
     int64_t key[U];
@@ -210,8 +219,7 @@ __global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const Part
   // Merge the warps and write the split's normalised output and LSE.
   for (int idx = threadIdx.x; idx < QB * D; idx += kThreads) {
     const int qi = idx / D, e = idx % D;
-    const int64_t i = i0 + qi;
-    if (i >= p.Nq) continue;
+    if (r0 + qi >= p.R) continue;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][qi]);
@@ -225,7 +233,9 @@ __global__ void __launch_bounds__(kThreads, 2) splitkv_partial_kernel(const Part
       }
     }
     const bool empty = !(L > 0.0f);
-    const int64_t slot = (bh * p.S + s) * p.Nq + i;
+    // partial slot of (batch * H + query head, split s, position)
+    const int64_t bh = qrow[qi] / p.Nq;
+    const int64_t slot = (bh * p.S + s) * p.Nq + pos[qi];
     p.o_part[slot * D + e] = empty ? 0.0f : acc / L;
     if (e == 0) p.lse_part[slot] = empty ? -INFINITY : (M + log2f(L)) * kLn2;
   }
@@ -285,7 +295,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (lane == 0) lse[row] = empty ? -INFINITY : M + logf(W);
 }
 
-template <int D, int QB, int U>
+template <int D, int QB, int U, int MINB>
 cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
   PartialParams p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -298,23 +308,31 @@ cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
   p.qoff = a.query_offset;
   p.L = a.keys_per_split;
   p.S = a.splits;
-  p.n_qb = static_cast<int>((a.Nq + QB - 1) / QB);
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = a.H / a.Hkv;
+  p.R = p.G * a.Nq;
+  p.n_qb = static_cast<int>((p.R + QB - 1) / QB);
   p.causal = a.causal;
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
-  const int64_t blocks = a.BH * p.n_qb * a.splits;
-  splitkv_partial_kernel<D, QB, U><<<dim3(static_cast<unsigned>(blocks)), kThreads, 0, stream>>>(p);
+  const int64_t blocks = (a.BH / p.G) * p.n_qb * a.splits;
+  splitkv_partial_kernel<D, QB, U, MINB>
+      <<<dim3(static_cast<unsigned>(blocks)), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_splitkv_partial(const SplitArgs& a, cudaStream_t stream) {
+  const int64_t qb = splitkv_rows_per_cta((a.H / a.Hkv) * a.Nq);
   if (a.d == 64) {
-    if (a.Nq == 1) return launch_partial<64, 1, 4>(a, stream);
-    return launch_partial<64, 4, 2>(a, stream);
+    if (qb == 1) return launch_partial<64, 1, 4, 2>(a, stream);
+    if (qb == 4) return launch_partial<64, 4, 2, 2>(a, stream);
+    return launch_partial<64, 8, 2, 1>(a, stream);
   }
-  if (a.Nq == 1) return launch_partial<128, 1, 4>(a, stream);
-  return launch_partial<128, 4, 2>(a, stream);
+  if (qb == 1) return launch_partial<128, 1, 4, 2>(a, stream);
+  if (qb == 4) return launch_partial<128, 4, 2, 2>(a, stream);
+  return launch_partial<128, 8, 2, 1>(a, stream);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, void* o, float* lse,

@@ -30,6 +30,11 @@ class Workload:
     seed: int
     k_boost_frac: float = 0.0
     splits: tuple = field(default=())
+    Hkv: int = 0  # K/V heads (grouped-query attention); 0 = H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv or self.H
 
     @property
     def scale(self) -> float:
@@ -48,6 +53,9 @@ LONG_PREFILL_NONCAUSAL = Workload("long prefill B2 H32 N8192 d128 non-causal, K 
                                   2, 32, 8192, 8192, 128, False, 1003, k_boost_frac=0.01)
 DECODE = Workload("decode B16 H32 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768, 128, False,
                   1004, splits=(16, 32, 64))
+# Grouped-query decode: 8 K/V heads shared by groups of 4 query heads.
+DECODE_GQA = Workload("decode GQA B16 H32 Hkv8 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768,
+                      128, False, 1005, splits=(16, 32, 64), Hkv=8)
 
 
 def ragged(n: int, causal: bool) -> Workload:
@@ -58,7 +66,7 @@ def ragged(n: int, causal: bool) -> Workload:
 
 def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = None,
              Nk: int | None = None):
-    """Draw (q, k, v) as contiguous bfloat16 [B, H, N, d] tensors on ``device``.
+    """Draw q [B, H, Nq, d] and k, v [B, Hkv, Nk, d] as contiguous bfloat16.
 
     ``Nq``/``Nk`` override the workload's lengths (smaller parity cases that
     keep the same distribution).
@@ -67,18 +75,18 @@ def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = N
     Nk = w.Nk if Nk is None else Nk
     g = torch.Generator(device=device).manual_seed(w.seed)
 
-    def draw(n):
-        out = torch.empty((w.B, w.H, n, w.d), dtype=torch.bfloat16, device=device)
+    def draw(n, heads):
+        out = torch.empty((w.B, heads, n, w.d), dtype=torch.bfloat16, device=device)
         for b in range(w.B):  # per batch keeps the float32 temporary small
-            out[b] = torch.randn((w.H, n, w.d), generator=g, device=device,
+            out[b] = torch.randn((heads, n, w.d), generator=g, device=device,
                                  dtype=torch.float32).to(torch.bfloat16)
         return out
 
-    q, k, v = draw(Nq), draw(Nk), draw(Nk)
+    q, k, v = draw(Nq, w.H), draw(Nk, w.kv_heads), draw(Nk, w.kv_heads)
     if w.k_boost_frac > 0.0:
         n_boost = math.ceil(w.k_boost_frac * Nk)
         for b in range(w.B):
-            for h in range(w.H):
+            for h in range(w.kv_heads):
                 rows = torch.randperm(Nk, generator=g, device=device)[:n_boost]
                 k[b, h, rows] = k[b, h, rows] * 4
     return q, k, v

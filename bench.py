@@ -74,7 +74,7 @@ def prefill_flops(w: W.Workload) -> float:
 
 
 def decode_bytes(w: W.Workload) -> int:
-    kv = 2 * w.B * w.H * w.Nk * w.d * 2
+    kv = 2 * w.B * w.kv_heads * w.Nk * w.d * 2
     qo = 2 * w.B * w.H * w.Nq * w.d * 2
     return kv + qo + w.B * w.H * w.Nq * 4
 
@@ -380,6 +380,7 @@ def main():
 
     others = []
     decode = None
+    decode_gqa = None
     if not args.quick:
         # ---- the other prefill workloads
         for wo in (W.LONG_PREFILL_NONCAUSAL, W.PREFILL):
@@ -410,39 +411,45 @@ def main():
                            "l2": "inputs > L2" if wo.Nq >= 8192 else
                                  "L2 flushed (256 MB rewrite) before each timed launch"})
 
-        # ---- decode (split-KV + combine), memory bound
-        wd = W.DECODE
-        qd, kd, vd = W.make_qkv(wd, device=dev)
-        od = torch.empty_like(qd)
-        ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
-        results = []
-        for S in wd.splits:
-            need = binding.attn_splitkv_workspace_bytes(wd.B, wd.H, 1, wd.d, S)
-            ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        # ---- decode (split-KV + combine), memory bound; MHA and grouped K/V heads
+        def run_decode(wd):
+            nonlocal launches
+            qd, kd, vd = W.make_qkv(wd, device=dev)
+            od = torch.empty_like(qd)
+            ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
+            results = []
+            for S in wd.splits:
+                need = binding.attn_splitkv_workspace_bytes(wd.B, wd.H, 1, wd.d, S)
+                ws = torch.empty((need,), dtype=torch.uint8, device=dev)
 
-            def sd(S=S, ws=ws):
-                binding.attn_fwd_splitkv(qd, kd, vd, False, wd.scale, S, workspace=ws, o=od,
-                                         lse=ld, stream=stream)
+                def sd(S=S, ws=ws):
+                    binding.attn_fwd_splitkv(qd, kd, vd, False, wd.scale, S, workspace=ws, o=od,
+                                             lse=ld, stream=stream)
 
-            for _ in range(args.warmup):
-                sd()
-            n = max(10, args.steps // 4)
-            m = max_over_ranks(event_time(sd, n, stream))
-            launches += 2 * n
-            gbs = decode_bytes(wd) / (m / 1e3) / 1e9
-            results.append({"splits": S, "ms_per_step": m, "GB/s": gbs,
-                            "workspace_bytes": need})
-        best = max(results, key=lambda r: r["GB/s"])
-        decode = {"workload": wd.name, "metric": "HBM GB/s", "unit": "GB/s",
-                  "value": world * best["GB/s"], "ms_per_step": best["ms_per_step"],
-                  "splits": best["splits"], "per_split_count": results,
-                  "algorithmic_bytes_per_step": decode_bytes(wd),
-                  "roofline": {"bound": "hbm", "achieved": best["GB/s"], "peak": pk["hbm_gbs"],
-                               "unit": "GB/s", "frac": best["GB/s"] / pk["hbm_gbs"],
-                               "peak_source": f"{pk_src} copy bandwidth",
-                               "traffic": recorded_traffic(DECODE_PROFILE_TXT, DECODE_SOURCES)},
-                  "l2": "inputs 8.6 GB > L2"}
-        del qd, kd, vd
+                for _ in range(args.warmup):
+                    sd()
+                n = max(10, args.steps // 4)
+                m = max_over_ranks(event_time(sd, n, stream))
+                launches += 2 * n
+                gbs = decode_bytes(wd) / (m / 1e3) / 1e9
+                results.append({"splits": S, "ms_per_step": m, "GB/s": gbs,
+                                "workspace_bytes": need})
+            del qd, kd, vd
+            best = max(results, key=lambda r: r["GB/s"])
+            return {"workload": wd.name, "metric": "HBM GB/s", "unit": "GB/s",
+                    "value": world * best["GB/s"], "ms_per_step": best["ms_per_step"],
+                    "splits": best["splits"], "per_split_count": results,
+                    "algorithmic_bytes_per_step": decode_bytes(wd),
+                    "roofline": {"bound": "hbm", "achieved": best["GB/s"],
+                                 "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                 "frac": best["GB/s"] / pk["hbm_gbs"],
+                                 "peak_source": f"{pk_src} copy bandwidth",
+                                 "traffic": recorded_traffic(DECODE_PROFILE_TXT, DECODE_SOURCES)
+                                 if wd is W.DECODE else None},
+                    "l2": f"inputs {decode_bytes(wd) / 1e9:.1f} GB > L2"}
+
+        decode = run_decode(W.DECODE)
+        decode_gqa = run_decode(W.DECODE_GQA)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -458,7 +465,7 @@ def main():
                    "l2": "inputs (403 MB) larger than L2; no flush",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clocks, "decode": decode, "other_workloads": others,
+        "clocks": clocks, "decode": decode, "decode_gqa": decode_gqa, "other_workloads": others,
         "kernel_source_sha256_16": kernel_source_hash(),
     }
     if rank == 0:

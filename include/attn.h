@@ -73,11 +73,13 @@ enum {
 };
 
 /* Full argument set of the prefill entry point (attn_fwd_ex) and of the
- * split-KV entry point (attn_fwd_splitkv_ex). */
+ * split-KV entry point (attn_fwd_splitkv_ex).  Grouped K/V heads (GQA/MQA,
+ * among FlashAttention's production features in "GPU Kernels: CUDA, HIP &
+ * Triton", section 7.6) are available through these two entry points. */
 typedef struct attn_params {
   const void* q;          /* bf16 [B][H][Nq][d], device                    */
-  const void* k;          /* bf16 [B][H][Nk][d], device                    */
-  const void* v;          /* bf16 [B][H][Nk][d], device                    */
+  const void* k;          /* bf16 [B][Hkv][Nk][d], device                  */
+  const void* v;          /* bf16 [B][Hkv][Nk][d], device                  */
   void* o;                /* bf16 [B][H][Nq][d], device, written           */
   float* lse;             /* f32  [B][H][Nq],    device, written           */
   int64_t B, H, Nq, Nk, d;
@@ -88,6 +90,9 @@ typedef struct attn_params {
                              as bit 0; NULL = the library's own status word */
   uint32_t flags;         /* ATTN_FLAG_* */
   uint32_t wait_timeout_us; /* per-wait device timeout; 0 = 1,000,000 us   */
+  int64_t Hkv;            /* K/V heads (grouped-query / multi-query attention):
+                             K and V are [B][Hkv][Nk][d] and query head h reads
+                             K/V head h / (H / Hkv); H % Hkv == 0.  0 = H.  */
 } attn_params;
 
 /*
@@ -114,7 +119,9 @@ size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
  * cut into num_splits contiguous ranges of L = ceil(Nk/num_splits) keys
  * rounded up to a multiple of 128 (trailing ranges may be empty); each range
  * yields a partial (normalised o, lse) in `workspace`, then attn_combine
- * merges them into O and LSE.  1 <= num_splits <= 256.  Two launches on
+ * merges them into O and LSE.  With grouped K/V heads (attn_fwd_splitkv_ex)
+ * one CTA serves all query heads of a K/V head, so each K/V byte is read
+ * once per group.  1 <= num_splits <= 256.  Two launches on
  * `stream`; `workspace` (device, 16-byte aligned, caller-owned) must hold
  * attn_splitkv_workspace_bytes(...) bytes (ATTN_ERR_WORKSPACE otherwise).
  */

@@ -77,7 +77,7 @@ def test_fwd_rejects(lib, kw, code):
 
 def _params(**kw):
     base = dict(q=A16, k=A16, v=A16, o=A16, lse=A16, B=1, H=1, Nq=8, Nk=8, d=64, causal=1,
-                scale=0.125, query_offset=0, dev_status=None, flags=0, wait_timeout_us=0)
+                scale=0.125, query_offset=0, dev_status=None, flags=0, wait_timeout_us=0, Hkv=0)
     base.update(kw)
     return binding.attn_params(**base)
 
@@ -88,6 +88,14 @@ def test_negative_offset_needs_flag(lib):
     p = _params(query_offset=1 << 41, flags=binding.ATTN_FLAG_ALLOW_NEG_OFFSET)
     assert lib.attn_fwd_ex(ctypes.byref(p), None) == binding.ATTN_ERR_INVALID
     assert lib.attn_fwd_ex(None, None) == binding.ATTN_ERR_INVALID
+
+
+@pytest.mark.parametrize("H,Hkv", [(8, 3), (8, 16), (8, -1), (6, 4)])
+def test_grouped_heads_must_divide(lib, H, Hkv):
+    p = _params(H=H, Hkv=Hkv)
+    assert lib.attn_fwd_ex(ctypes.byref(p), None) == binding.ATTN_ERR_INVALID
+    need = lib.attn_splitkv_workspace_bytes(1, H, 8, 64, 2)
+    assert lib.attn_fwd_splitkv_ex(ctypes.byref(p), 2, A16, need, None) == binding.ATTN_ERR_INVALID
 
 
 def test_workspace_bytes(lib):
