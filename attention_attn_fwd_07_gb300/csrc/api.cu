@@ -212,6 +212,9 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   a.splits = num_splits;
   a.causal = p->causal ? 1 : 0;
   a.scale = p->scale;
+  a.status = p->dev_status;
+  if (a.status == nullptr && default_status_word(&a.status) != cudaSuccess) return ATTN_ERR_CUDA;
+  a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
   if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   if (launch_combine(a.o_part, a.lse_part, p->o, p->lse, BH, p->Nq, a.d, num_splits, stream) !=
       cudaSuccess)

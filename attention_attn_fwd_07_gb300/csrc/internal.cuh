@@ -35,6 +35,8 @@ struct SplitArgs {
   int splits;
   int causal;
   float scale;
+  int* status;          // device status word (bit 0 = wait timeout)
+  uint64_t timeout_ns;  // per-wait limit of the pipelined partial kernel
 };
 
 // Query rows per CTA of the prefill kernel (two 128-row tiles).

@@ -107,6 +107,8 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   a.splits = num_splits;
   a.causal = causal ? 1 : 0;
   a.scale = scale;
+  if (default_status_word(&a.status) != cudaSuccess) return ATTN_ERR_CUDA;
+  a.timeout_ns = 1000000000ull;
   if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   if (launch_combine(a.o_part, a.lse_part, o, lse, BH, Nq, a.d, num_splits, stream) !=
       cudaSuccess)

@@ -15,6 +15,13 @@
 // rescaling.  Output per (row, split): the normalised o (f32) and its
 // natural-log LSE; an empty or fully masked split gives o = 0, lse = -inf.
 //
+// Pipelined variant (several query rows per K/V head: GQA groups or Nq > 1):
+// a producer warp streams the split's contiguous K and V slices into a
+// 4-stage shared-memory ring with 1-D bulk copies (64 keys per stage), so
+// the bytes in flight do not depend on registers; eight consumer warps run
+// the same online-softmax arithmetic from shared memory.  Its waits are
+// bounded like the prefill kernel's (timeout -> status word, clean exit).
+//
 // Combine kernel: one warp per (batch*head, query row) merges the splits:
 // M = max lse_s, w_s = exp(lse_s - M), O = sum w_s o_s / sum w_s (-> bf16),
 // LSE = M + ln sum w_s; M = -inf gives O = +0.0, LSE = -inf (the section 22.7
@@ -42,6 +49,8 @@ struct PartialParams {
   int64_t H, Hkv, G, R;  // query heads, K/V heads, group size, rows per K/V head
   int S, n_qb, causal;
   float sc_log2;
+  int* status;
+  uint64_t timeout_ns;
 };
 
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* ptr) {
@@ -241,6 +250,255 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
   }
 }
 
+constexpr int kBulkWarps = 8;                        // consumer warps
+constexpr int kBulkThreads = (kBulkWarps + 1) * 32;  // + one producer warp
+constexpr int kChunk = 64;                           // keys per pipeline stage
+constexpr int kBulkStages = 4;
+
+template <int D>
+constexpr uint32_t bulk_smem_bytes() {
+  return kBulkStages * 2u * kChunk * D * 2u + 2u * kBulkStages * 8u + 16u;
+}
+
+template <int D, int QB>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    splitkv_partial_bulk_kernel(const PartialParams p) {
+  constexpr int LPR = D / 8;            // lanes per key row (16 B each)
+  constexpr int G = 32 / LPR;           // key rows per warp instruction
+  constexpr int KPW = kChunk / kBulkWarps;  // keys per warp per stage
+  constexpr int U = KPW / G;            // key rows per lane group per stage
+  constexpr int UB = (QB >= 8 && U > 1) ? 1 : U;  // rows per online-softmax step
+  constexpr uint32_t kChunkBytes = kChunk * D * 2;
+  static_assert(U >= 1 && KPW % G == 0, "stage split");
+
+  extern __shared__ __align__(128) uint8_t dyn[];
+  __shared__ float sm_m[kBulkWarps][QB];
+  __shared__ float sm_l[kBulkWarps][QB];
+  __shared__ __align__(16) float sm_o[kBulkWarps][QB][D];
+  const uint32_t sbase = smem_u32(dyn);
+  const uint32_t bar_base = sbase + kBulkStages * 2u * kChunkBytes;
+  auto full = [&](int st) { return bar_base + 8u * st; };
+  auto empty = [&](int st) { return bar_base + 8u * (kBulkStages + st); };
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(dyn + kBulkStages * 2u * kChunkBytes + 16u * kBulkStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPR, sub = lane % LPR;
+  const int64_t lin = blockIdx.x;
+  const int s = static_cast<int>(lin % p.S);
+  const int64_t rest = lin / p.S;
+  const int qb = static_cast<int>(rest % p.n_qb);
+  const int64_t bkv = rest / p.n_qb;
+  const int64_t r0 = static_cast<int64_t>(qb) * QB;
+  // Row qi of this CTA: query row index (batch*H + head)*Nq + position.
+  auto row_of = [&](int qi, int64_t& position) -> int64_t {
+    const int64_t r = min(r0 + qi, p.R - 1);
+    position = r % p.Nq;
+    const int64_t h = (bkv % p.Hkv) * p.G + r / p.Nq;
+    return ((bkv / p.Hkv) * p.H + h) * p.Nq + position;
+  };
+  const int64_t k_lo = static_cast<int64_t>(s) * p.L;
+  int64_t k_hi = min(k_lo + p.L, p.Nk);
+  // Last admissible key of each row, relative to k_lo (clamped to int).
+  int lim_rel[QB];
+  int64_t top = -1;
+#pragma unroll
+  for (int qi = 0; qi < QB; ++qi) {
+    int64_t position;
+    row_of(qi, position);
+    const int64_t lim = p.causal ? min(p.Nk - 1, position + p.qoff) : p.Nk - 1;
+    top = max(top, lim);
+    const int64_t rel = lim - k_lo;
+    lim_rel[qi] = static_cast<int>(rel < -1 ? -1 : (rel > (1 << 30) ? (1 << 30) : rel));
+  }
+  k_hi = min(k_hi, top + 1);
+  const int n_chunks = k_hi > k_lo ? static_cast<int>((k_hi - k_lo + kChunk - 1) / kChunk) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kBulkStages; ++st) {
+      mbar_init(full(st), 1);
+      mbar_init(empty(st), kBulkWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  // Bounded wait; false when this CTA is aborting or the wait timed out.
+  auto wait = [&](uint32_t bar, uint32_t parity, bool honour_abort) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((spin & 31u) == 0) {
+        if (honour_abort && *abort_flag) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          *abort_flag = 1;
+          atomicOr(p.status, 1);
+          return false;
+        }
+      }
+    }
+  };
+
+  if (warp == kBulkWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int last[kBulkStages];
+      for (int st = 0; st < kBulkStages; ++st) last[st] = -1;
+      const uint16_t* kg = p.k + bkv * p.Nk * D;
+      const uint16_t* vg = p.v + bkv * p.Nk * D;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int st = c % kBulkStages;
+        if (c >= kBulkStages && !wait(empty(st), ((c / kBulkStages) - 1) & 1, true)) break;
+        const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
+        const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kChunk), k_hi - key0)) * D * 2;
+        mbar_arrive_expect_tx(full(st), 2 * bytes);
+        bulk_load(sbase + st * 2u * kChunkBytes, kg + key0 * D, bytes, full(st));
+        bulk_load(sbase + st * 2u * kChunkBytes + kChunkBytes, vg + key0 * D, bytes, full(st));
+        last[st] = c;
+      }
+      // Copies in flight must land before the CTA exits (bounded, ignores abort).
+      for (int st = 0; st < kBulkStages; ++st)
+        if (last[st] >= 0) wait(full(st), (last[st] / kBulkStages) & 1, false);
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    float qf[QB][8];
+#pragma unroll
+    for (int qi = 0; qi < QB; ++qi) {
+      int64_t position;
+      const uint4 r = ld_stream(p.q + row_of(qi, position) * D + 8 * sub);
+      unpack8(r, qf[qi]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qf[qi][e] *= p.sc_log2;
+    }
+    float m[QB], l[QB], o[QB][8];
+#pragma unroll
+    for (int qi = 0; qi < QB; ++qi) {
+      m[qi] = -INFINITY;
+      l[qi] = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[qi][e] = 0.0f;
+    }
+    for (int c = 0; c < n_chunks; ++c) {
+      const int st = c % kBulkStages;
+      if (!__all_sync(0xffffffffu, wait(full(st), (c / kBulkStages) & 1, true))) break;
+      const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
+      const int nk = static_cast<int>(min(static_cast<int64_t>(kChunk), k_hi - key0));
+      const uint16_t* ks = reinterpret_cast<const uint16_t*>(dyn + st * 2u * kChunkBytes);
+      const uint16_t* vs = ks + kChunk * D;
+      // This warp's KPW keys of the stage, UB key rows per lane group at a
+      // time (fewer live registers when QB is large).
+#pragma unroll
+      for (int u0 = 0; u0 < U; u0 += UB) {
+        uint4 kr[UB], vr[UB];
+        int kk[UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          kk[u] = warp * KPW + (u0 + u) * G + grp;
+          if (kk[u] < nk) {
+            kr[u] = *reinterpret_cast<const uint4*>(ks + kk[u] * D + 8 * sub);
+            vr[u] = *reinterpret_cast<const uint4*>(vs + kk[u] * D + 8 * sub);
+          } else {
+            kr[u] = make_uint4(0u, 0u, 0u, 0u);
+            vr[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        if (u0 + UB >= U) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty(st));  // release orders this warp's reads
+        }
+        float sc[QB][UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          float kf[8];
+          unpack8(kr[u], kf);
+          const int key_rel = static_cast<int>(key0 - k_lo) + kk[u];
+#pragma unroll
+          for (int qi = 0; qi < QB; ++qi) {
+            float dot = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dot = fmaf(qf[qi][e], kf[e], dot);
+#pragma unroll
+            for (int off = 1; off < LPR; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+            sc[qi][u] = (kk[u] < nk && key_rel <= lim_rel[qi]) ? dot : -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int qi = 0; qi < QB; ++qi) {
+          float mx = sc[qi][0];
+#pragma unroll
+          for (int u = 1; u < UB; ++u) mx = fmaxf(mx, sc[qi][u]);
+          const float m_new = fmaxf(m[qi], mx);
+          if (m_new == -INFINITY) continue;
+          const float alpha = ex2_approx(m[qi] - m_new);
+          l[qi] *= alpha;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[qi][e] *= alpha;
+          m[qi] = m_new;
+#pragma unroll
+          for (int u = 0; u < UB; ++u) {
+            const float pu = ex2_approx(sc[qi][u] - m_new);
+            l[qi] += pu;
+            float vf[8];
+            unpack8(vr[u], vf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[qi][e] = fmaf(pu, vf[e], o[qi][e]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int off = LPR; off < 32; off <<= 1) {
+#pragma unroll
+      for (int qi = 0; qi < QB; ++qi) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m[qi], off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l[qi], off);
+        float o2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[qi][e], off);
+        merge_state(m[qi], l[qi], o[qi], m2, l2, o2);
+      }
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int qi = 0; qi < QB; ++qi) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sm_o[warp][qi][8 * sub + e] = o[qi][e];
+        if (sub == 0) {
+          sm_m[warp][qi] = m[qi];
+          sm_l[warp][qi] = l[qi];
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < QB * D; idx += kBulkThreads) {
+    const int qi = idx / D, e = idx % D;
+    if (r0 + qi >= p.R) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kBulkWarps; ++w) M = fmaxf(M, sm_m[w][qi]);
+    float L = 0.0f, acc = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kBulkWarps; ++w) {
+        const float f = ex2_approx(sm_m[w][qi] - M);
+        L = fmaf(sm_l[w][qi], f, L);
+        acc = fmaf(sm_o[w][qi][e], f, acc);
+      }
+    }
+    const bool empty_row = !(L > 0.0f);
+    int64_t ps;
+    const int64_t qr = row_of(qi, ps);
+    const int64_t slot = ((qr / p.Nq) * p.S + s) * p.Nq + ps;
+    p.o_part[slot * D + e] = empty_row ? 0.0f : acc / L;
+    if (e == 0) p.lse_part[slot] = empty_row ? -INFINITY : (M + log2f(L)) * kLn2;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o_part,
                                                       const float* __restrict__ lse_part,
@@ -321,18 +579,53 @@ cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int D, int QB>
+cudaError_t launch_partial_bulk(const SplitArgs& a, cudaStream_t stream) {
+  PartialParams p;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.k = static_cast<const uint16_t*>(a.k);
+  p.v = static_cast<const uint16_t*>(a.v);
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.qoff = a.query_offset;
+  p.L = a.keys_per_split;
+  p.S = a.splits;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = a.H / a.Hkv;
+  p.R = p.G * a.Nq;
+  p.n_qb = static_cast<int>((p.R + QB - 1) / QB);
+  p.causal = a.causal;
+  p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.status = a.status;
+  p.timeout_ns = a.timeout_ns;
+  constexpr uint32_t smem = bulk_smem_bytes<D>();
+  cudaError_t err = cudaFuncSetAttribute(splitkv_partial_bulk_kernel<D, QB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int64_t blocks = (a.BH / p.G) * p.n_qb * a.splits;
+  splitkv_partial_bulk_kernel<D, QB>
+      <<<dim3(static_cast<unsigned>(blocks)), kBulkThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_splitkv_partial(const SplitArgs& a, cudaStream_t stream) {
+  // One row per K/V head: register streaming.  Several rows (GQA groups,
+  // Nq > 1): the bulk-copy pipeline, which reads each K/V byte once per CTA.
   const int64_t qb = splitkv_rows_per_cta((a.H / a.Hkv) * a.Nq);
   if (a.d == 64) {
     if (qb == 1) return launch_partial<64, 1, 4, 2>(a, stream);
-    if (qb == 4) return launch_partial<64, 4, 2, 2>(a, stream);
-    return launch_partial<64, 8, 2, 1>(a, stream);
+    if (qb == 4) return launch_partial_bulk<64, 4>(a, stream);
+    return launch_partial_bulk<64, 8>(a, stream);
   }
   if (qb == 1) return launch_partial<128, 1, 4, 2>(a, stream);
-  if (qb == 4) return launch_partial<128, 4, 2, 2>(a, stream);
-  return launch_partial<128, 8, 2, 1>(a, stream);
+  if (qb == 4) return launch_partial_bulk<128, 4>(a, stream);
+  return launch_partial_bulk<128, 8>(a, stream);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, void* o, float* lse,

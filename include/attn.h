@@ -130,9 +130,10 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      int causal, float scale, int num_splits, void* workspace,
                      size_t workspace_bytes, cudaStream_t stream);
 
-/* attn_fwd_splitkv with query_offset and flags from `p` (dev_status,
- * wait_timeout_us and ATTN_FLAG_TEST_SKIP_LOAD do not apply: the split-KV
- * kernels have no inter-thread waits beyond block barriers). */
+/* attn_fwd_splitkv with query_offset, Hkv, flags, dev_status and
+ * wait_timeout_us from `p` (the latter two apply to the pipelined partial
+ * kernel used when several query rows share a K/V head; ATTN_FLAG_TEST_SKIP_LOAD
+ * applies to the prefill kernel only). */
 int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream);
 
