@@ -28,6 +28,8 @@ ATTN_ERR_CUDA = -5
 ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_FLAG_ALLOW_NEG_OFFSET = 1 << 0
 ATTN_FLAG_TEST_SKIP_LOAD = 1 << 1
+ATTN_QK_BF16 = 0
+ATTN_QK_E4M3 = 1
 
 EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_ex",
             "attn_combine", "attn_splitkv_workspace_bytes", "attn_get_device_status",
@@ -48,7 +50,8 @@ class attn_params(ctypes.Structure):
                 ("causal", ctypes.c_int), ("scale", ctypes.c_float),
                 ("query_offset", ctypes.c_int64), ("dev_status", ctypes.c_void_p),
                 ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
-                ("Hkv", ctypes.c_int64)]
+                ("Hkv", ctypes.c_int64), ("qk_dtype", ctypes.c_int),
+                ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float)]
 
 
 def load_library(path: str | None = None):
@@ -175,6 +178,33 @@ def attn_fwd_ex(q, k, v, causal: bool, scale: float, query_offset: int = 0, flag
     p = make_params(q, k, v, o, lse, causal, scale, query_offset, flags, dev_status,
                     wait_timeout_us)
     _check(load_library().attn_fwd_ex(ctypes.byref(p), _stream(stream)), "attn_fwd_ex")
+    return o, lse
+
+
+def attn_fwd_fp8(q8, k8, v, causal: bool, scale: float, q_descale: float, k_descale: float,
+                 query_offset: int = 0, o=None, lse=None, stream=None):
+    """Prefill with FP8 Q K^T: q8 [B,H,Nq,128], k8 [B,Hkv,Nk,128] e4m3 codes
+    (uint8 or float8_e4m3fn tensors), v bf16; scores are
+    scale * q_descale * k_descale * <q, k>.  Calls attn_fwd_ex."""
+    for name, t in (("q8", q8), ("k8", k8)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise ValueError(f"{name} must hold e4m3 codes (uint8 or float8_e4m3fn)")
+    _require(v, torch.bfloat16, "v")
+    B, H, Nq, d = q8.shape
+    if k8.dim() != 4 or tuple(v.shape) != tuple(k8.shape) or k8.shape[0] != B or k8.shape[3] != d:
+        raise ValueError("k8 and v must be [B, Hkv, Nk, d]")
+    if o is None:
+        o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    _require(o, torch.bfloat16, "o")
+    _require(lse, torch.float32, "lse")
+    p = attn_params(_ptr(q8), _ptr(k8), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, k8.shape[2], d,
+                    int(bool(causal)), float(scale), int(query_offset), 0, 0, 0,
+                    int(k8.shape[1]), ATTN_QK_E4M3, float(q_descale), float(k_descale))
+    _check(load_library().attn_fwd_ex(ctypes.byref(p), _stream(stream)), "attn_fwd_ex (fp8)")
     return o, lse
 
 

@@ -42,17 +42,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// [BH][N][d] bf16 viewed as a 3-D tensor (d fastest); 64 x 128 x 1 boxes with
-// the 128-byte swizzle the MMA descriptors expect; out-of-range rows read 0.
+// [BH][N][d] viewed as a 3-D tensor (d fastest) of 2-byte (bf16) or 1-byte
+// (e4m3) elements; boxes of 128 bytes x 128 rows x 1 with the 128-byte
+// swizzle the MMA descriptors expect; out-of-range rows read 0.
 bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* ptr,
-                int64_t N, int64_t BH, int64_t d) {
+                int64_t N, int64_t BH, int64_t d, int elem_bytes = 2) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(N * d * 2)};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * elem_bytes),
+                           static_cast<cuuint64_t>(N * d * elem_bytes)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem_bytes), 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(map, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                   3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -96,6 +99,14 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   const int64_t BH = p->B * p->H;
   const int64_t blocks = BH * ((p->Nq + kFwdRowsPerCta - 1) / kFwdRowsPerCta);
   if (blocks > kMaxDim) return ATTN_ERR_UNSUPPORTED;
+  const bool fp8 = p->qk_dtype == ATTN_QK_E4M3;
+  if (p->qk_dtype != ATTN_QK_BF16 && !fp8) return ATTN_ERR_INVALID;
+  if (fp8) {
+    if (!std::isfinite(p->q_descale) || !(p->q_descale > 0.0f) ||
+        !std::isfinite(p->k_descale) || !(p->k_descale > 0.0f))
+      return ATTN_ERR_INVALID;
+    if (p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  }
 
   int* status = p->dev_status;
   if (status == nullptr && default_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -104,8 +115,9 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
   const int64_t BHkv = p->B * Hkv;
   CUtensorMap tq, tk, tv;
-  if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d) ||
-      !encode_map(enc, &tk, p->k, p->Nk, BHkv, p->d) ||
+  const int qk_bytes = fp8 ? 1 : 2;
+  if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d, qk_bytes) ||
+      !encode_map(enc, &tk, p->k, p->Nk, BHkv, p->d, qk_bytes) ||
       !encode_map(enc, &tv, p->v, p->Nk, BHkv, p->d))
     return ATTN_ERR_CUDA;
 
@@ -121,7 +133,9 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   a.group = p->H / Hkv;
   a.d = static_cast<int>(p->d);
   a.causal = p->causal ? 1 : 0;
-  a.scale = p->scale;
+  a.fp8_qk = fp8 ? 1 : 0;
+  a.scale = fp8 ? static_cast<float>(static_cast<double>(p->scale) * p->q_descale * p->k_descale)
+                : p->scale;
   a.flags = p->flags;
   a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
   return launch_fwd_tcgen05(a, tq, tk, tv, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -183,6 +197,7 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   int rc = validate(p);
   if (rc != ATTN_OK) return rc;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
+  if (p->qk_dtype != ATTN_QK_BF16) return ATTN_ERR_UNSUPPORTED;
   const size_t need = attn_splitkv_workspace_bytes(p->B, p->H, p->Nq, p->d, num_splits);
   if (need == 0) return ATTN_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;

@@ -20,6 +20,7 @@
 //               NS-stage shared-memory ring (full/empty mbarriers).
 //   warp 8      MMA issuer (one thread): S_X = Q_X K^T into TMEM (SS MMA), and
 //               O_X += P_X V (TS MMA, P read from TMEM) for X in {A, B},
+//               (With FP8 Q and K, S comes from kind::f8f6f4 MMAs instead.)
 //               ordered so that the tensor core works on one tile while the
 //               other tile's softmax runs (ping-pong).
 //   warps 0-3   softmax of tile A; warps 4-7 softmax of tile B.  One thread
@@ -50,12 +51,15 @@ constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows by > 2^8
 
-template <int D>
+template <int D, bool FP8>
 struct Cfg {
-  static constexpr int kAtoms = D / 64;                     // 128-byte swizzle atoms per row
-  static constexpr uint32_t kAtomBytes = 128u * 128u;       // one [128 rows][64 bf16] box
-  static constexpr uint32_t kQBytes = BM * D * 2;           // one Q tile
-  static constexpr uint32_t kKVBytes = BN * D * 2;          // one K or V tile
+  static constexpr int kQKElem = FP8 ? 1 : 2;               // bytes per Q/K element
+  static constexpr int kQKAtoms = D * kQKElem / 128;        // 128-byte swizzle atoms per Q/K row
+  static constexpr int kVAtoms = D / 64;                    // ... per V row (bf16)
+  static constexpr uint32_t kAtomBytes = 128u * 128u;       // one [128 rows][128 B] box
+  static constexpr uint32_t kQBytes = BM * D * kQKElem;     // one Q tile
+  static constexpr uint32_t kKBytes = BN * D * kQKElem;     // one K tile
+  static constexpr uint32_t kKVBytes = BN * D * 2;          // one ring stage (a V tile)
   static constexpr int kStages = (D == 128) ? 4 : 8;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQBytes;
@@ -74,7 +78,7 @@ struct Cfg {
   static constexpr uint32_t kColS = 0;      // + 128 * tile
   static constexpr uint32_t kColO = 256;    // + D * tile
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);
+  static constexpr uint32_t kIdescQK = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kSmemBytes > 232448 / 2, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
@@ -129,12 +133,12 @@ __device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
   return static_cast<int>(min(n_all, last_key / BN + 1));
 }
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tcgen05_kernel(const __grid_constant__ CUtensorMap tq,
                             const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv, const KParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -200,9 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar(C::kBarQ), qbytes);
       for (int x = 0; x < 2; ++x) {
         if (ntile[x] == 0) continue;
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sQ + x * C::kQBytes + a * C::kAtomBytes, &tq, bar(C::kBarQ), a * 64,
-                      static_cast<int>(q0 + x * BM), static_cast<int>(bh));
+        for (int a = 0; a < C::kQKAtoms; ++a)
+          tma_load_3d(sQ + x * C::kQBytes + a * C::kAtomBytes, &tq, bar(C::kBarQ),
+                      a * (128 / C::kQKElem), static_cast<int>(q0 + x * BM),
+                      static_cast<int>(bh));
       }
       // Ring position t: K(t/2) for even t, V(t/2) for odd t.
       int last_t[C::kStages];
@@ -218,12 +223,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           skipped = t;
           continue;
         }
-        mbar_arrive_expect_tx(bar(C::kBarFull + s), C::kKVBytes);
-        const CUtensorMap* map = (t & 1) ? &tv : &tk;
+        const bool is_v = (t & 1) != 0;
+        mbar_arrive_expect_tx(bar(C::kBarFull + s), is_v ? C::kKVBytes : C::kKBytes);
         const int key0 = (t >> 1) * BN;
-        for (int a = 0; a < C::kAtoms; ++a)
-          tma_load_3d(sKV + s * C::kKVBytes + a * C::kAtomBytes, map, bar(C::kBarFull + s),
-                      a * 64, key0, static_cast<int>(bkv));
+        const int atoms = is_v ? C::kVAtoms : C::kQKAtoms;
+        const int per_atom = is_v ? 64 : 128 / C::kQKElem;  // elements per 128-byte row
+        for (int a = 0; a < atoms; ++a)
+          tma_load_3d(sKV + s * C::kKVBytes + a * C::kAtomBytes, is_v ? &tv : &tk,
+                      bar(C::kBarFull + s), a * per_atom, key0, static_cast<int>(bkv));
       }
       // Every issued load must land before the CTA can exit.  Only this
       // thread arrives on the full barriers, so the phase of the last load
@@ -241,11 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_kv > 0) {
       auto qk = [&](int x, int stage) {
         const uint32_t d_tmem = tmem + C::kColS + 128 * x;
-        for (int kk = 0; kk < D / 16; ++kk) {
+        // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
+        for (int kk = 0; kk < D * C::kQKElem / 32; ++kk) {
           const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
           const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes + off, 16, 1024);
           const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes + off, 16, 1024);
-          mma_ss(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            mma_ss_f8(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+          else
+            mma_ss(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto pv = [&](int x, int stage, bool acc) {
@@ -449,12 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                    const CUtensorMap& tv, cudaStream_t stream) {
-  using C = Cfg<D>;
+  using C = Cfg<D, FP8>;
   static_assert(C::kSmemBytes < (1u << 20), "");
-  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D>,
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
   if (err != cudaSuccess) return err;
@@ -473,7 +484,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.flags = a.flags;
   p.timeout_ns = a.timeout_ns;
   const int64_t blocks = a.BH * p.n_qblk;
-  attn_fwd_tcgen05_kernel<D><<<dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
+  attn_fwd_tcgen05_kernel<D, FP8><<<dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
                                C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -482,8 +493,9 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream) {
-  if (a.d == 64) return launch<64>(a, tq, tk, tv, stream);
-  return launch<128>(a, tq, tk, tv, stream);
+  if (a.fp8_qk) return launch<128, true>(a, tq, tk, tv, stream);
+  if (a.d == 64) return launch<64, false>(a, tq, tk, tv, stream);
+  return launch<128, false>(a, tq, tk, tv, stream);
 }
 
 }  // namespace attn

@@ -16,6 +16,7 @@ struct FwdArgs {
   int* status;         // device status word (bit 0 = wait timeout)
   int64_t BH, Nq, Nk, query_offset;
   int64_t H, group;    // query heads per batch; query heads per K/V head
+  int fp8_qk;          // Q and K are e4m3 (scale already includes the descales)
   int d;
   int causal;
   float scale;

@@ -91,3 +91,34 @@ def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = N
                 k[b, h, rows] = k[b, h, rows] * 4
     return q, k, v
 
+
+
+def make_qkv_fp8(w: Workload, device: str | torch.device = "cpu", Nq: int | None = None,
+                 Nk: int | None = None):
+    """FP8 Q K^T inputs: q, k as e4m3 codes (uint8 tensors) with per-tensor
+    descales, v as bfloat16.  The float32 draws of ``make_qkv``'s recipe are
+    divided by amax / 448 (e4m3's largest finite value) and rounded to e4m3
+    by torch's converter; returns (q8, k8, v, q_descale, k_descale)."""
+    Nq = w.Nq if Nq is None else Nq
+    Nk = w.Nk if Nk is None else Nk
+    g = torch.Generator(device=device).manual_seed(w.seed + 7919)
+
+    def draw(n, heads):
+        return torch.randn((w.B, heads, n, w.d), generator=g, device=device, dtype=torch.float32)
+
+    def quantise(x):
+        descale = float(x.abs().max()) / 448.0
+        codes = (x / descale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        return codes, descale
+
+    q8, qd = quantise(draw(Nq, w.H))
+    k32 = draw(Nk, w.kv_heads)
+    if w.k_boost_frac > 0.0:
+        n_boost = math.ceil(w.k_boost_frac * Nk)
+        for b in range(w.B):
+            for h in range(w.kv_heads):
+                rows = torch.randperm(Nk, generator=g, device=device)[:n_boost]
+                k32[b, h, rows] *= 4
+    k8, kd = quantise(k32)
+    v = draw(Nk, w.kv_heads).to(torch.bfloat16)
+    return q8, k8, v, qd, kd

@@ -411,6 +411,28 @@ def main():
                            "l2": "inputs > L2" if wo.Nq >= 8192 else
                                  "L2 flushed (256 MB rewrite) before each timed launch"})
 
+        # ---- long prefill causal with FP8 (e4m3) Q K^T, P V in bf16
+        wf = W.LONG_PREFILL_CAUSAL
+        q8, k8, v8, qdesc, kdesc = W.make_qkv_fp8(wf)
+        q8, k8, v8 = q8.to(dev), k8.to(dev), v8.to(dev)
+        of = torch.empty((wf.B, wf.H, wf.Nq, wf.d), dtype=torch.bfloat16, device=dev)
+        lf = torch.empty((wf.B, wf.H, wf.Nq), dtype=torch.float32, device=dev)
+
+        def sf():
+            binding.attn_fwd_fp8(q8, k8, v8, True, wf.scale, qdesc, kdesc, o=of, lse=lf,
+                                 stream=stream)
+
+        for _ in range(args.warmup):
+            sf()
+        mf = max_over_ranks(event_time(sf, args.steps, stream))
+        launches += args.steps
+        tff = prefill_flops(wf) / (mf / 1e3) / 1e12
+        others.append({"workload": wf.name + ", FP8 e4m3 Q K^T (P V bf16)", "metric": "TFLOPS",
+                       "value": world * tff, "ms_per_step": mf,
+                       "frac_of_bf16_peak": tff / pk["bf16_tflops"],
+                       "l2": "inputs (269 MB) larger than L2"})
+        del q8, k8, v8, of, lf
+
         # ---- decode (split-KV + combine), memory bound; MHA and grouped K/V heads
         def run_decode(wd):
             nonlocal launches

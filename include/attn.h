@@ -75,7 +75,8 @@ enum {
 /* Full argument set of the prefill entry point (attn_fwd_ex) and of the
  * split-KV entry point (attn_fwd_splitkv_ex).  Grouped K/V heads (GQA/MQA,
  * among FlashAttention's production features in "GPU Kernels: CUDA, HIP &
- * Triton", section 7.6) are available through these two entry points. */
+ * Triton", section 7.6) are available through these two entry points, and
+ * so is FP8 Q K^T (the same section's FP8 mode) for the prefill kernel. */
 typedef struct attn_params {
   const void* q;          /* bf16 [B][H][Nq][d], device                    */
   const void* k;          /* bf16 [B][Hkv][Nk][d], device                  */
@@ -93,7 +94,16 @@ typedef struct attn_params {
   int64_t Hkv;            /* K/V heads (grouped-query / multi-query attention):
                              K and V are [B][Hkv][Nk][d] and query head h reads
                              K/V head h / (H / Hkv); H % Hkv == 0.  0 = H.  */
+  int qk_dtype;           /* ATTN_QK_BF16 (0) or ATTN_QK_E4M3 (prefill only,
+                             d = 128): Q and K are FP8 e4m3 (1 byte each) and
+                             the scores are scale * q_descale * k_descale *
+                             <q, k>; V stays bf16.                          */
+  float q_descale;        /* per-tensor factors of the FP8 Q and K; finite, */
+  float k_descale;        /* > 0 (ignored for bf16)                         */
 } attn_params;
+
+/* attn_params.qk_dtype */
+enum { ATTN_QK_BF16 = 0, ATTN_QK_E4M3 = 1 };
 
 /*
  * Prefill / general forward: O and LSE for all rows, query_offset = 0.

@@ -77,7 +77,8 @@ def test_fwd_rejects(lib, kw, code):
 
 def _params(**kw):
     base = dict(q=A16, k=A16, v=A16, o=A16, lse=A16, B=1, H=1, Nq=8, Nk=8, d=64, causal=1,
-                scale=0.125, query_offset=0, dev_status=None, flags=0, wait_timeout_us=0, Hkv=0)
+                scale=0.125, query_offset=0, dev_status=None, flags=0, wait_timeout_us=0, Hkv=0,
+                qk_dtype=0, q_descale=0.0, k_descale=0.0)
     base.update(kw)
     return binding.attn_params(**base)
 
@@ -96,6 +97,20 @@ def test_grouped_heads_must_divide(lib, H, Hkv):
     assert lib.attn_fwd_ex(ctypes.byref(p), None) == binding.ATTN_ERR_INVALID
     need = lib.attn_splitkv_workspace_bytes(1, H, 8, 64, 2)
     assert lib.attn_fwd_splitkv_ex(ctypes.byref(p), 2, A16, need, None) == binding.ATTN_ERR_INVALID
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(qk_dtype=1, q_descale=1.0, k_descale=1.0, d=64), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(qk_dtype=1, q_descale=0.0, k_descale=1.0, d=128), binding.ATTN_ERR_INVALID),
+    (dict(qk_dtype=1, q_descale=1.0, k_descale=float("nan"), d=128), binding.ATTN_ERR_INVALID),
+    (dict(qk_dtype=2, q_descale=1.0, k_descale=1.0, d=128), binding.ATTN_ERR_INVALID),
+])
+def test_fp8_arguments(lib, kw, code):
+    p = _params(**kw)
+    assert lib.attn_fwd_ex(ctypes.byref(p), None) == code
+    if code == binding.ATTN_ERR_UNSUPPORTED:
+        need = lib.attn_splitkv_workspace_bytes(1, 1, 8, 64, 2)
+        assert lib.attn_fwd_splitkv_ex(ctypes.byref(p), 2, A16, need, None) == code
 
 
 def test_workspace_bytes(lib):

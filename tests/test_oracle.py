@@ -47,3 +47,20 @@ def test_thread_count_does_not_change_bits():
     a = oracle.attention(q, k, v, causal=False, scale=0.3, threads=1)
     b = oracle.attention(q, k, v, causal=False, scale=0.3, threads=7)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_e4m3_decoder_matches_the_format_and_torch():
+    """The oracle's e4m3 decoder: spec values, and torch's converter on all codes."""
+    import torch
+    from oracle.fp8 import decode_e4m3
+    assert decode_e4m3(0x7E) == 448.0          # largest finite
+    assert decode_e4m3(0x08) == 2.0 ** -6      # smallest normal
+    assert decode_e4m3(0x01) == 2.0 ** -9      # smallest subnormal
+    assert decode_e4m3(0x38) == 1.0 and decode_e4m3(0xB8) == -1.0
+    assert np.isnan(decode_e4m3(0x7F)) and np.isnan(decode_e4m3(0xFF))
+    codes = np.arange(256, dtype=np.uint8)
+    ours = decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    finite = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), ~finite)
+    assert np.array_equal(ours[finite], ref[finite])
