@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--decode-profile-batch", type=int, default=0,
                     help="run only the split-KV decode workload with this batch size "
                          "(smaller cases for ncu captures) and print its GB/s")
+    ap.add_argument("--decode-profile-gqa", action="store_true",
+                    help="with --decode-profile-batch: the grouped-K/V-head decode workload")
     return ap.parse_args()
 
 
@@ -303,9 +305,10 @@ def main():
 
     if args.decode_profile_batch > 0:
         # Decode only, smaller batch: the case the ncu captures run on.
-        wd = W.Workload(W.DECODE.name.replace("B16", f"B{args.decode_profile_batch}"),
-                        args.decode_profile_batch, W.DECODE.H, 1, W.DECODE.Nk, W.DECODE.d,
-                        False, W.DECODE.seed)
+        base = W.DECODE_GQA if args.decode_profile_gqa else W.DECODE
+        wd = W.Workload(base.name.replace("B16", f"B{args.decode_profile_batch}"),
+                        args.decode_profile_batch, base.H, 1, base.Nk, base.d,
+                        False, base.seed, Hkv=base.Hkv)
         qd, kd, vd = W.make_qkv(wd, device=dev)
         od = torch.empty_like(qd)
         ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
