@@ -25,6 +25,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
+_SRC_BWD = os.path.join(_HERE, "oracle_bwd.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -38,7 +39,7 @@ def build(out_path: str = _LIB_PATH, plant: int = 0) -> str:
     ``plant`` > 0 builds a deliberately wrong variant for the pin tests.
     """
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
-           "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", out_path, "-lm"]
+           "-fno-fast-math", "-ffp-contract=off", _SRC, _SRC_BWD, "-o", out_path, "-lm"]
     if plant:
         cmd.insert(1, f"-DORACLE_PLANT={int(plant)}")
     subprocess.run(cmd, check=True)
@@ -47,7 +48,8 @@ def build(out_path: str = _LIB_PATH, plant: int = 0) -> str:
 
 def _stale() -> bool:
     return (not os.path.exists(_LIB_PATH)
-            or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+            or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC),
+                                                 os.path.getmtime(_SRC_BWD)))
 
 
 def load(path: str | None = None):
@@ -74,6 +76,10 @@ def _declare(lib) -> None:
                   ctypes.c_int, i64, ctypes.c_double, i64, i64, vp, i64, vp,
                   vp, ctypes.c_int]
     lib.oracle_plant.restype = ctypes.c_int
+    b = lib.oracle_attention_bwd
+    b.restype = ctypes.c_int
+    b.argtypes = [vp, vp, vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64,
+                  ctypes.c_double, vp, vp, vp, ctypes.c_int]
 
 
 def _as_array(x):
@@ -151,3 +157,31 @@ def attention(q, k, v, *, causal: bool, scale: float, query_offset: int = 0,
     if rows_a is None:
         return o.reshape(B, H, Nq, dv), lse.reshape(B, H, Nq)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, *, causal: bool, scale: float, query_offset: int = 0,
+                  threads: int | None = None, lib=None):
+    """Dense fp64 gradients (dq, dk, dv) of softmax attention for the loss
+    gradient ``dout`` on O; q, dout [B, H, Nq, d], k, v [B, Hkv, Nk, d]."""
+    lib = lib or load()
+    qa, qe = _as_array(q)
+    ka, ke = _as_array(k)
+    va, ve = _as_array(v)
+    da, de = _as_array(dout)
+    if not (qe == ke == ve == de):
+        raise ValueError("q, k, v and dout must share one element type")
+    B, H, Nq, d = qa.shape
+    Bk, Hkv, Nk, dk_ = ka.shape
+    if (Bk, dk_) != (B, d) or va.shape != ka.shape or da.shape != qa.shape or H % Hkv != 0:
+        raise ValueError("incompatible shapes")
+    dq = np.empty((B, H, Nq, d), dtype=np.float64)
+    dk = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    dv = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    rc = lib.oracle_attention_bwd(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
+                                  da.ctypes.data, qe, B, H, Hkv, Nq, Nk, d, int(bool(causal)),
+                                  int(query_offset), float(scale), dq.ctypes.data,
+                                  dk.ctypes.data, dv.ctypes.data,
+                                  int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle_attention_bwd rejected its arguments (status {rc})")
+    return dq, dk, dv

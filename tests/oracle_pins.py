@@ -326,4 +326,104 @@ def pin_grouped_heads_equal_replicated_heads(lib):
             assert np.array_equal(o1, o2) and np.array_equal(l1, l2), f"Hkv={hkv}"
 
 
+def _bwd(lib, q, k, v, g, causal, scale, offset=0):
+    return oracle.attention_bwd(q, k, v, g, causal=causal, scale=scale, query_offset=offset,
+                                threads=2, lib=lib)
+
+
+def pin_bwd_finite_differences(lib):
+    """Gradients against central finite differences of L = sum(O * G) in fp64
+    (the lab's check: perturb Q, K, V separately in random directions)."""
+    rng = np.random.default_rng(21)
+    cases = []
+    q, k, v = (rng.normal(size=s)[None, None] for s in ((7, 5), (11, 5), (11, 5)))
+    cases += [(q, k, v, True, 0), (q, k, v, True, 2), (q, k, v, False, 0)]
+    q = rng.normal(size=(1, 4, 6, 4)); k = rng.normal(size=(1, 2, 9, 4))
+    v = rng.normal(size=(1, 2, 9, 4))
+    cases += [(q, k, v, False, 0), (q, k, v, True, 3)]
+    eps = 1e-5
+    for q, k, v, causal, off in cases:
+        scale = 0.6
+        g = rng.normal(size=q.shape)
+        dq, dk, dv = _bwd(lib, q, k, v, g, causal, scale, off)
+
+        def loss(qq, kk, vv):
+            o, _ = _att(lib, qq, kk, vv, causal, scale, off)
+            return float((o * g).sum())
+
+        for name, x, dx in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            u = rng.normal(size=x.shape)
+            args_p = [q, k, v]; args_m = [q, k, v]
+            i = "qkv".index(name)
+            args_p[i] = x + eps * u
+            args_m[i] = x - eps * u
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            an = float((dx * u).sum())
+            assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), f"d{name}: fd {fd} vs {an}"
+
+
+def backward_reference(q, k, v, g, o, lse, tile, causal, scale, offset):
+    """Test-only restatement of the lab's recomputing backward for one head:
+    P recomputed tile by tile as exp(scores - LSE), row correction
+    rowsum(G * O); q, g [Nq, d], k, v [Nk, d]."""
+    Nq, Nk = q.shape[0], k.shape[0]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    corr = (g * o).sum(axis=1)
+    valid = np.isfinite(lse)
+    ref = np.where(valid, lse, 0.0)
+    for start in range(0, Nk, tile):
+        kt, vt = k[start:start + tile], v[start:start + tile]
+        s = (q @ kt.T) * scale
+        if causal:
+            keys = np.arange(start, start + len(kt))[None, :]
+            s = np.where(keys > np.arange(Nq)[:, None] + offset, -np.inf, s)
+        p = np.exp(s - ref[:, None])
+        p[~valid] = 0.0
+        ds = p * (g @ vt.T - corr[:, None])
+        dq += (ds @ kt) * scale
+        dk[start:start + tile] += (ds.T @ q) * scale
+        dv[start:start + tile] += p.T @ g
+    return dq, dk, dv
+
+
+def pin_bwd_tiled_recompute(lib):
+    """The lab's tiled backward (tiles 1, 4, > Nk, recompute from LSE, row
+    correction rowsum(dO * O)) equals the dense definition."""
+    rng = np.random.default_rng(22)
+    q, k, v = (_bf16_like(rng, s) for s in ((9, 8), (13, 8), (13, 8)))
+    g = _bf16_like(rng, (9, 8))
+    for causal, off in ((True, 0), (True, 4), (False, 0), (True, -3)):
+        o, lse = _att(lib, q[None, None], k[None, None], v[None, None], causal, 0.45, off)
+        ref = _bwd(lib, q[None, None], k[None, None], v[None, None], g[None, None], causal,
+                   0.45, off)
+        for tile in (1, 4, 20):
+            mine = backward_reference(q, k, v, g, o[0, 0], lse[0, 0], tile, causal, 0.45, off)
+            for name, a, b in zip("qkv", ref, mine):
+                _close(a[0, 0], b, 1e-11, f"d{name} tile={tile} causal={causal} off={off}")
+
+
+def pin_bwd_single_key(lib):
+    """One key: P = 1, so dS = 0 (dQ = dK = 0 exactly) and dV = sum of dO."""
+    rng = np.random.default_rng(23)
+    q = _bf16_like(rng, (2, 4, 5, 8)); k = _bf16_like(rng, (2, 2, 1, 8))
+    v = _bf16_like(rng, (2, 2, 1, 8)); g = _bf16_like(rng, (2, 4, 5, 8))
+    dq, dk, dv = _bwd(lib, q, k, v, g, False, 0.3)
+    assert np.array_equal(dq, np.zeros_like(dq)) and np.array_equal(dk, np.zeros_like(dk))
+    expect = g.reshape(2, 2, 2 * 5, 8).sum(axis=2, keepdims=True)
+    _close(dv, expect, 1e-15, "single key dV")
+
+
+def pin_bwd_masked_rows_and_keys(lib):
+    """Rows without admissible keys get zero dQ; keys no row can see get zero
+    dK and dV (exact zeros)."""
+    rng = np.random.default_rng(24)
+    q = _bf16_like(rng, (1, 2, 6, 8)); k = _bf16_like(rng, (1, 2, 10, 8))
+    v = _bf16_like(rng, (1, 2, 10, 8)); g = _bf16_like(rng, (1, 2, 6, 8))
+    dq, dk, dv = _bwd(lib, q, k, v, g, True, 0.5, offset=-2)
+    assert np.all(dq[:, :, :2] == 0.0) and np.any(dq[:, :, 2:] != 0.0)
+    # rows 0..5 with offset -2 see keys <= 3; keys 4..9 are never attended
+    assert np.all(dk[:, :, 4:] == 0.0) and np.all(dv[:, :, 4:] == 0.0)
+    assert np.any(dk[:, :, :4] != 0.0) and np.any(dv[:, :, :4] != 0.0)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -12,7 +12,8 @@ from tests import oracle_pins
 
 PLANTS = {1: "causal mask dropped", 2: "mask off by one", 3: "exponent sign",
           4: "no normalisation", 5: "transposed K", 6: "LSE without max",
-          7: "grouped K/V heads mapped round-robin"}
+          7: "grouped K/V heads mapped round-robin",
+          8: "backward: softmax row correction dropped", 9: "backward: scale missing from dK"}
 
 
 @pytest.mark.parametrize("plant", sorted(PLANTS), ids=lambda p: PLANTS[p])
