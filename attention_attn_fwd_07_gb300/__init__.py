@@ -12,7 +12,8 @@ from __future__ import annotations
 __all__ = [
     "attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_ex",
     "attn_combine", "attn_splitkv_workspace_bytes", "attn_get_device_status",
-    "attn_status_string", "AttnError", "load_library",
+    "attn_status_string", "AttnError", "load_library", "attn_bwd",
+    "attn_bwd_workspace_bytes", "attn_fwd_fp8",
 ]
 
 

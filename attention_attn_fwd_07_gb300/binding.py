@@ -33,7 +33,7 @@ ATTN_QK_E4M3 = 1
 
 EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_ex",
             "attn_combine", "attn_splitkv_workspace_bytes", "attn_get_device_status",
-            "attn_status_string")
+            "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes")
 
 
 class AttnError(RuntimeError):
@@ -52,6 +52,17 @@ class attn_params(ctypes.Structure):
                 ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
                 ("Hkv", ctypes.c_int64), ("qk_dtype", ctypes.c_int),
                 ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float)]
+
+
+class attn_bwd_params(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("dout", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Hkv", ctypes.c_int64),
+                ("Nq", ctypes.c_int64), ("Nk", ctypes.c_int64), ("d", ctypes.c_int64),
+                ("causal", ctypes.c_int), ("scale", ctypes.c_float),
+                ("query_offset", ctypes.c_int64), ("dev_status", ctypes.c_void_p),
+                ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32)]
 
 
 def load_library(path: str | None = None):
@@ -82,6 +93,10 @@ def load_library(path: str | None = None):
         lib.attn_combine.restype = c_int
         lib.attn_get_device_status.argtypes = [ctypes.POINTER(c_int), vp]
         lib.attn_get_device_status.restype = c_int
+        lib.attn_bwd.argtypes = [ctypes.POINTER(attn_bwd_params), vp, ctypes.c_size_t, vp]
+        lib.attn_bwd.restype = c_int
+        lib.attn_bwd_workspace_bytes.argtypes = [i64, i64, i64]
+        lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.attn_status_string.argtypes = [c_int]
         lib.attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -288,3 +303,33 @@ def fwd_from_host(q_host, k_host, v_host, causal: bool, scale: float, q_dev, k_d
         o_host.copy_(o_dev, non_blocking=True)
         lse_host.copy_(lse_dev, non_blocking=True)
     return o_host, lse_host
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, Nq: int) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(B, H, Nq))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, query_offset: int = 0,
+             flags: int = 0, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Backward pass: returns (dq, dk, dv) bf16 for the loss gradient dout on o."""
+    B, H, Nq, Nk, d = _shape(q, k, v)
+    _require(o, torch.bfloat16, "o")
+    _require(dout, torch.bfloat16, "dout")
+    _require(lse, torch.float32, "lse")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have the shape of q")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _require(t, torch.bfloat16, name)
+    need = attn_bwd_workspace_bytes(B, H, Nq)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    p = attn_bwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                        _ptr(dk), _ptr(dv), B, H, k.shape[1], Nq, Nk, d, int(bool(causal)),
+                        float(scale), int(query_offset), 0, int(flags), 0)
+    rc = load_library().attn_bwd(ctypes.byref(p), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
-SOURCES = ["api.cu", "fwd_tcgen05.cu", "splitkv.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd_tcgen05.cu", "splitkv.cu", "noalloc.cu", "bwd_tcgen05.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -257,6 +257,70 @@ extern "C" int attn_fwd_splitkv(const void* q, const void* k, const void* v, voi
   return attn_fwd_splitkv_ex(&p, num_splits, workspace, workspace_bytes, stream);
 }
 
+extern "C" size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq) {
+  if (B < 1 || H < 1 || Nq < 1 || B > kMaxDim || H > kMaxDim || Nq > kMaxDim ||
+      B * H > kMaxDim)
+    return 0;
+  return align256(static_cast<size_t>(B * H) * static_cast<size_t>(Nq) * 4);
+}
+
+extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  if (p == nullptr) return ATTN_ERR_INVALID;
+  if (!p->q || !p->k || !p->v || !p->o || !p->dout || !p->lse || !p->dq || !p->dk || !p->dv)
+    return ATTN_ERR_INVALID;
+  if (p->B < 1 || p->H < 1 || p->Nq < 1 || p->Nk < 1) return ATTN_ERR_INVALID;
+  if (!std::isfinite(p->scale) || !(p->scale > 0.0f)) return ATTN_ERR_INVALID;
+  if (p->query_offset < -kMaxOffset || p->query_offset > kMaxOffset) return ATTN_ERR_INVALID;
+  if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
+  if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
+  if (p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
+      p->Nk > kMaxDim)
+    return ATTN_ERR_UNSUPPORTED;
+  const void* ptrs16[] = {p->q, p->k, p->v, p->o, p->dout, p->dq, p->dk, p->dv};
+  for (const void* ptr : ptrs16)
+    if (!aligned(ptr, 16)) return ATTN_ERR_ALIGN;
+  if (!aligned(p->lse, 4)) return ATTN_ERR_ALIGN;
+  const size_t need = attn_bwd_workspace_bytes(p->B, p->H, p->Nq);
+  if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return ATTN_ERR_ALIGN;
+  const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
+  const int64_t BH = p->B * p->H, BHkv = p->B * Hkv;
+  if (BHkv * ((p->Nk + 127) / 128) > kMaxDim || BH * ((p->Nq + 127) / 128) > kMaxDim)
+    return ATTN_ERR_UNSUPPORTED;
+
+  int* status = p->dev_status;
+  if (status == nullptr && default_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d) ||
+      !encode_map(enc, &tdo, p->dout, p->Nq, BH, p->d) ||
+      !encode_map(enc, &tk, p->k, p->Nk, BHkv, p->d) ||
+      !encode_map(enc, &tv, p->v, p->Nk, BHkv, p->d))
+    return ATTN_ERR_CUDA;
+  BwdArgs a;
+  a.o = p->o;
+  a.dout = p->dout;
+  a.lse = p->lse;
+  a.delta = static_cast<float*>(workspace);
+  a.dq = p->dq;
+  a.dk = p->dk;
+  a.dv = p->dv;
+  a.status = status;
+  a.B = p->B;
+  a.H = p->H;
+  a.Hkv = Hkv;
+  a.Nq = p->Nq;
+  a.Nk = p->Nk;
+  a.query_offset = p->query_offset;
+  a.causal = p->causal ? 1 : 0;
+  a.scale = p->scale;
+  a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
+  return launch_bwd(a, tq, tk, tv, tdo, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 extern "C" int attn_get_device_status(int* dev_status_host, cudaStream_t stream) {
   if (dev_status_host == nullptr) return ATTN_ERR_INVALID;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;

@@ -1,0 +1,582 @@
+// bwd_tcgen05.cu -- attention backward (dQ, dK, dV) for sm_103a, d = 128.
+//
+// Gradients of O = softmax(S) V with S = scale * Q K^T [causal], from
+// "GPU Engineering: Correctness, Throughput, and Attention" (sections 22.5
+// and 22.7): dV = P^T dO, dP = dO V^T, dS = P * (dP - Delta) with the row
+// correction Delta = rowsum(dO * O) (the section 22.7 identity), dQ =
+// scale * dS K, dK = scale * dS^T Q; P is recomputed tile by tile from the
+// forward's log-sum-exp (P = exp(S - LSE)), never stored whole.
+//
+// Three launches, no atomics (the two gradient kernels each own their
+// output rows, so the result is deterministic):
+//   bwd_delta_kernel   Delta_i = sum_c dO_ic O_ic, one warp per query row.
+//   bwd_dkdv_kernel    one CTA per (b, K/V head, 128-key tile), K and V
+//                      resident in shared memory, streaming (Q, dO) tiles of
+//                      every query head of the group:
+//                        S^T  = K Q^T,  dP^T = V dO^T      (SS MMA -> TMEM)
+//                        P^T  = exp2(S^T * scale*log2e - LSE*log2e)
+//                        dS^T = P^T * (dP^T - Delta)       (elementwise warps)
+//                        dV  += P^T dO,  dK += dS^T Q       (TS MMA, A = TMEM)
+//                      TMEM: S^T [0,128) dP^T [128,256) dV [256,384) dK [384,512);
+//                      P^T and dS^T overwrite S^T and dP^T as bf16.
+//   bwd_dq_kernel      one CTA per (b, h, 128-query tile), Q and dO resident,
+//                      streaming (K, V) tiles: S = Q K^T, dP = dO V^T,
+//                      dS = P * (dP - Delta), dQ += dS K.
+//                      TMEM: S [0,128) dP [128,256) dQ [256,384).
+// Warp roles in both: warps 0-3 elementwise (one thread per TMEM lane = row),
+// warp 4 single-thread MMA issuer, warp 5 TMA producer.  Every mbarrier wait
+// is bounded; a timeout sets the status word and the CTA leaves cleanly.
+#include <cuda_bf16.h>
+
+#include "attn.h"
+#include "internal.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int D = 128;
+constexpr int T = 128;                    // rows per query tile and per key tile
+constexpr int kThreads = 192;
+constexpr int kWarpMma = 4;
+constexpr int kWarpLoad = 5;
+constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
+constexpr uint32_t kTileBytes = T * D * 2;    // one [128][128] bf16 tile (2 atoms)
+constexpr int kStages = 2;                    // streamed tile pairs in flight
+constexpr uint32_t kIdescSS = idesc_bf16_f32(T, T, 0);  // both operands K-major
+constexpr uint32_t kIdescTS = idesc_bf16_f32(T, D, 1);  // B (N = d) MN-major
+constexpr float kLog2e = 1.4426950408889634074f;
+
+// Shared memory: 2 resident tiles, kStages x 2 streamed tiles, then the
+// per-tile row statistics, barriers and bookkeeping.
+constexpr uint32_t kOffRes = 0;
+constexpr uint32_t kOffRing = 2 * kTileBytes;
+constexpr uint32_t kOffStat = kOffRing + kStages * 2 * kTileBytes;  // 2 x [2][128] floats
+constexpr uint32_t kOffBar = kOffStat + 2 * 2 * T * 4;
+// barriers: res_full, full[2], empty[2], s_full, p_ready, acc_full, drain,
+// stats_ready[2] (dK/dV kernel: per-tile row statistics written by the 128
+// elementwise threads, one arrival each)
+constexpr int kBarRes = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 6, kBarAcc = 7,
+              kBarDrain = 8, kBarStat = 9, kNumBars = 11;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+static_assert(kSmemBytes <= 232448 && kSmemBytes > 232448 / 2, "one CTA per SM");
+
+struct BwdParams {
+  const __nv_bfloat16 *o, *dout;
+  const float* lse;
+  float* delta;
+  __nv_bfloat16 *dq, *dk, *dv;
+  int* status;
+  int64_t B, H, Hkv, Nq, Nk, qoff;
+  int causal;
+  float scale;
+  float sc_log2;  // scale * log2(e)
+  uint64_t timeout_ns;
+};
+
+struct Waiter {
+  volatile int* abort_flag;
+  int* status;
+  uint64_t timeout_ns;
+  __device__ __forceinline__ bool operator()(uint32_t bar, uint32_t parity) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+      if (mbar_try_wait(bar, parity)) return true;
+      if ((spin & 31u) == 0) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+          *abort_flag = 1;
+          atomicOr(status, 1);
+          return false;
+        }
+      }
+    }
+  }
+};
+
+// K-major SW128 operand (rows = M or N, 128 x 128 bf16 tile): K step kk.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+  return sdesc_sw128(tile + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
+}
+// MN-major SW128 operand (rows = K, N = d contiguous): K step kk (16 rows).
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+  return sdesc_sw128(tile + kk * 16 * 128, kAtomBytes, 1024);
+}
+
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int row, int64_t z) {
+  for (int a = 0; a < 2; ++a)
+    tma_load_3d(dst + a * kAtomBytes, map, bar, a * 64, row, static_cast<int>(z));
+}
+
+// Shared prologue: barriers, TMEM (512 columns), abort flag.
+struct Ctx {
+  uint8_t* smem;
+  uint32_t sbase;
+  uint32_t tmem;
+  volatile int* abort_flag;
+  __device__ __forceinline__ uint32_t bar(int i) const { return sbase + kOffBar + 8u * i; }
+};
+
+__device__ __forceinline__ Ctx prologue(uint8_t* smem_raw, int warp) {
+  Ctx c;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  c.smem = smem_raw + pad;
+  c.sbase = raw + pad;
+  c.abort_flag = reinterpret_cast<volatile int*>(c.smem + kOffMisc + 4);
+  if (threadIdx.x == 0) {
+    mbar_init(c.bar(kBarRes), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(c.bar(kBarFull + s), 1);
+      mbar_init(c.bar(kBarEmpty + s), 1);
+    }
+    mbar_init(c.bar(kBarS), 1);
+    mbar_init(c.bar(kBarP), 4);
+    mbar_init(c.bar(kBarAcc), 1);
+    mbar_init(c.bar(kBarDrain), 1);
+    mbar_init(c.bar(kBarStat + 0), 128);
+    mbar_init(c.bar(kBarStat + 1), 128);
+    *c.abort_flag = 0;
+    fence_barrier_init();
+  }
+  uint32_t* slot = reinterpret_cast<uint32_t*>(c.smem + kOffMisc);
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  c.tmem = *slot;
+  return c;
+}
+
+__device__ __forceinline__ void epilogue_sync(const Ctx& c, int warp) {
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(c.tmem, 512);
+  }
+}
+
+// Row statistics of one 128-query tile as the exponent offsets the
+// elementwise warps use: nl2[i] = -LSE_i*log2(e) (-inf where the row has no
+// admissible key or lies past Nq, so P = 0 there) and nd[i] = -Delta_i.
+__device__ __forceinline__ void load_stats(const BwdParams& p, int64_t row_base, int64_t q0,
+                                           int t, float* nl2, float* nd) {
+  const int64_t i = q0 + t;
+  float l2 = -INFINITY, dl = 0.0f;
+  if (i < p.Nq) {
+    const float lse = p.lse[row_base + i];
+    l2 = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
+    dl = -p.delta[row_base + i];
+  }
+  nl2[t] = l2;
+  nd[t] = dl;
+}
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
+                                               float mul, bool zero) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]) * mul, __uint_as_float(v[8 * q + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul);
+    if (zero) w = make_uint4(0u, 0u, 0u, 0u);
+    d4[q] = w;
+  }
+}
+
+// ======================================================================= Delta
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, int64_t rows) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (row >= rows) return;
+  const uint2 a = *reinterpret_cast<const uint2*>(o + row * D + 4 * lane);
+  const uint2 b = *reinterpret_cast<const uint2*>(dout + row * D + 4 * lane);
+  auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
+  auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
+  float acc = lo(a.x) * lo(b.x) + hi(a.x) * hi(b.x) + lo(a.y) * lo(b.y) + hi(a.y) * hi(b.y);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// ======================================================================= dK, dV
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Ctx c = prologue(smem_raw, warp);
+  const Waiter wait{c.abort_flag, p.status, p.timeout_ns};
+
+  // CTA -> (b, K/V head, key tile)
+  const int64_t n_kt = (p.Nk + T - 1) / T;
+  const int64_t bkv = blockIdx.x / n_kt;
+  const int64_t k0 = (blockIdx.x % n_kt) * T;
+  const int64_t b = bkv / p.Hkv, hk = bkv % p.Hkv, G = p.H / p.Hkv;
+  const int64_t n_qt = (p.Nq + T - 1) / T;
+  // First query tile whose rows can see a key of this tile (causal).
+  int64_t qt_first = 0;
+  if (p.causal) {
+    const int64_t need = k0 - p.qoff - (T - 1);  // smallest q0 with q0 + T - 1 + off >= k0
+    qt_first = need <= 0 ? 0 : (need + T - 1) / T;
+  }
+  const int64_t per_head = qt_first < n_qt ? n_qt - qt_first : 0;
+  const int64_t n_items = G * per_head;
+  auto item_rows = [&](int64_t n, int64_t& bh, int64_t& q0) {
+    const int64_t g = n / per_head;
+    bh = b * p.H + hk * G + g;
+    q0 = (qt_first + n % per_head) * T;
+  };
+
+  const uint32_t sK = c.sbase + kOffRes, sV = sK + kTileBytes;
+  auto sQ = [&](int s) { return c.sbase + kOffRing + s * 2 * kTileBytes; };
+  auto sdO = [&](int s) { return sQ(s) + kTileBytes; };
+  const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + 256, tdK = c.tmem + 384;
+
+  if (warp == kWarpLoad) {
+    if (lane == 0) {
+      int last = -1;
+      bool ok = true;
+      mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
+      load_tile(sK, &tk, c.bar(kBarRes), static_cast<int>(k0), bkv);
+      load_tile(sV, &tv, c.bar(kBarRes), static_cast<int>(k0), bkv);
+      for (int64_t n = 0; n < n_items && ok; ++n) {
+        const int s = static_cast<int>(n % kStages);
+        if (n >= kStages) ok = wait(c.bar(kBarEmpty + s), ((n / kStages) - 1) & 1);
+        if (!ok) break;
+        int64_t bh, q0;
+        item_rows(n, bh, q0);
+        mbar_arrive_expect_tx(c.bar(kBarFull + s), 2 * kTileBytes);
+        load_tile(sQ(s), &tq, c.bar(kBarFull + s), static_cast<int>(q0), bh);
+        load_tile(sdO(s), &tdo, c.bar(kBarFull + s), static_cast<int>(q0), bh);
+        last = static_cast<int>(n);
+      }
+      volatile int no_abort = 0;
+      const Waiter own{&no_abort, p.status, p.timeout_ns};
+      own(c.bar(kBarRes), 0);
+      for (int64_t n = last - kStages + 1; n <= last; ++n)
+        if (n >= 0) own(c.bar(kBarFull + static_cast<int>(n % kStages)), (n / kStages) & 1);
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0 && n_items > 0) {
+      bool ok = wait(c.bar(kBarRes), 0);
+      for (int64_t n = 0; n < n_items && ok; ++n) {
+        const int s = static_cast<int>(n % kStages);
+        ok = wait(c.bar(kBarFull + s), (n / kStages) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kk = 0; kk < D / 16; ++kk)  // S^T = K Q^T
+          mma_ss(tS, desc_kmajor(sK, kk), desc_kmajor(sQ(s), kk), kIdescSS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
+          mma_ss(tdP, desc_kmajor(sV, kk), desc_kmajor(sdO(s), kk), kIdescSS, kk > 0);
+        mma_commit(c.bar(kBarS));
+        ok = wait(c.bar(kBarP), n & 1);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kk = 0; kk < T / 16; ++kk)  // dV += P^T dO
+          mma_ts(tdV, tS + kk * 8, desc_mnmajor(sdO(s), kk), kIdescTS, (n > 0 || kk > 0));
+        for (int kk = 0; kk < T / 16; ++kk)  // dK += dS^T Q
+          mma_ts(tdK, tdP + kk * 8, desc_mnmajor(sQ(s), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit(c.bar(kBarEmpty + s));
+      }
+      if (ok) mma_commit(c.bar(kBarAcc));
+      mma_commit(c.bar(kBarDrain));
+      volatile int no_abort = 0;
+      const Waiter own{&no_abort, p.status, p.timeout_ns};
+      own(c.bar(kBarDrain), 0);
+    }
+  } else {
+    // ---------------------------------------------------------- elementwise
+    const int jl = (warp << 5) + lane;  // key row in the tile = TMEM lane
+    const int64_t j = k0 + jl;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float* nl2_buf = reinterpret_cast<float*>(c.smem + kOffStat);  // [2][2][128]
+    const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
+    bool ok = true;
+    for (int64_t n = 0; n < n_items; ++n) {
+      int64_t bh, q0;
+      item_rows(n, bh, q0);
+      float* nl2 = nl2_buf + (n & 1) * 2 * T;
+      float* nd = nl2 + T;
+      // Each thread writes one column's statistics; the four warps meet on
+      // a (bounded) mbarrier per tile, double-buffered by tile parity.
+      load_stats(p, bh * p.Nq, q0, jl, nl2, nd);
+      mbar_arrive(c.bar(kBarStat + (n & 1)));  // release: this thread's column is written
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarStat + (n & 1)), (n >> 1) & 1));
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
+      if (!ok) break;
+      tc_fence_after();
+      // Key j is visible to query i = q0 + col iff j < Nk and (not causal or
+      // j <= i + off), i.e. col >= thr.
+      const bool row_live = j < p.Nk;
+      const int64_t thr64 = p.causal ? j - q0 - p.qoff : -1;
+      const int thr = static_cast<int>(thr64 < -1 ? -1 : (thr64 > T ? T : thr64));
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_x32(tS + lane_off + 32 * ch, sr);
+        tmem_ld_x32(tdP + lane_off + 32 * ch, dr);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = 32 * ch + 2 * e;
+          const float2 l2 = *reinterpret_cast<const float2*>(nl2 + col);
+          const float2 dl = *reinterpret_cast<const float2*>(nd + col);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
+                           c2, f2_pack(l2.x, l2.y)),
+                    x0, x1);
+          if (!row_live || col < thr) x0 = -INFINITY;
+          if (!row_live || col + 1 < thr) x1 = -INFINITY;
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          float t0, t1;
+          f2_unpack(f2_mul(f2_pack(p0, p1),
+                           f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                                  f2_pack(dl.x, dl.y))),
+                    t0, t1);
+          pp[e] = pack_bf16x2(p0, p1);
+          pd[e] = pack_bf16x2(t0, t1);
+        }
+        // P^T over S^T and dS^T over dP^T, 16 packed columns per chunk (only
+        // columns this thread has already read are overwritten).
+        tmem_st_x16(tS + lane_off + 16 * ch, pp);
+        tmem_st_x16(tdP + lane_off + 16 * ch, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarP));
+    }
+    if (ok && n_items > 0) {
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarAcc), 0));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool valid = j < p.Nk;
+      const int64_t kv_row = bkv * p.Nk + j;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t kd[32] = {}, vd[32] = {};
+        if (n_items > 0) {
+          tmem_ld_x32(tdK + lane_off + 32 * cc, kd);
+          tmem_ld_x32(tdV + lane_off + 32 * cc, vd);
+        }
+        if (valid) {
+          store_row_bf16(p.dk + kv_row * D + 32 * cc, kd, p.scale, n_items == 0);
+          store_row_bf16(p.dv + kv_row * D + 32 * cc, vd, 1.0f, n_items == 0);
+        }
+      }
+    }
+  }
+  epilogue_sync(c, warp);
+}
+
+// ======================================================================= dQ
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Ctx c = prologue(smem_raw, warp);
+  const Waiter wait{c.abort_flag, p.status, p.timeout_ns};
+
+  const int64_t n_qt = (p.Nq + T - 1) / T;
+  const int64_t bh = blockIdx.x / n_qt;
+  const int64_t q0 = (blockIdx.x % n_qt) * T;
+  const int64_t b = bh / p.H, h = bh % p.H;
+  const int64_t bkv = b * p.Hkv + h / (p.H / p.Hkv);
+  int n_kt = static_cast<int>((p.Nk + T - 1) / T);
+  if (p.causal) {
+    const int64_t last_key = min(q0 + T - 1, p.Nq - 1) + p.qoff;
+    n_kt = last_key < 0 ? 0 : static_cast<int>(min(static_cast<int64_t>(n_kt), last_key / T + 1));
+  }
+
+  const uint32_t sQ = c.sbase + kOffRes, sdO = sQ + kTileBytes;
+  auto sK = [&](int s) { return c.sbase + kOffRing + s * 2 * kTileBytes; };
+  auto sV = [&](int s) { return sK(s) + kTileBytes; };
+  const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdQ = c.tmem + 256;
+
+  if (warp == kWarpLoad) {
+    if (lane == 0 && n_kt > 0) {
+      int last = -1;
+      bool ok = true;
+      mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
+      load_tile(sQ, &tq, c.bar(kBarRes), static_cast<int>(q0), bh);
+      load_tile(sdO, &tdo, c.bar(kBarRes), static_cast<int>(q0), bh);
+      for (int n = 0; n < n_kt && ok; ++n) {
+        const int s = n % kStages;
+        if (n >= kStages) ok = wait(c.bar(kBarEmpty + s), ((n / kStages) - 1) & 1);
+        if (!ok) break;
+        mbar_arrive_expect_tx(c.bar(kBarFull + s), 2 * kTileBytes);
+        load_tile(sK(s), &tk, c.bar(kBarFull + s), n * T, bkv);
+        load_tile(sV(s), &tv, c.bar(kBarFull + s), n * T, bkv);
+        last = n;
+      }
+      volatile int no_abort = 0;
+      const Waiter own{&no_abort, p.status, p.timeout_ns};
+      own(c.bar(kBarRes), 0);
+      for (int n = last - kStages + 1; n <= last; ++n)
+        if (n >= 0) own(c.bar(kBarFull + n % kStages), (n / kStages) & 1);
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0 && n_kt > 0) {
+      bool ok = wait(c.bar(kBarRes), 0);
+      for (int n = 0; n < n_kt && ok; ++n) {
+        const int s = n % kStages;
+        ok = wait(c.bar(kBarFull + s), (n / kStages) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kk = 0; kk < D / 16; ++kk)  // S = Q K^T
+          mma_ss(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(s), kk), kIdescSS, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)  // dP = dO V^T
+          mma_ss(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(s), kk), kIdescSS, kk > 0);
+        mma_commit(c.bar(kBarS));
+        ok = wait(c.bar(kBarP), n & 1);
+        if (!ok) break;
+        tc_fence_after();
+        for (int kk = 0; kk < T / 16; ++kk)  // dQ += dS K
+          mma_ts(tdQ, tS + kk * 8, desc_mnmajor(sK(s), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit(c.bar(kBarEmpty + s));
+      }
+      if (ok) mma_commit(c.bar(kBarAcc));
+      mma_commit(c.bar(kBarDrain));
+      volatile int no_abort = 0;
+      const Waiter own{&no_abort, p.status, p.timeout_ns};
+      own(c.bar(kBarDrain), 0);
+    }
+  } else {
+    // ---------------------------------------------------------- elementwise
+    const int il = (warp << 5) + lane;  // query row in the tile = TMEM lane
+    const int64_t i = q0 + il;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float nl2 = -INFINITY, nd = 0.0f;
+    if (i < p.Nq) {
+      const float lse = p.lse[bh * p.Nq + i];
+      nl2 = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
+      nd = -p.delta[bh * p.Nq + i];
+    }
+    const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
+    const uint64_t l22 = f2_pack(nl2, nl2);
+    const uint64_t nd2 = f2_pack(nd, nd);
+    // Last admissible key of this row.
+    const int64_t lim = p.causal ? min(p.Nk - 1, i + p.qoff) : p.Nk - 1;
+    bool ok = true;
+    for (int n = 0; n < n_kt; ++n) {
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t k0 = static_cast<int64_t>(n) * T;
+      const int64_t rel64 = lim - k0;
+      const int rel = static_cast<int>(rel64 < -1 ? -1 : (rel64 > T ? T : rel64));
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_x32(tS + lane_off + 32 * ch, sr);
+        tmem_ld_x32(tdP + lane_off + 32 * ch, dr);
+        uint32_t pd[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = 32 * ch + 2 * e;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
+                           c2, l22),
+                    x0, x1);
+          if (col > rel) x0 = -INFINITY;
+          if (col + 1 > rel) x1 = -INFINITY;
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          float t0, t1;
+          f2_unpack(f2_mul(f2_pack(p0, p1),
+                           f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                                  nd2)),
+                    t0, t1);
+          pd[e] = pack_bf16x2(t0, t1);
+        }
+        tmem_st_x16(tS + lane_off + 16 * ch, pd);  // dS over S
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarP));
+    }
+    if (ok && n_kt > 0) {
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarAcc), 0));
+      if (ok) tc_fence_after();
+    }
+    if (ok) {
+      const bool valid = i < p.Nq;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t qd[32] = {};
+        if (n_kt > 0) tmem_ld_x32(tdQ + lane_off + 32 * cc, qd);
+        // A row with no admissible key stores +0 exactly (its dS is +-0).
+        if (valid)
+          store_row_bf16(p.dq + (bh * p.Nq + i) * D + 32 * cc, qd, p.scale,
+                         n_kt == 0 || nl2 == -INFINITY);
+      }
+    }
+  }
+  epilogue_sync(c, warp);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
+  BwdParams p;
+  p.o = static_cast<const __nv_bfloat16*>(a.o);
+  p.dout = static_cast<const __nv_bfloat16*>(a.dout);
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.dk = static_cast<__nv_bfloat16*>(a.dk);
+  p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.status = a.status;
+  p.B = a.B;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.qoff = a.query_offset;
+  p.causal = a.causal;
+  p.scale = a.scale;
+  p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
+  p.timeout_ns = a.timeout_ns;
+
+  const int64_t rows = a.B * a.H * a.Nq;
+  bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p.o, p.dout,
+                                                                               a.delta, rows);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes));
+  if (err != cudaSuccess) return err;
+  const int64_t n_kt = (a.Nk + T - 1) / T, n_qt = (a.Nq + T - 1) / T;
+  bwd_dkdv_kernel<<<static_cast<unsigned>(a.B * a.Hkv * n_kt), kThreads, kSmemBytes, stream>>>(
+      tq, tk, tv, tdo, p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  bwd_dq_kernel<<<static_cast<unsigned>(a.B * a.H * n_qt), kThreads, kSmemBytes, stream>>>(
+      tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -49,6 +49,22 @@ inline int64_t splitkv_rows_per_cta(int64_t rows_per_kv_head) {
   return rows_per_kv_head == 1 ? 1 : (rows_per_kv_head <= 4 ? 4 : 8);
 }
 
+// Arguments of one backward pass (d = 128), already validated.
+struct BwdArgs {
+  const void *o, *dout;  // bf16 [B][H][Nq][d]
+  const float* lse;      // f32 [B][H][Nq] from the forward pass
+  float* delta;          // workspace f32 [B][H][Nq]: rowsum(dO * O)
+  void *dq, *dk, *dv;    // bf16 outputs, [B][H][Nq][d] and [B][Hkv][Nk][d]
+  int* status;
+  int64_t B, H, Hkv, Nq, Nk, query_offset;
+  int causal;
+  float scale;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
+
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream);
 

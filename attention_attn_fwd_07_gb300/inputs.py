@@ -92,6 +92,17 @@ def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = N
     return q, k, v
 
 
+def make_dout(w: Workload, device: str | torch.device = "cpu", Nq: int | None = None):
+    """Loss gradient on O for the backward pass: dO [B, H, Nq, d] bfloat16,
+    standard normal entries from its own seed (the workload's seed + 104729)."""
+    Nq = w.Nq if Nq is None else Nq
+    g = torch.Generator(device=device).manual_seed(w.seed + 104729)
+    out = torch.empty((w.B, w.H, Nq, w.d), dtype=torch.bfloat16, device=device)
+    for b in range(w.B):
+        out[b] = torch.randn((w.H, Nq, w.d), generator=g, device=device,
+                             dtype=torch.float32).to(torch.bfloat16)
+    return out
+
 
 def make_qkv_fp8(w: Workload, device: str | torch.device = "cpu", Nq: int | None = None,
                  Nk: int | None = None):

@@ -57,6 +57,9 @@ def parse_args():
                          "(smaller cases for ncu captures) and print its GB/s")
     ap.add_argument("--decode-profile-gqa", action="store_true",
                     help="with --decode-profile-batch: the grouped-K/V-head decode workload")
+    ap.add_argument("--bwd-profile-batch", type=int, default=0,
+                    help="run only the backward of the long causal prefill with this batch "
+                         "size (smaller cases for ncu captures) and print its TFLOPS")
     return ap.parse_args()
 
 
@@ -267,6 +270,35 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU leg
+def run_backward(w, q, k, v, o, lse, dev, stream, args, pk, pk_src, world, max_over_ranks):
+    """Time attn_bwd (three launches) on the workload's forward outputs."""
+    from attention_attn_fwd_07_gb300 import binding
+    dout = W.make_dout(w, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty((binding.attn_bwd_workspace_bytes(w.B, w.H, w.Nq),), dtype=torch.uint8,
+                     device=dev)
+    binding.attn_fwd(q, k, v, w.causal, w.scale, o=o, lse=lse, stream=stream)
+
+    def sb():
+        binding.attn_bwd(q, k, v, o, lse, dout, w.causal, w.scale, workspace=ws, dq=dq, dk=dk,
+                         dv=dv, stream=stream)
+
+    for _ in range(args.warmup):
+        sb()
+    m = max_over_ranks(event_time(sb, args.steps, stream))
+    flops = 2.5 * prefill_flops(w)
+    tf = flops / (m / 1e3) / 1e12
+    del dout, dq, dk, dv, ws
+    return {"workload": w.name + ", backward (dQ, dK, dV)", "metric": "TFLOPS",
+            "value": world * tf, "ms_per_step": m, "launches_per_step": 3,
+            "flops_convention": "2.5 x the forward's (five matmuls: S, dP, dV, dK, dQ); the "
+                                "kernels execute seven (S and dP again in the dQ kernel)",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
+                         "peak_source": f"{pk_src} bf16 dense (burst)", "traffic": None},
+            "l2": "inputs larger than L2; no flush"}
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -302,6 +334,20 @@ def main():
         return float(t.item())
 
     launches = 0
+
+    if args.bwd_profile_batch > 0:
+        # Backward only, smaller batch: the case the ncu captures run on.
+        base = W.LONG_PREFILL_CAUSAL
+        wb = W.Workload(base.name.replace("B2", f"B{args.bwd_profile_batch}"),
+                        args.bwd_profile_batch, base.H, base.Nq, base.Nk, base.d, True,
+                        base.seed)
+        qb, kb, vb = W.make_qkv(wb, device=dev)
+        ob = torch.empty_like(qb)
+        lb = torch.empty((wb.B, wb.H, wb.Nq), dtype=torch.float32, device=dev)
+        r = run_backward(wb, qb, kb, vb, ob, lb, dev, stream, args, pk, pk_src, 1,
+                         lambda x: x)
+        print(json.dumps(r), flush=True)
+        return 0
 
     if args.decode_profile_batch > 0:
         # Decode only, smaller batch: the case the ncu captures run on.
@@ -435,6 +481,11 @@ def main():
                        "frac_of_bf16_peak": tff / pk["bf16_tflops"],
                        "l2": "inputs (269 MB) larger than L2"})
         del q8, k8, v8, of, lf
+
+        # ---- backward of the long causal prefill (dQ, dK, dV from O, LSE, dO)
+        others.append(run_backward(w, q, k, v, o, lse, dev, stream, args, pk, pk_src, world,
+                                   max_over_ranks))
+        launches += 3 * args.steps
 
         # ---- decode (split-KV + combine), memory bound; MHA and grouped K/V heads
         def run_decode(wd):

@@ -160,6 +160,46 @@ int attn_combine(const float* o_part, const float* lse_part, void* o, float* lse
                  int64_t B, int64_t H, int64_t Nq, int64_t d, int num_splits,
                  cudaStream_t stream);
 
+/* Arguments of the backward pass (attn_bwd). */
+typedef struct attn_bwd_params {
+  const void* q;          /* bf16 [B][H][Nq][d], the forward's inputs         */
+  const void* k;          /* bf16 [B][Hkv][Nk][d]                             */
+  const void* v;          /* bf16 [B][Hkv][Nk][d]                             */
+  const void* o;          /* bf16 [B][H][Nq][d], the forward's output         */
+  const void* dout;       /* bf16 [B][H][Nq][d], loss gradient on O           */
+  const float* lse;       /* f32  [B][H][Nq], the forward's log-sum-exp       */
+  void* dq;               /* bf16 [B][H][Nq][d], written                      */
+  void* dk;               /* bf16 [B][Hkv][Nk][d], written                    */
+  void* dv;               /* bf16 [B][Hkv][Nk][d], written                    */
+  int64_t B, H, Hkv, Nq, Nk, d;  /* Hkv = 0 means H; d must be 128           */
+  int causal;
+  float scale;
+  int64_t query_offset;
+  int* dev_status;        /* as in attn_params                                */
+  uint32_t flags;         /* ATTN_FLAG_ALLOW_NEG_OFFSET only                  */
+  uint32_t wait_timeout_us;
+} attn_bwd_params;
+
+/* Bytes of workspace attn_bwd needs: f32 [B][H][Nq] (the row corrections
+ * rowsum(dO * O)).  Returns 0 for invalid sizes. */
+size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq);
+
+/*
+ * Gradients of the forward above for the loss gradient dout on O
+ * ("GPU Engineering: Correctness, Throughput, and Attention", sections 22.5
+ * and 22.7): dV = P^T dO, dP = dO V^T, dS = P * (dP - rowsum(dO * O)),
+ * dQ = scale * dS K, dK = scale * dS^T Q, with P recomputed tile by tile
+ * from `lse` (never stored).  Rows with no admissible key get zero dQ; keys no
+ * row can see get zero dK and dV.  Grouped K/V heads sum their group's
+ * contributions.  Three launches on `stream` (row corrections, a dK/dV kernel
+ * per 128-key tile, a dQ kernel per 128-query tile); no atomics, so the
+ * result is deterministic.  d = 128 only (ATTN_ERR_UNSUPPORTED otherwise).
+ * `workspace` (device, 16-byte aligned, caller-owned) must hold
+ * attn_bwd_workspace_bytes(B, H, Nq) bytes.
+ */
+int attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
+             cudaStream_t stream);
+
 /* Size of the library-owned scratch array used by attn_fwd_splitkv_noalloc
  * (one per GPU that loads the library, kept until the process exits). */
 #define ATTN_NOALLOC_SCRATCH_BYTES (32u << 20)

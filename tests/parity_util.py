@@ -78,3 +78,42 @@ def check_guards(buf: torch.Tensor, pad: int, what: str = "") -> None:
     sentinel = 0x7FA5 if buf.dtype == torch.bfloat16 else 0x7FC0DEAD
     assert (raw[:pad] == sentinel).all(), f"{what}: write before the output"
     assert (raw[-pad:] == sentinel).all(), f"{what}: write after the output"
+
+
+# Backward tolerance.  Every gradient element is an fp32 sum of products whose
+# one staged factor (P for dV, dS for dK and dQ) was rounded to bf16 (relative
+# error <= 2^-9), and the result is rounded to bf16 once more (<= 2^-9); the
+# row correction comes from the bf16 O.  Together that stays below 4 * 2^-9
+# ~ 8e-3 of the largest terms, so with u = 1e-2:
+#   * normwise  ||G - R||_F <= u * ||R||_F      (each of dQ, dK, dV)
+#   * per element |G - R| <= half_ulp_bf16(R) + u * max|R|
+#   * exact zeros: rows with no admissible key have dQ == 0 and keys that no
+#     row sees have dK == dV == 0 (compared as values: -0.0 counts as zero).
+# Plus an absolute floor for the one cancellation in the path, dP - Delta in
+# fp32: its rounding is 2^-24 x (|dP| + |Delta|), and for unit-normal inputs
+# at d = 128 those stay below ~160, so ~1e-5 (this is what is left where the
+# exact dS is 0, e.g. a single visible key, where P = 1 and dP = Delta).
+GRAD_TOL = 1e-2
+GRAD_ATOL = 1e-5
+
+
+def compare_grad(g_gpu: torch.Tensor, ref: np.ndarray, what: str = "",
+                 zero_rows: np.ndarray | None = None) -> dict:
+    g = g_gpu.detach().cpu().to(torch.float64).numpy()
+    assert g.shape == ref.shape, f"{what}: shape {g.shape} vs {ref.shape}"
+    assert np.isfinite(g).all(), f"{what}: non-finite gradient"
+    err = np.abs(g - ref)
+    rmax = float(np.abs(ref).max()) if ref.size else 0.0
+    fro_ref = float(np.linalg.norm(ref.ravel()))
+    fro_err = float(np.linalg.norm(err.ravel()))
+    excess = err - half_ulp_bf16(ref) - GRAD_TOL * rmax - GRAD_ATOL
+    stats = {"max_abs": float(err.max()) if err.size else 0.0, "ref_max": rmax,
+             "rel_fro": fro_err / fro_ref if fro_ref > 0 else fro_err,
+             "max_excess": float(excess.max()) if excess.size else 0.0}
+    if zero_rows is not None and zero_rows.any():
+        assert (g[zero_rows] == 0).all(), f"{what}: rows that must be zero are not"
+        assert (ref[zero_rows] == 0).all(), f"{what}: oracle rows that must be zero are not"
+    assert stats["max_excess"] <= 0.0, f"{what}: element error {stats}"
+    assert fro_err <= GRAD_TOL * fro_ref + GRAD_ATOL * np.sqrt(max(ref.size, 1)), \
+        f"{what}: normwise error {stats}"
+    return stats

@@ -164,3 +164,38 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         binding.load_library(str(tmp_path / "nope.so"))
+
+
+def _bwd_params(**kw):
+    base = dict(q=A16, k=A16, v=A16, o=A16, dout=A16, lse=A16, dq=A16, dk=A16, dv=A16, B=1, H=2,
+                Hkv=0, Nq=8, Nk=8, d=128, causal=1, scale=0.125, query_offset=0,
+                dev_status=None, flags=0, wait_timeout_us=0)
+    base.update(kw)
+    return binding.attn_bwd_params(**base)
+
+
+@pytest.mark.parametrize("kw,ws,code", [
+    (dict(q=0), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(dout=0), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(dk=0), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(Nq=0), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(scale=float("nan")), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(Hkv=3), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(Hkv=4), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(query_offset=-1), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(d=64), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(Nq=1 << 31), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(dq=MIS), 1 << 20, binding.ATTN_ERR_ALIGN),
+    (dict(lse=A16 + 2), 1 << 20, binding.ATTN_ERR_ALIGN),
+    (dict(), 16, binding.ATTN_ERR_WORKSPACE),
+])
+def test_bwd_rejects(lib, kw, ws, code):
+    p = _bwd_params(**kw)
+    assert lib.attn_bwd(ctypes.byref(p), A16, ws, None) == code
+
+
+def test_bwd_workspace_bytes(lib):
+    assert lib.attn_bwd_workspace_bytes(2, 3, 100) >= 2 * 3 * 100 * 4
+    assert lib.attn_bwd_workspace_bytes(2, 3, 100) % 256 == 0
+    assert lib.attn_bwd_workspace_bytes(0, 3, 100) == 0
+    assert lib.attn_bwd(None, A16, 1 << 20, None) == binding.ATTN_ERR_INVALID
