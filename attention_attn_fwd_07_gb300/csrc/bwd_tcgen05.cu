@@ -23,9 +23,13 @@
 //                      streaming (K, V) tiles: S = Q K^T, dP = dO V^T,
 //                      dS = P * (dP - Delta), dQ += dS K.
 //                      TMEM: S [0,128) dP [128,256) dQ [256,384).
-// Warp roles in both: warps 0-3 elementwise (one thread per TMEM lane = row),
-// warp 4 single-thread MMA issuer, warp 5 TMA producer.  Every mbarrier wait
-// is bounded; a timeout sets the status word and the CTA leaves cleanly.
+// Warp roles in both: warps 0-7 elementwise (warp w owns TMEM lane quarter
+// w % 4 = 32 rows and column half w / 4 = 64 columns), warp 8 single-thread
+// MMA issuer, warp 9 TMA producer.  The elementwise work of a tile runs in
+// two phases so that it overlaps the tensor core: phase A turns S into P
+// while dP is computed, phase B turns dP into dS while the MMA that needs
+// only P (dV, or the next tile's S) runs.  Every mbarrier wait is bounded; a
+// timeout sets the status word and the CTA leaves cleanly.
 #include <cuda_bf16.h>
 
 #include "attn.h"
@@ -37,9 +41,11 @@ namespace {
 
 constexpr int D = 128;
 constexpr int T = 128;                    // rows per query tile and per key tile
-constexpr int kThreads = 192;
-constexpr int kWarpMma = 4;
-constexpr int kWarpLoad = 5;
+constexpr int kEwWarps = 8;
+constexpr int kEwThreads = kEwWarps * 32;
+constexpr int kThreads = kEwThreads + 64;
+constexpr int kWarpMma = 8;
+constexpr int kWarpLoad = 9;
 constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
 constexpr uint32_t kTileBytes = T * D * 2;    // one [128][128] bf16 tile (2 atoms)
 constexpr int kStages = 2;                    // streamed tile pairs in flight
@@ -53,14 +59,22 @@ constexpr uint32_t kOffRes = 0;
 constexpr uint32_t kOffRing = 2 * kTileBytes;
 constexpr uint32_t kOffStat = kOffRing + kStages * 2 * kTileBytes;  // 2 x [2][128] floats
 constexpr uint32_t kOffBar = kOffStat + 2 * 2 * T * 4;
-// barriers: res_full, full[2], empty[2], s_full, p_ready, acc_full, drain,
-// stats_ready[2] (dK/dV kernel: per-tile row statistics written by the 128
+// barriers: res_full, full[2], empty[2], s_full, dp_full, p (dK/dV kernel:
+// P stored; dQ kernel: S read, its columns free), ds (dS stored), acc_full,
+// drain, stats_ready[2] (dK/dV kernel: per-tile row statistics written by the
 // elementwise threads, one arrival each)
-constexpr int kBarRes = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 6, kBarAcc = 7,
-              kBarDrain = 8, kBarStat = 9, kNumBars = 11;
+constexpr int kBarRes = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarDP = 6, kBarP = 7,
+              kBarDS = 8, kBarAcc = 9, kBarDrain = 10, kBarStat = 11, kNumBars = 13;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448 && kSmemBytes > 232448 / 2, "one CTA per SM");
+
+// Column of the packed bf16 operand (P or dS, two values per 32-bit column)
+// that holds K step kk (16 values): column half h = kk / 4 packs its 64
+// values into the first 32 columns of its own 64-column range.
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3));
+}
 
 struct BwdParams {
   const __nv_bfloat16 *o, *dout;
@@ -134,11 +148,13 @@ __device__ __forceinline__ Ctx prologue(uint8_t* smem_raw, int warp) {
       mbar_init(c.bar(kBarEmpty + s), 1);
     }
     mbar_init(c.bar(kBarS), 1);
-    mbar_init(c.bar(kBarP), 4);
+    mbar_init(c.bar(kBarDP), 1);
+    mbar_init(c.bar(kBarP), kEwWarps);
+    mbar_init(c.bar(kBarDS), kEwWarps);
     mbar_init(c.bar(kBarAcc), 1);
     mbar_init(c.bar(kBarDrain), 1);
-    mbar_init(c.bar(kBarStat + 0), 128);
-    mbar_init(c.bar(kBarStat + 1), 128);
+    mbar_init(c.bar(kBarStat + 0), kEwThreads);
+    mbar_init(c.bar(kBarStat + 1), kEwThreads);
     *c.abort_flag = 0;
     fence_barrier_init();
   }
@@ -167,17 +183,21 @@ __device__ __forceinline__ void epilogue_sync(const Ctx& c, int warp) {
 // Row statistics of one 128-query tile as the exponent offsets the
 // elementwise warps use: nl2[i] = -LSE_i*log2(e) (-inf where the row has no
 // admissible key or lies past Nq, so P = 0 there) and nd[i] = -Delta_i.
+// Elementwise thread t < 128 writes nl2[t], thread 128 + t writes nd[t].
 __device__ __forceinline__ void load_stats(const BwdParams& p, int64_t row_base, int64_t q0,
                                            int t, float* nl2, float* nd) {
-  const int64_t i = q0 + t;
-  float l2 = -INFINITY, dl = 0.0f;
-  if (i < p.Nq) {
-    const float lse = p.lse[row_base + i];
-    l2 = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
-    dl = -p.delta[row_base + i];
+  const int r = t & (T - 1);
+  const int64_t i = q0 + r;
+  if (t < T) {
+    float l2 = -INFINITY;
+    if (i < p.Nq) {
+      const float lse = p.lse[row_base + i];
+      l2 = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
+    }
+    nl2[r] = l2;
+  } else {
+    nd[r] = i < p.Nq ? -p.delta[row_base + i] : 0.0f;
   }
-  nl2[t] = l2;
-  nd[t] = dl;
 }
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
@@ -243,13 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   const uint32_t sK = c.sbase + kOffRes, sV = sK + kTileBytes;
-  auto sQ = [&](int s) { return c.sbase + kOffRing + s * 2 * kTileBytes; };
-  auto sdO = [&](int s) { return sQ(s) + kTileBytes; };
+  auto sQ = [&](int64_t n) { return c.sbase + kOffRing + static_cast<uint32_t>(n % kStages) * 2 * kTileBytes; };
+  auto sdO = [&](int64_t n) { return sQ(n) + kTileBytes; };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + 256, tdK = c.tmem + 384;
 
   if (warp == kWarpLoad) {
     if (lane == 0) {
-      int last = -1;
+      int64_t last = -1;
       bool ok = true;
       mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
       load_tile(sK, &tk, c.bar(kBarRes), static_cast<int>(k0), bkv);
@@ -261,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t bh, q0;
         item_rows(n, bh, q0);
         mbar_arrive_expect_tx(c.bar(kBarFull + s), 2 * kTileBytes);
-        load_tile(sQ(s), &tq, c.bar(kBarFull + s), static_cast<int>(q0), bh);
-        load_tile(sdO(s), &tdo, c.bar(kBarFull + s), static_cast<int>(q0), bh);
-        last = static_cast<int>(n);
+        load_tile(sQ(n), &tq, c.bar(kBarFull + s), static_cast<int>(q0), bh);
+        load_tile(sdO(n), &tdo, c.bar(kBarFull + s), static_cast<int>(q0), bh);
+        last = n;
       }
       volatile int no_abort = 0;
       const Waiter own{&no_abort, p.status, p.timeout_ns};
@@ -272,26 +292,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= 0) own(c.bar(kBarFull + static_cast<int>(n % kStages)), (n / kStages) & 1);
     }
   } else if (warp == kWarpMma) {
+    // Issue order per tile n: ... dV(n), S(n+1), dK(n), dP(n+1), ...; the
+    // tensor pipe executes in issue order, so S(n+1) overwrites P(n) only
+    // after dV(n) read it, and dP(n+1) overwrites dS(n) only after dK(n).
     if (lane == 0 && n_items > 0) {
-      bool ok = wait(c.bar(kBarRes), 0);
-      for (int64_t n = 0; n < n_items && ok; ++n) {
-        const int s = static_cast<int>(n % kStages);
-        ok = wait(c.bar(kBarFull + s), (n / kStages) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        for (int kk = 0; kk < D / 16; ++kk)  // S^T = K Q^T
-          mma_ss(tS, desc_kmajor(sK, kk), desc_kmajor(sQ(s), kk), kIdescSS, kk > 0);
-        for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
-          mma_ss(tdP, desc_kmajor(sV, kk), desc_kmajor(sdO(s), kk), kIdescSS, kk > 0);
+      auto issue_s = [&](int64_t n) {  // S^T = K Q^T
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tS, desc_kmajor(sK, kk), desc_kmajor(sQ(n), kk), kIdescSS, kk > 0);
         mma_commit(c.bar(kBarS));
+      };
+      auto issue_dp = [&](int64_t n) {  // dP^T = V dO^T
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tdP, desc_kmajor(sV, kk), desc_kmajor(sdO(n), kk), kIdescSS, kk > 0);
+        mma_commit(c.bar(kBarDP));
+      };
+      bool ok = wait(c.bar(kBarRes), 0) && wait(c.bar(kBarFull), 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int64_t n = 0; n < n_items && ok; ++n) {
         ok = wait(c.bar(kBarP), n & 1);
         if (!ok) break;
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dV += P^T dO
-          mma_ts(tdV, tS + kk * 8, desc_mnmajor(sdO(s), kk), kIdescTS, (n > 0 || kk > 0));
+          mma_ts(tdV, tS + packed_col(kk), desc_mnmajor(sdO(n), kk), kIdescTS, (n > 0 || kk > 0));
+        const bool more = n + 1 < n_items;
+        if (more) {
+          ok = wait(c.bar(kBarFull + static_cast<int>((n + 1) % kStages)), ((n + 1) / kStages) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        ok = wait(c.bar(kBarDS), n & 1);
+        if (!ok) break;
+        tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dK += dS^T Q
-          mma_ts(tdK, tdP + kk * 8, desc_mnmajor(sQ(s), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit(c.bar(kBarEmpty + s));
+          mma_ts(tdK, tdP + packed_col(kk), desc_mnmajor(sQ(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit(c.bar(kBarEmpty + static_cast<int>(n % kStages)));
+        if (more) issue_dp(n + 1);
       }
       if (ok) mma_commit(c.bar(kBarAcc));
       mma_commit(c.bar(kBarDrain));
@@ -301,84 +341,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- elementwise
-    const int jl = (warp << 5) + lane;  // key row in the tile = TMEM lane
+    const int quarter = warp & 3, half = warp >> 2;
+    const int jl = (quarter << 5) + lane;  // key row in the tile = TMEM lane
     const int64_t j = k0 + jl;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    float* nl2_buf = reinterpret_cast<float*>(c.smem + kOffStat);  // [2][2][128]
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(64 * half);
+    float* stat_buf = reinterpret_cast<float*>(c.smem + kOffStat);  // [2][2][128]
     const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
+    const bool row_live = j < p.Nk;
     bool ok = true;
     for (int64_t n = 0; n < n_items; ++n) {
       int64_t bh, q0;
       item_rows(n, bh, q0);
-      float* nl2 = nl2_buf + (n & 1) * 2 * T;
-      float* nd = nl2 + T;
-      // Each thread writes one column's statistics; the four warps meet on
-      // a (bounded) mbarrier per tile, double-buffered by tile parity.
-      load_stats(p, bh * p.Nq, q0, jl, nl2, nd);
-      mbar_arrive(c.bar(kBarStat + (n & 1)));  // release: this thread's column is written
+      const float* nl2 = stat_buf + (n & 1) * 2 * T;
+      const float* nd = nl2 + T;
+      // Each thread writes one statistic; the eight warps meet on a
+      // (bounded) mbarrier per tile, double-buffered by tile parity.
+      load_stats(p, bh * p.Nq, q0, threadIdx.x, stat_buf + (n & 1) * 2 * T,
+                 stat_buf + (n & 1) * 2 * T + T);
+      mbar_arrive(c.bar(kBarStat + (n & 1)));  // release: this thread's statistic is written
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarStat + (n & 1)), (n >> 1) & 1));
       if (!ok) break;
+      // Key j is visible to query i = q0 + col iff j < Nk and (not causal or
+      // j <= i + off), i.e. col >= thr.
+      const int64_t thr64 = p.causal ? j - q0 - p.qoff : -1;
+      const int thr = row_live ? static_cast<int>(thr64 < -1 ? -1 : (thr64 > T ? T : thr64)) : T;
+
+      // Phase A: P^T = exp2(S^T c - LSE log2e), stored as bf16 over S^T.
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
       if (!ok) break;
       tc_fence_after();
-      // Key j is visible to query i = q0 + col iff j < Nk and (not causal or
-      // j <= i + off), i.e. col >= thr.
-      const bool row_live = j < p.Nk;
-      const int64_t thr64 = p.causal ? j - q0 - p.qoff : -1;
-      const int thr = static_cast<int>(thr64 < -1 ? -1 : (thr64 > T ? T : thr64));
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tS + lane_off + 32 * ch, sr);
-        tmem_ld_x32(tdP + lane_off + 32 * ch, dr);
-        uint32_t pp[16], pd[16];
+      float pf[64];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sr[32], pp[16];
+        tmem_ld_x32(tS + lane_off + col0 + 32 * ch, sr);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = 32 * ch + 2 * e;
+          const int col = static_cast<int>(col0) + 32 * ch + 2 * e;
           const float2 l2 = *reinterpret_cast<const float2*>(nl2 + col);
-          const float2 dl = *reinterpret_cast<const float2*>(nd + col);
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                            c2, f2_pack(l2.x, l2.y)),
                     x0, x1);
-          if (!row_live || col < thr) x0 = -INFINITY;
-          if (!row_live || col + 1 < thr) x1 = -INFINITY;
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-          float t0, t1;
-          f2_unpack(f2_mul(f2_pack(p0, p1),
-                           f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
-                                  f2_pack(dl.x, dl.y))),
-                    t0, t1);
-          pp[e] = pack_bf16x2(p0, p1);
-          pd[e] = pack_bf16x2(t0, t1);
+          if (col < thr) x0 = -INFINITY;
+          if (col + 1 < thr) x1 = -INFINITY;
+          pf[32 * ch + 2 * e] = ex2_approx(x0);
+          pf[32 * ch + 2 * e + 1] = ex2_approx(x1);
+          pp[e] = pack_bf16x2(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]);
         }
-        // P^T over S^T and dS^T over dP^T, 16 packed columns per chunk (only
-        // columns this thread has already read are overwritten).
-        tmem_st_x16(tS + lane_off + 16 * ch, pp);
-        tmem_st_x16(tdP + lane_off + 16 * ch, pd);
+        // Only columns this thread has already read are overwritten.
+        tmem_st_x16(tS + lane_off + col0 + 16 * ch, pp);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarP));
+
+      // Phase B: dS^T = P^T (dP^T - Delta), stored as bf16 over dP^T.
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarDP), n & 1));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dr[32], pd[16];
+        tmem_ld_x32(tdP + lane_off + col0 + 32 * ch, dr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int col = static_cast<int>(col0) + 32 * ch + 2 * e;
+          const float2 dl = *reinterpret_cast<const float2*>(nd + col);
+          float t0, t1;
+          f2_unpack(f2_mul(f2_pack(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]),
+                           f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
+                                  f2_pack(dl.x, dl.y))),
+                    t0, t1);
+          pd[e] = pack_bf16x2(t0, t1);
+        }
+        tmem_st_x16(tdP + lane_off + col0 + 16 * ch, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarDS));
     }
     if (ok && n_items > 0) {
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarAcc), 0));
       if (ok) tc_fence_after();
     }
     if (ok) {
-      const bool valid = j < p.Nk;
       const int64_t kv_row = bkv * p.Nk + j;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t col = col0 + 32 * cc;
         uint32_t kd[32] = {}, vd[32] = {};
         if (n_items > 0) {
-          tmem_ld_x32(tdK + lane_off + 32 * cc, kd);
-          tmem_ld_x32(tdV + lane_off + 32 * cc, vd);
+          tmem_ld_x32(tdK + lane_off + col, kd);
+          tmem_ld_x32(tdV + lane_off + col, vd);
         }
-        if (valid) {
-          store_row_bf16(p.dk + kv_row * D + 32 * cc, kd, p.scale, n_items == 0);
-          store_row_bf16(p.dv + kv_row * D + 32 * cc, vd, 1.0f, n_items == 0);
+        if (row_live) {
+          store_row_bf16(p.dk + kv_row * D + col, kd, p.scale, n_items == 0);
+          store_row_bf16(p.dv + kv_row * D + col, vd, 1.0f, n_items == 0);
         }
       }
     }
@@ -408,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const uint32_t sQ = c.sbase + kOffRes, sdO = sQ + kTileBytes;
-  auto sK = [&](int s) { return c.sbase + kOffRing + s * 2 * kTileBytes; };
-  auto sV = [&](int s) { return sK(s) + kTileBytes; };
+  auto sK = [&](int n) { return c.sbase + kOffRing + static_cast<uint32_t>(n % kStages) * 2 * kTileBytes; };
+  auto sV = [&](int n) { return sK(n) + kTileBytes; };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdQ = c.tmem + 256;
 
   if (warp == kWarpLoad) {
@@ -424,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= kStages) ok = wait(c.bar(kBarEmpty + s), ((n / kStages) - 1) & 1);
         if (!ok) break;
         mbar_arrive_expect_tx(c.bar(kBarFull + s), 2 * kTileBytes);
-        load_tile(sK(s), &tk, c.bar(kBarFull + s), n * T, bkv);
-        load_tile(sV(s), &tv, c.bar(kBarFull + s), n * T, bkv);
+        load_tile(sK(n), &tk, c.bar(kBarFull + s), n * T, bkv);
+        load_tile(sV(n), &tv, c.bar(kBarFull + s), n * T, bkv);
         last = n;
       }
       volatile int no_abort = 0;
@@ -435,24 +497,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= 0) own(c.bar(kBarFull + n % kStages), (n / kStages) & 1);
     }
   } else if (warp == kWarpMma) {
+    // Issue order per tile n: ... S(n+1) (once tile n's S is read), dQ(n),
+    // dP(n+1), ...; dP(n+1) overwrites dS(n) only after dQ(n) read it.
     if (lane == 0 && n_kt > 0) {
-      bool ok = wait(c.bar(kBarRes), 0);
-      for (int n = 0; n < n_kt && ok; ++n) {
-        const int s = n % kStages;
-        ok = wait(c.bar(kBarFull + s), (n / kStages) & 1);
-        if (!ok) break;
-        tc_fence_after();
-        for (int kk = 0; kk < D / 16; ++kk)  // S = Q K^T
-          mma_ss(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(s), kk), kIdescSS, kk > 0);
-        for (int kk = 0; kk < D / 16; ++kk)  // dP = dO V^T
-          mma_ss(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(s), kk), kIdescSS, kk > 0);
+      auto issue_s = [&](int n) {  // S = Q K^T
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(n), kk), kIdescSS, kk > 0);
         mma_commit(c.bar(kBarS));
-        ok = wait(c.bar(kBarP), n & 1);
+      };
+      auto issue_dp = [&](int n) {  // dP = dO V^T
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
+        mma_commit(c.bar(kBarDP));
+      };
+      bool ok = wait(c.bar(kBarRes), 0) && wait(c.bar(kBarFull), 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int n = 0; n < n_kt && ok; ++n) {
+        const bool more = n + 1 < n_kt;
+        if (more) {
+          ok = wait(c.bar(kBarFull + (n + 1) % kStages), ((n + 1) / kStages) & 1) &&
+               wait(c.bar(kBarP), n & 1);  // S(n) read: its columns are free
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        ok = wait(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dQ += dS K
-          mma_ts(tdQ, tS + kk * 8, desc_mnmajor(sK(s), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit(c.bar(kBarEmpty + s));
+          mma_ts(tdQ, tdP + packed_col(kk), desc_mnmajor(sK(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit(c.bar(kBarEmpty + n % kStages));
+        if (more) issue_dp(n + 1);
       }
       if (ok) mma_commit(c.bar(kBarAcc));
       mma_commit(c.bar(kBarDrain));
@@ -462,9 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- elementwise
-    const int il = (warp << 5) + lane;  // query row in the tile = TMEM lane
+    const int quarter = warp & 3, half = warp >> 2;
+    const int il = (quarter << 5) + lane;  // query row in the tile = TMEM lane
     const int64_t i = q0 + il;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col0 = static_cast<uint32_t>(64 * half);
     float nl2 = -INFINITY, nd = 0.0f;
     if (i < p.Nq) {
       const float lse = p.lse[bh * p.Nq + i];
@@ -478,41 +559,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t lim = p.causal ? min(p.Nk - 1, i + p.qoff) : p.Nk - 1;
     bool ok = true;
     for (int n = 0; n < n_kt; ++n) {
-      ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
-      if (!ok) break;
-      tc_fence_after();
       const int64_t k0 = static_cast<int64_t>(n) * T;
       const int64_t rel64 = lim - k0;
       const int rel = static_cast<int>(rel64 < -1 ? -1 : (rel64 > T ? T : rel64));
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_x32(tS + lane_off + 32 * ch, sr);
-        tmem_ld_x32(tdP + lane_off + 32 * ch, dr);
-        uint32_t pd[16];
+
+      // Phase A: P = exp2(S c - LSE log2e) into registers; S's columns free.
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
+      if (!ok) break;
+      tc_fence_after();
+      float pf[64];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sr[32];
+        tmem_ld_x32(tS + lane_off + col0 + 32 * ch, sr);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = 32 * ch + 2 * e;
+          const int col = static_cast<int>(col0) + 32 * ch + 2 * e;
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                            c2, l22),
                     x0, x1);
           if (col > rel) x0 = -INFINITY;
           if (col + 1 > rel) x1 = -INFINITY;
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          pf[32 * ch + 2 * e] = ex2_approx(x0);
+          pf[32 * ch + 2 * e + 1] = ex2_approx(x1);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(kBarP));
+
+      // Phase B: dS = P (dP - Delta), stored as bf16 over dP.
+      ok = __all_sync(0xffffffffu, wait(c.bar(kBarDP), n & 1));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dr[32], pd[16];
+        tmem_ld_x32(tdP + lane_off + col0 + 32 * ch, dr);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
           float t0, t1;
-          f2_unpack(f2_mul(f2_pack(p0, p1),
+          f2_unpack(f2_mul(f2_pack(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]),
                            f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
                                   nd2)),
                     t0, t1);
           pd[e] = pack_bf16x2(t0, t1);
         }
-        tmem_st_x16(tS + lane_off + 16 * ch, pd);  // dS over S
+        tmem_st_x16(tdP + lane_off + col0 + 16 * ch, pd);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(kBarP));
+      if (lane == 0) mbar_arrive(c.bar(kBarDS));
     }
     if (ok && n_kt > 0) {
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarAcc), 0));
@@ -521,12 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       const bool valid = i < p.Nq;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t col = col0 + 32 * cc;
         uint32_t qd[32] = {};
-        if (n_kt > 0) tmem_ld_x32(tdQ + lane_off + 32 * cc, qd);
+        if (n_kt > 0) tmem_ld_x32(tdQ + lane_off + col, qd);
         // A row with no admissible key stores +0 exactly (its dS is +-0).
         if (valid)
-          store_row_bf16(p.dq + (bh * p.Nq + i) * D + 32 * cc, qd, p.scale,
+          store_row_bf16(p.dq + (bh * p.Nq + i) * D + col, qd, p.scale,
                          n_kt == 0 || nl2 == -INFINITY);
       }
     }
