@@ -42,6 +42,8 @@ PROFILE_TXT = os.path.join(ROOT, "profiles", "fwd_tcgen05_long_prefill_causal.md
 KERNEL_SOURCES = ["fwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
 DECODE_PROFILE_TXT = os.path.join(ROOT, "profiles", "splitkv_decode.md")
 DECODE_SOURCES = ["splitkv.cu", "ptx.cuh", "internal.cuh"]
+BWD_PROFILE_TXT = os.path.join(ROOT, "profiles", "bwd_tcgen05_long_prefill_causal.md")
+BWD_SOURCES = ["bwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
 
 
 def parse_args():
@@ -295,7 +297,10 @@ def run_backward(w, q, k, v, o, lse, dev, stream, args, pk, pk_src, world, max_o
                                 "kernels execute seven (S and dP again in the dQ kernel)",
             "roofline": {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / pk["bf16_tflops"],
-                         "peak_source": f"{pk_src} bf16 dense (burst)", "traffic": None},
+                         "peak_source": f"{pk_src} bf16 dense (burst)",
+                         "traffic": recorded_traffic(BWD_PROFILE_TXT, BWD_SOURCES)
+                         if w is W.LONG_PREFILL_CAUSAL else None,
+                         "traffic_kernel": "bwd_dkdv_kernel (dominant launch of the three)"},
             "l2": "inputs larger than L2; no flush"}
 
 
