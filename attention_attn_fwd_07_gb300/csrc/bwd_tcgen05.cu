@@ -48,23 +48,28 @@ constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
 constexpr uint32_t kTileBytes = T * D * 2;    // one [128][128] bf16 tile (2 atoms)
-constexpr int kStages = 2;                    // streamed tile pairs in flight
+constexpr int kStages = 2;                    // streamed tiles of each kind in flight
 constexpr uint32_t kIdescSS = idesc_bf16_f32(T, T, 0);  // both operands K-major
 constexpr uint32_t kIdescTS = idesc_bf16_f32(T, D, 1);  // B (N = d) MN-major
 constexpr float kLog2e = 1.4426950408889634074f;
 
-// Shared memory: 2 resident tiles, kStages x 2 streamed tiles, then the
-// per-tile row statistics, barriers and bookkeeping.
+// Shared memory: 2 resident tiles, then two rings of kStages streamed tiles
+// each (ring A: Q tiles in the dK/dV kernel, K tiles in the dQ kernel; ring
+// B: dO, respectively V), then the per-tile row statistics, barriers and
+// bookkeeping.  The two rings have their own barriers, so a slot is refilled
+// as soon as the last MMA that reads it is done.
 constexpr uint32_t kOffRes = 0;
-constexpr uint32_t kOffRing = 2 * kTileBytes;
-constexpr uint32_t kOffStat = kOffRing + kStages * 2 * kTileBytes;  // 2 x [2][128] floats
+constexpr uint32_t kOffRingA = 2 * kTileBytes;
+constexpr uint32_t kOffRingB = kOffRingA + kStages * kTileBytes;
+constexpr uint32_t kOffStat = kOffRingB + kStages * kTileBytes;  // 2 x [2][128] floats
 constexpr uint32_t kOffBar = kOffStat + 2 * 2 * T * 4;
-// barriers: res_full, full[2], empty[2], s_full, dp_full, p (dK/dV kernel:
-// P stored; dQ kernel: S read, its columns free), ds (dS stored), acc_full,
-// drain, stats_ready[2] (dK/dV kernel: per-tile row statistics written by the
-// elementwise threads, one arrival each)
-constexpr int kBarRes = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarDP = 6, kBarP = 7,
-              kBarDS = 8, kBarAcc = 9, kBarDrain = 10, kBarStat = 11, kNumBars = 13;
+// barriers: res_full, full_a[2], full_b[2], empty_a[2], empty_b[2], s_full,
+// dp_full, p (dK/dV kernel: P stored; dQ kernel: S read, its columns free),
+// ds (dS stored), acc_full, drain, stats_ready[2] (dK/dV kernel: per-tile row
+// statistics written by the elementwise threads, one arrival each)
+constexpr int kBarRes = 0, kBarFullA = 1, kBarFullB = 3, kBarEmptyA = 5, kBarEmptyB = 7,
+              kBarS = 9, kBarDP = 10, kBarP = 11, kBarDS = 12, kBarAcc = 13, kBarDrain = 14,
+              kBarStat = 15, kNumBars = 17;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kSmemBytes <= 232448 && kSmemBytes > 232448 / 2, "one CTA per SM");
@@ -144,8 +149,10 @@ __device__ __forceinline__ Ctx prologue(uint8_t* smem_raw, int warp) {
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarRes), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(c.bar(kBarFull + s), 1);
-      mbar_init(c.bar(kBarEmpty + s), 1);
+      mbar_init(c.bar(kBarFullA + s), 1);
+      mbar_init(c.bar(kBarFullB + s), 1);
+      mbar_init(c.bar(kBarEmptyA + s), 1);
+      mbar_init(c.bar(kBarEmptyB + s), 1);
     }
     mbar_init(c.bar(kBarS), 1);
     mbar_init(c.bar(kBarDP), 1);
@@ -232,6 +239,36 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   if (lane == 0) delta[row] = acc;
 }
 
+// Loader of the two rings: tile n of ring B, then tile n of ring A, each
+// into slot n % kStages once the slot's previous tile is released.  Before
+// returning it waits for every copy it issued (the CTA must not exit with
+// copies in flight): per slot only the latest load's phase, which no later
+// load can have advanced.
+template <typename LoadA, typename LoadB>
+__device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, const BwdParams& p,
+                                           int64_t n_items, LoadA load_a, LoadB load_b) {
+  int64_t last_a = -1, last_b = -1;
+  for (int64_t n = 0; n < n_items; ++n) {
+    const int s = static_cast<int>(n % kStages);
+    const uint32_t par = static_cast<uint32_t>(((n / kStages) - 1) & 1);
+    if (n >= kStages && !wait(c.bar(kBarEmptyB + s), par)) break;
+    mbar_arrive_expect_tx(c.bar(kBarFullB + s), kTileBytes);
+    load_b(n, c.bar(kBarFullB + s));
+    last_b = n;
+    if (n >= kStages && !wait(c.bar(kBarEmptyA + s), par)) break;
+    mbar_arrive_expect_tx(c.bar(kBarFullA + s), kTileBytes);
+    load_a(n, c.bar(kBarFullA + s));
+    last_a = n;
+  }
+  volatile int no_abort = 0;
+  const Waiter own{&no_abort, p.status, p.timeout_ns};
+  own(c.bar(kBarRes), 0);
+  for (int64_t n = last_a - kStages + 1; n <= last_a; ++n)
+    if (n >= 0) own(c.bar(kBarFullA + static_cast<int>(n % kStages)), (n / kStages) & 1);
+  for (int64_t n = last_b - kStages + 1; n <= last_b; ++n)
+    if (n >= 0) own(c.bar(kBarFullB + static_cast<int>(n % kStages)), (n / kStages) & 1);
+}
+
 // ======================================================================= dK, dV
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -263,78 +300,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   const uint32_t sK = c.sbase + kOffRes, sV = sK + kTileBytes;
-  auto sQ = [&](int64_t n) { return c.sbase + kOffRing + static_cast<uint32_t>(n % kStages) * 2 * kTileBytes; };
-  auto sdO = [&](int64_t n) { return sQ(n) + kTileBytes; };
+  auto sQ = [&](int64_t n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStages) * kTileBytes; };
+  auto sdO = [&](int64_t n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStages) * kTileBytes; };
+  auto slot = [](int64_t n) { return static_cast<int>(n % kStages); };
+  auto par = [](int64_t n) { return static_cast<uint32_t>((n / kStages) & 1); };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + 256, tdK = c.tmem + 384;
 
   if (warp == kWarpLoad) {
     if (lane == 0) {
-      int64_t last = -1;
-      bool ok = true;
       mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
       load_tile(sK, &tk, c.bar(kBarRes), static_cast<int>(k0), bkv);
       load_tile(sV, &tv, c.bar(kBarRes), static_cast<int>(k0), bkv);
-      for (int64_t n = 0; n < n_items && ok; ++n) {
-        const int s = static_cast<int>(n % kStages);
-        if (n >= kStages) ok = wait(c.bar(kBarEmpty + s), ((n / kStages) - 1) & 1);
-        if (!ok) break;
-        int64_t bh, q0;
-        item_rows(n, bh, q0);
-        mbar_arrive_expect_tx(c.bar(kBarFull + s), 2 * kTileBytes);
-        load_tile(sQ(n), &tq, c.bar(kBarFull + s), static_cast<int>(q0), bh);
-        load_tile(sdO(n), &tdo, c.bar(kBarFull + s), static_cast<int>(q0), bh);
-        last = n;
-      }
-      volatile int no_abort = 0;
-      const Waiter own{&no_abort, p.status, p.timeout_ns};
-      own(c.bar(kBarRes), 0);
-      for (int64_t n = last - kStages + 1; n <= last; ++n)
-        if (n >= 0) own(c.bar(kBarFull + static_cast<int>(n % kStages)), (n / kStages) & 1);
+      run_loader(
+          c, wait, p, n_items,
+          [&](int64_t n, uint32_t bar) {
+            int64_t bh, q0;
+            item_rows(n, bh, q0);
+            load_tile(sQ(n), &tq, bar, static_cast<int>(q0), bh);
+          },
+          [&](int64_t n, uint32_t bar) {
+            int64_t bh, q0;
+            item_rows(n, bh, q0);
+            load_tile(sdO(n), &tdo, bar, static_cast<int>(q0), bh);
+          });
     }
   } else if (warp == kWarpMma) {
     // Issue order per tile n: ... dV(n), S(n+1), dK(n), dP(n+1), ...; the
     // tensor pipe executes in issue order, so S(n+1) overwrites P(n) only
     // after dV(n) read it, and dP(n+1) overwrites dS(n) only after dK(n).
-    if (lane == 0 && n_items > 0) {
+    // dO(n) is released after dV(n), Q(n) after dK(n).
+    // The whole warp runs this loop (waits made warp-uniform); the MMA and
+    // commit calls elect one lane to issue.
+    auto wait_w = [&](uint32_t b, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait(b, parity));
+    };
+    if (n_items > 0) {
       auto issue_s = [&](int64_t n) {  // S^T = K Q^T
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tS, desc_kmajor(sK, kk), desc_kmajor(sQ(n), kk), kIdescSS, kk > 0);
-        mma_commit(c.bar(kBarS));
+          mma_ss_w(tS, desc_kmajor(sK, kk), desc_kmajor(sQ(n), kk), kIdescSS, kk > 0);
+        mma_commit_w(c.bar(kBarS));
       };
       auto issue_dp = [&](int64_t n) {  // dP^T = V dO^T
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tdP, desc_kmajor(sV, kk), desc_kmajor(sdO(n), kk), kIdescSS, kk > 0);
-        mma_commit(c.bar(kBarDP));
+          mma_ss_w(tdP, desc_kmajor(sV, kk), desc_kmajor(sdO(n), kk), kIdescSS, kk > 0);
+        mma_commit_w(c.bar(kBarDP));
       };
-      bool ok = wait(c.bar(kBarRes), 0) && wait(c.bar(kBarFull), 0);
+      bool ok = wait_w(c.bar(kBarRes), 0) && wait_w(c.bar(kBarFullA), 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp(0);
+        ok = wait_w(c.bar(kBarFullB), 0);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+        }
       }
       for (int64_t n = 0; n < n_items && ok; ++n) {
-        ok = wait(c.bar(kBarP), n & 1);
+        ok = wait_w(c.bar(kBarP), n & 1);
         if (!ok) break;
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dV += P^T dO
-          mma_ts(tdV, tS + packed_col(kk), desc_mnmajor(sdO(n), kk), kIdescTS, (n > 0 || kk > 0));
+          mma_ts_w(tdV, tS + packed_col(kk), desc_mnmajor(sdO(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit_w(c.bar(kBarEmptyB + slot(n)));
         const bool more = n + 1 < n_items;
         if (more) {
-          ok = wait(c.bar(kBarFull + static_cast<int>((n + 1) % kStages)), ((n + 1) / kStages) & 1);
+          ok = wait_w(c.bar(kBarFullA + slot(n + 1)), par(n + 1));
           if (!ok) break;
           tc_fence_after();
           issue_s(n + 1);
         }
-        ok = wait(c.bar(kBarDS), n & 1);
+        ok = wait_w(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dK += dS^T Q
-          mma_ts(tdK, tdP + packed_col(kk), desc_mnmajor(sQ(n), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit(c.bar(kBarEmpty + static_cast<int>(n % kStages)));
-        if (more) issue_dp(n + 1);
+          mma_ts_w(tdK, tdP + packed_col(kk), desc_mnmajor(sQ(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit_w(c.bar(kBarEmptyA + slot(n)));
+        if (more) {
+          ok = wait_w(c.bar(kBarFullB + slot(n + 1)), par(n + 1));
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(n + 1);
+        }
       }
-      if (ok) mma_commit(c.bar(kBarAcc));
-      mma_commit(c.bar(kBarDrain));
+      if (ok) mma_commit_w(c.bar(kBarAcc));
+      mma_commit_w(c.bar(kBarDrain));
       volatile int no_abort = 0;
       const Waiter own{&no_abort, p.status, p.timeout_ns};
       own(c.bar(kBarDrain), 0);
@@ -345,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int jl = (quarter << 5) + lane;  // key row in the tile = TMEM lane
     const int64_t j = k0 + jl;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(64 * half);
+    const int col0 = 64 * half;
     float* stat_buf = reinterpret_cast<float*>(c.smem + kOffStat);  // [2][2][128]
     const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
     const bool row_live = j < p.Nk;
@@ -353,45 +402,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t n = 0; n < n_items; ++n) {
       int64_t bh, q0;
       item_rows(n, bh, q0);
-      const float* nl2 = stat_buf + (n & 1) * 2 * T;
-      const float* nd = nl2 + T;
+      float* nl2 = stat_buf + (n & 1) * 2 * T;
+      float* nd = nl2 + T;
       // Each thread writes one statistic; the eight warps meet on a
       // (bounded) mbarrier per tile, double-buffered by tile parity.
-      load_stats(p, bh * p.Nq, q0, threadIdx.x, stat_buf + (n & 1) * 2 * T,
-                 stat_buf + (n & 1) * 2 * T + T);
+      load_stats(p, bh * p.Nq, q0, threadIdx.x, nl2, nd);
       mbar_arrive(c.bar(kBarStat + (n & 1)));  // release: this thread's statistic is written
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarStat + (n & 1)), (n >> 1) & 1));
       if (!ok) break;
       // Key j is visible to query i = q0 + col iff j < Nk and (not causal or
-      // j <= i + off), i.e. col >= thr.
+      // j <= i + off), i.e. col >= thr.  Tiles where no lane masks any of
+      // its columns take the unmasked path.
       const int64_t thr64 = p.causal ? j - q0 - p.qoff : -1;
       const int thr = row_live ? static_cast<int>(thr64 < -1 ? -1 : (thr64 > T ? T : thr64)) : T;
+      const bool masked = __any_sync(0xffffffffu, thr > col0);
 
       // Phase A: P^T = exp2(S^T c - LSE log2e), stored as bf16 over S^T.
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
       if (!ok) break;
       tc_fence_after();
       float pf[64];
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sr[32], pp[16];
-        tmem_ld_x32(tS + lane_off + col0 + 32 * ch, sr);
+      {
+        uint32_t sr[64];
+        tmem_ld_x64(tS + lane_off + col0, sr);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = static_cast<int>(col0) + 32 * ch + 2 * e;
-          const float2 l2 = *reinterpret_cast<const float2*>(nl2 + col);
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
-                           c2, f2_pack(l2.x, l2.y)),
+          const int col = col0 + 4 * e;
+          const float4 l4 = *reinterpret_cast<const float4*>(nl2 + col);
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * e]), __uint_as_float(sr[4 * e + 1])),
+                           c2, f2_pack(l4.x, l4.y)),
                     x0, x1);
-          if (col < thr) x0 = -INFINITY;
-          if (col + 1 < thr) x1 = -INFINITY;
-          pf[32 * ch + 2 * e] = ex2_approx(x0);
-          pf[32 * ch + 2 * e + 1] = ex2_approx(x1);
-          pp[e] = pack_bf16x2(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * e + 2]), __uint_as_float(sr[4 * e + 3])),
+                           c2, f2_pack(l4.z, l4.w)),
+                    x2, x3);
+          if (masked) {
+            if (col < thr) x0 = -INFINITY;
+            if (col + 1 < thr) x1 = -INFINITY;
+            if (col + 2 < thr) x2 = -INFINITY;
+            if (col + 3 < thr) x3 = -INFINITY;
+          }
+          pf[4 * e] = ex2_approx(x0);
+          pf[4 * e + 1] = ex2_approx(x1);
+          pf[4 * e + 2] = ex2_approx(x2);
+          pf[4 * e + 3] = ex2_approx(x3);
         }
-        // Only columns this thread has already read are overwritten.
-        tmem_st_x16(tS + lane_off + col0 + 16 * ch, pp);
+      }
+      {
+        uint32_t pp[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pp[e] = pack_bf16x2(pf[2 * e], pf[2 * e + 1]);
+        tmem_st_x32(tS + lane_off + col0, pp);  // columns this thread has already read
       }
       tmem_st_wait();
       tc_fence_before();
@@ -402,22 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarDP), n & 1));
       if (!ok) break;
       tc_fence_after();
-#pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t dr[32], pd[16];
-        tmem_ld_x32(tdP + lane_off + col0 + 32 * ch, dr);
+      {
+        uint32_t dr[64], pd[32];
+        tmem_ld_x64(tdP + lane_off + col0, dr);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int col = static_cast<int>(col0) + 32 * ch + 2 * e;
-          const float2 dl = *reinterpret_cast<const float2*>(nd + col);
-          float t0, t1;
-          f2_unpack(f2_mul(f2_pack(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]),
-                           f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
-                                  f2_pack(dl.x, dl.y))),
+          const int col = col0 + 4 * e;
+          const float4 d4 = *reinterpret_cast<const float4*>(nd + col);
+          float t0, t1, t2, t3;
+          f2_unpack(f2_mul(f2_pack(pf[4 * e], pf[4 * e + 1]),
+                           f2_add(f2_pack(__uint_as_float(dr[4 * e]), __uint_as_float(dr[4 * e + 1])),
+                                  f2_pack(d4.x, d4.y))),
                     t0, t1);
-          pd[e] = pack_bf16x2(t0, t1);
+          f2_unpack(f2_mul(f2_pack(pf[4 * e + 2], pf[4 * e + 3]),
+                           f2_add(f2_pack(__uint_as_float(dr[4 * e + 2]), __uint_as_float(dr[4 * e + 3])),
+                                  f2_pack(d4.z, d4.w))),
+                    t2, t3);
+          pd[2 * e] = pack_bf16x2(t0, t1);
+          pd[2 * e + 1] = pack_bf16x2(t2, t3);
         }
-        tmem_st_x16(tdP + lane_off + col0 + 16 * ch, pd);
+        tmem_st_x32(tdP + lane_off + col0, pd);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -432,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t kv_row = bkv * p.Nk + j;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t col = col0 + 32 * cc;
+        const uint32_t col = static_cast<uint32_t>(col0 + 32 * cc);
         uint32_t kd[32] = {}, vd[32] = {};
         if (n_items > 0) {
           tmem_ld_x32(tdK + lane_off + col, kd);
@@ -470,71 +535,81 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const uint32_t sQ = c.sbase + kOffRes, sdO = sQ + kTileBytes;
-  auto sK = [&](int n) { return c.sbase + kOffRing + static_cast<uint32_t>(n % kStages) * 2 * kTileBytes; };
-  auto sV = [&](int n) { return sK(n) + kTileBytes; };
+  auto sK = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStages) * kTileBytes; };
+  auto sV = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStages) * kTileBytes; };
+  auto slot = [](int n) { return n % kStages; };
+  auto par = [](int n) { return static_cast<uint32_t>((n / kStages) & 1); };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdQ = c.tmem + 256;
 
   if (warp == kWarpLoad) {
     if (lane == 0 && n_kt > 0) {
-      int last = -1;
-      bool ok = true;
       mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
       load_tile(sQ, &tq, c.bar(kBarRes), static_cast<int>(q0), bh);
       load_tile(sdO, &tdo, c.bar(kBarRes), static_cast<int>(q0), bh);
-      for (int n = 0; n < n_kt && ok; ++n) {
-        const int s = n % kStages;
-        if (n >= kStages) ok = wait(c.bar(kBarEmpty + s), ((n / kStages) - 1) & 1);
-        if (!ok) break;
-        mbar_arrive_expect_tx(c.bar(kBarFull + s), 2 * kTileBytes);
-        load_tile(sK(n), &tk, c.bar(kBarFull + s), n * T, bkv);
-        load_tile(sV(n), &tv, c.bar(kBarFull + s), n * T, bkv);
-        last = n;
-      }
-      volatile int no_abort = 0;
-      const Waiter own{&no_abort, p.status, p.timeout_ns};
-      own(c.bar(kBarRes), 0);
-      for (int n = last - kStages + 1; n <= last; ++n)
-        if (n >= 0) own(c.bar(kBarFull + n % kStages), (n / kStages) & 1);
+      run_loader(
+          c, wait, p, n_kt,
+          [&](int64_t n, uint32_t bar) {
+            load_tile(sK(static_cast<int>(n)), &tk, bar, static_cast<int>(n) * T, bkv);
+          },
+          [&](int64_t n, uint32_t bar) {
+            load_tile(sV(static_cast<int>(n)), &tv, bar, static_cast<int>(n) * T, bkv);
+          });
     }
   } else if (warp == kWarpMma) {
     // Issue order per tile n: ... S(n+1) (once tile n's S is read), dQ(n),
-    // dP(n+1), ...; dP(n+1) overwrites dS(n) only after dQ(n) read it.
-    if (lane == 0 && n_kt > 0) {
+    // dP(n+1), ...; dP(n+1) overwrites dS(n) only after dQ(n) read it.  V(n)
+    // is released after dP(n), K(n) after dQ(n).
+    // The whole warp runs this loop (waits made warp-uniform); the MMA and
+    // commit calls elect one lane to issue.
+    auto wait_w = [&](uint32_t b, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait(b, parity));
+    };
+    if (n_kt > 0) {
       auto issue_s = [&](int n) {  // S = Q K^T
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(n), kk), kIdescSS, kk > 0);
-        mma_commit(c.bar(kBarS));
+          mma_ss_w(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(n), kk), kIdescSS, kk > 0);
+        mma_commit_w(c.bar(kBarS));
       };
       auto issue_dp = [&](int n) {  // dP = dO V^T
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
-        mma_commit(c.bar(kBarDP));
+          mma_ss_w(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
+        mma_commit_w(c.bar(kBarDP));
+        mma_commit_w(c.bar(kBarEmptyB + slot(n)));
       };
-      bool ok = wait(c.bar(kBarRes), 0) && wait(c.bar(kBarFull), 0);
+      bool ok = wait_w(c.bar(kBarRes), 0) && wait_w(c.bar(kBarFullA), 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp(0);
+        ok = wait_w(c.bar(kBarFullB), 0);
+        if (ok) {
+          tc_fence_after();
+          issue_dp(0);
+        }
       }
       for (int n = 0; n < n_kt && ok; ++n) {
         const bool more = n + 1 < n_kt;
         if (more) {
-          ok = wait(c.bar(kBarFull + (n + 1) % kStages), ((n + 1) / kStages) & 1) &&
-               wait(c.bar(kBarP), n & 1);  // S(n) read: its columns are free
+          ok = wait_w(c.bar(kBarFullA + slot(n + 1)), par(n + 1)) &&
+               wait_w(c.bar(kBarP), n & 1);  // S(n) read: its columns are free
           if (!ok) break;
           tc_fence_after();
           issue_s(n + 1);
         }
-        ok = wait(c.bar(kBarDS), n & 1);
+        ok = wait_w(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dQ += dS K
-          mma_ts(tdQ, tdP + packed_col(kk), desc_mnmajor(sK(n), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit(c.bar(kBarEmpty + n % kStages));
-        if (more) issue_dp(n + 1);
+          mma_ts_w(tdQ, tdP + packed_col(kk), desc_mnmajor(sK(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_commit_w(c.bar(kBarEmptyA + slot(n)));
+        if (more) {
+          ok = wait_w(c.bar(kBarFullB + slot(n + 1)), par(n + 1));
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(n + 1);
+        }
       }
-      if (ok) mma_commit(c.bar(kBarAcc));
-      mma_commit(c.bar(kBarDrain));
+      if (ok) mma_commit_w(c.bar(kBarAcc));
+      mma_commit_w(c.bar(kBarDrain));
       volatile int no_abort = 0;
       const Waiter own{&no_abort, p.status, p.timeout_ns};
       own(c.bar(kBarDrain), 0);
@@ -545,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int il = (quarter << 5) + lane;  // query row in the tile = TMEM lane
     const int64_t i = q0 + il;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col0 = static_cast<uint32_t>(64 * half);
+    const int col0 = 64 * half;
     float nl2 = -INFINITY, nd = 0.0f;
     if (i < p.Nq) {
       const float lse = p.lse[bh * p.Nq + i];
@@ -562,27 +637,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t k0 = static_cast<int64_t>(n) * T;
       const int64_t rel64 = lim - k0;
       const int rel = static_cast<int>(rel64 < -1 ? -1 : (rel64 > T ? T : rel64));
+      const bool masked = __any_sync(0xffffffffu, rel < col0 + 63);
 
       // Phase A: P = exp2(S c - LSE log2e) into registers; S's columns free.
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarS), n & 1));
       if (!ok) break;
       tc_fence_after();
       float pf[64];
+      {
+        uint32_t sr[64];
+        tmem_ld_x64(tS + lane_off + col0, sr);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sr[32];
-        tmem_ld_x32(tS + lane_off + col0 + 32 * ch, sr);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int col = static_cast<int>(col0) + 32 * ch + 2 * e;
+        for (int e = 0; e < 32; ++e) {
+          const int col = col0 + 2 * e;
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])),
                            c2, l22),
                     x0, x1);
-          if (col > rel) x0 = -INFINITY;
-          if (col + 1 > rel) x1 = -INFINITY;
-          pf[32 * ch + 2 * e] = ex2_approx(x0);
-          pf[32 * ch + 2 * e + 1] = ex2_approx(x1);
+          if (masked) {
+            if (col > rel) x0 = -INFINITY;
+            if (col + 1 > rel) x1 = -INFINITY;
+          }
+          pf[2 * e] = ex2_approx(x0);
+          pf[2 * e + 1] = ex2_approx(x1);
         }
       }
       tc_fence_before();
@@ -593,20 +670,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarDP), n & 1));
       if (!ok) break;
       tc_fence_after();
+      {
+        uint32_t dr[64], pd[32];
+        tmem_ld_x64(tdP + lane_off + col0, dr);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t dr[32], pd[16];
-        tmem_ld_x32(tdP + lane_off + col0 + 32 * ch, dr);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           float t0, t1;
-          f2_unpack(f2_mul(f2_pack(pf[32 * ch + 2 * e], pf[32 * ch + 2 * e + 1]),
+          f2_unpack(f2_mul(f2_pack(pf[2 * e], pf[2 * e + 1]),
                            f2_add(f2_pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])),
                                   nd2)),
                     t0, t1);
           pd[e] = pack_bf16x2(t0, t1);
         }
-        tmem_st_x16(tdP + lane_off + col0 + 16 * ch, pd);
+        tmem_st_x32(tdP + lane_off + col0, pd);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -621,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = i < p.Nq;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t col = col0 + 32 * cc;
+        const uint32_t col = static_cast<uint32_t>(col0 + 32 * cc);
         uint32_t qd[32] = {};
         if (n_kt > 0) tmem_ld_x32(tdQ + lane_off + col, qd);
         // A row with no admissible key stores +0 exactly (its dS is +-0).

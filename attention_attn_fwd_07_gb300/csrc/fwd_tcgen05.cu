@@ -245,7 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    // The whole warp runs this loop (waits made warp-uniform); the MMA and
+    // commit calls elect one lane to issue.
+    auto wait_w = [&](uint32_t b, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait(b, parity));
+    };
+    if (n_kv > 0) {
       auto qk = [&](int x, int stage) {
         const uint32_t d_tmem = tmem + C::kColS + 128 * x;
         // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
@@ -254,9 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes + off, 16, 1024);
           const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes + off, 16, 1024);
           if constexpr (FP8)
-            mma_ss_f8(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+            mma_ss_f8_w(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
           else
-            mma_ss(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
+            mma_ss_w(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto pv = [&](int x, int stage, bool acc) {
@@ -265,59 +270,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t b =
               sdesc_sw128(sKV + stage * C::kKVBytes + kk * 16 * 128, C::kAtomBytes, 1024);
-          mma_ts(d_tmem, p_tmem + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_w(d_tmem, p_tmem + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = wait(bar(C::kBarQ), 0);
-      if (ok) ok = wait(bar(C::kBarFull + 0), 0);
+      bool ok = wait_w(bar(C::kBarQ), 0);
+      if (ok) ok = wait_w(bar(C::kBarFull + 0), 0);
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < 2; ++x) {
           if (ntile[x] > 0) {
             qk(x, 0);
-            mma_commit(bar(C::kBarS + x));
+            mma_commit_w(bar(C::kBarS + x));
           }
         }
-        mma_commit(bar(C::kBarEmpty + 0));
+        mma_commit_w(bar(C::kBarEmpty + 0));
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int tV = 2 * j + 1, sV = tV % C::kStages;
         const int tK = 2 * j + 2, sK = tK % C::kStages;
         const bool next = j + 1 < n_kv;
         bool k_ready = false;
-        ok = wait(bar(C::kBarFull + sV), (tV / C::kStages) & 1);
+        ok = wait_w(bar(C::kBarFull + sV), (tV / C::kStages) & 1);
         if (!ok) break;
         for (int x = 0; x < 2 && ok; ++x) {
           if (j >= ntile[x]) continue;
-          ok = wait(bar(C::kBarP + x), j & 1);
+          ok = wait_w(bar(C::kBarP + x), j & 1);
           if (!ok) break;
           tc_fence_after();
           pv(x, sV, j > 0);
-          if (j == ntile[x] - 1) mma_commit(bar(C::kBarO + x));
+          if (j == ntile[x] - 1) mma_commit_w(bar(C::kBarO + x));
           if (j + 1 < ntile[x]) {
             if (!k_ready) {
-              ok = wait(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
+              ok = wait_w(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
               if (!ok) break;
               tc_fence_after();
               k_ready = true;
             }
             qk(x, sK);
-            mma_commit(bar(C::kBarS + x));
+            mma_commit_w(bar(C::kBarS + x));
           }
         }
         if (!ok) break;
-        mma_commit(bar(C::kBarEmpty + sV));
+        mma_commit_w(bar(C::kBarEmpty + sV));
         if (next) {
           if (!k_ready) {  // K(j+1) is used by no tile: still consume it in order
-            ok = wait(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
+            ok = wait_w(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
             if (!ok) break;
           }
-          mma_commit(bar(C::kBarEmpty + sK));
+          mma_commit_w(bar(C::kBarEmpty + sK));
         }
       }
       // All issued MMAs must complete before TMEM is released (bounded wait
       // that ignores the abort flag).
-      mma_commit(bar(C::kBarDrain));
+      mma_commit_w(bar(C::kBarDrain));
       volatile int no_abort = 0;
       const Waiter own{&no_abort, p.status, p.timeout_ns};
       own(bar(C::kBarDrain), 0);
