@@ -151,10 +151,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // CTA -> (bh, query block); causal grids start with the heaviest blocks.
-  const int64_t bh = blockIdx.x / p.n_qblk;
-  const int qi = static_cast<int>(blockIdx.x % p.n_qblk);
-  const int qb = p.causal ? (p.n_qblk - 1 - qi) : qi;
+  // CTA -> (bh, query block).  Causal grids run longest-first over the whole
+  // grid: CTAs are ordered by query block, last (heaviest) first, then by
+  // head, so the CTAs dispatched last are the shortest and the tail is short.
+  int64_t bh;
+  int qb;
+  if (p.causal) {
+    const int64_t n_bh = gridDim.x / p.n_qblk;
+    bh = blockIdx.x % n_bh;
+    qb = p.n_qblk - 1 - static_cast<int>(blockIdx.x / n_bh);
+  } else {
+    bh = blockIdx.x / p.n_qblk;
+    qb = static_cast<int>(blockIdx.x % p.n_qblk);
+  }
   const int64_t q0 = static_cast<int64_t>(qb) * (2 * BM);
   // K/V head of this query head (grouped K/V heads: H / group per batch).
   const int64_t bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
