@@ -35,6 +35,7 @@
 // Every mbarrier wait is bounded (globaltimer budget); on expiry the CTA
 // records a timeout in the status word, all roles leave their loops, pending
 // TMA loads and MMAs are awaited (bounded), TMEM is freed and the CTA exits.
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -90,6 +91,8 @@ struct KParams {
   int* status;
   int64_t Nq, Nk, qoff;
   int64_t H, group;  // query heads per batch; query heads per K/V head
+  int64_t n_bh;       // batch x query heads
+  int64_t heads_per_group;  // (b, h) slices per causal scheduling group
   int n_qblk;
   int causal;
   float sc_log2;  // scale * log2(e)
@@ -151,15 +154,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // CTA -> (bh, query block).  Causal grids run longest-first over the whole
-  // grid: CTAs are ordered by query block, last (heaviest) first, then by
-  // head, so the CTAs dispatched last are the shortest and the tail is short.
+  // CTA -> (bh, query block).  Causal grids run in groups of consecutive
+  // (b, h) slices whose K and V fit in L2 together; inside a group the CTAs
+  // go longest-first (last query block first, then by head), so the CTAs
+  // dispatched last are short and K/V are read from DRAM about once.
   int64_t bh;
   int qb;
   if (p.causal) {
-    const int64_t n_bh = gridDim.x / p.n_qblk;
-    bh = blockIdx.x % n_bh;
-    qb = p.n_qblk - 1 - static_cast<int>(blockIdx.x / n_bh);
+    const int64_t per_group = p.heads_per_group * p.n_qblk;
+    const int64_t h0 = (blockIdx.x / per_group) * p.heads_per_group;
+    const int64_t r = blockIdx.x % per_group;
+    const int64_t gh = min(p.heads_per_group, p.n_bh - h0);  // the last group may be smaller
+    bh = h0 + r % gh;
+    qb = p.n_qblk - 1 - static_cast<int>(r / gh);
   } else {
     bh = blockIdx.x / p.n_qblk;
     qb = static_cast<int>(blockIdx.x % p.n_qblk);
@@ -493,6 +500,12 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.H = a.H;
   p.group = a.group;
   p.n_qblk = static_cast<int>((a.Nq + 2 * BM - 1) / (2 * BM));
+  // Scheduling groups: whole K/V heads whose K and V take about 48 MB of L2.
+  const double kv_head_bytes =
+      static_cast<double>(a.Nk) * a.d * ((FP8 ? 1.0 : 2.0) + 2.0);
+  const int64_t kv_fit = std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / kv_head_bytes));
+  p.n_bh = a.BH;
+  p.heads_per_group = std::min<int64_t>(a.BH, kv_fit * a.group);
   p.causal = a.causal;
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.flags = a.flags;
