@@ -30,6 +30,7 @@
 // while dP is computed, phase B turns dP into dS while the MMA that needs
 // only P (dV, or the next tile's S) runs.  Every mbarrier wait is bounded; a
 // timeout sets the status word and the CTA leaves cleanly.
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "attn.h"
@@ -88,6 +89,8 @@ struct BwdParams {
   __nv_bfloat16 *dq, *dk, *dv;
   int* status;
   int64_t B, H, Hkv, Nq, Nk, qoff;
+  int64_t kv_per_group;  // dK/dV kernel: K/V heads per scheduling group
+  int64_t q_per_group;   // dQ kernel: query heads per scheduling group
   int causal;
   float scale;
   float sc_log2;  // scale * log2(e)
@@ -279,10 +282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Ctx c = prologue(smem_raw, warp);
   const Waiter wait{c.abort_flag, p.status, p.timeout_ns};
 
-  // CTA -> (b, K/V head, key tile)
+  // CTA -> (b, K/V head, key tile).  Groups of consecutive K/V heads whose
+  // streamed Q and dO fit in L2 together; inside a group key tiles go in
+  // ascending order (under a causal mask the first key tiles see the most
+  // query tiles), so the CTAs dispatched last are the shortest.
   const int64_t n_kt = (p.Nk + T - 1) / T;
-  const int64_t bkv = blockIdx.x / n_kt;
-  const int64_t k0 = (blockIdx.x % n_kt) * T;
+  int64_t bkv, k0;
+  {
+    const int64_t per_group = p.kv_per_group * n_kt;
+    const int64_t u0 = (blockIdx.x / per_group) * p.kv_per_group;
+    const int64_t r = blockIdx.x % per_group;
+    const int64_t gu = min(p.kv_per_group, p.B * p.Hkv - u0);
+    bkv = u0 + r % gu;
+    k0 = (r / gu) * T;
+  }
   const int64_t b = bkv / p.Hkv, hk = bkv % p.Hkv, G = p.H / p.Hkv;
   const int64_t n_qt = (p.Nq + T - 1) / T;
   // First query tile whose rows can see a key of this tile (causal).
@@ -523,9 +536,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Ctx c = prologue(smem_raw, warp);
   const Waiter wait{c.abort_flag, p.status, p.timeout_ns};
 
+  // CTA -> (b, h, query tile).  Groups of consecutive query heads whose K
+  // and V fit in L2 together; inside a group query tiles go last first
+  // (under a causal mask the last query tiles see the most key tiles).
   const int64_t n_qt = (p.Nq + T - 1) / T;
-  const int64_t bh = blockIdx.x / n_qt;
-  const int64_t q0 = (blockIdx.x % n_qt) * T;
+  int64_t bh, q0;
+  {
+    const int64_t per_group = p.q_per_group * n_qt;
+    const int64_t u0 = (blockIdx.x / per_group) * p.q_per_group;
+    const int64_t r = blockIdx.x % per_group;
+    const int64_t gu = min(p.q_per_group, p.B * p.H - u0);
+    bh = u0 + r % gu;
+    q0 = (n_qt - 1 - r / gu) * T;
+  }
   const int64_t b = bh / p.H, h = bh % p.H;
   const int64_t bkv = b * p.Hkv + h / (p.H / p.Hkv);
   int n_kt = static_cast<int>((p.Nk + T - 1) / T);
@@ -733,6 +756,16 @@ cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMa
   p.scale = a.scale;
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.timeout_ns = a.timeout_ns;
+  // Scheduling groups sized so that the tiles one group streams (Q and dO of
+  // its query heads for the dK/dV kernel, K and V for the dQ kernel) take
+  // about 48 MB of L2.
+  const int64_t G = a.H / a.Hkv;
+  const double q_head_bytes = 2.0 * static_cast<double>(a.Nq) * D * 2.0;
+  const double kv_head_bytes = 2.0 * static_cast<double>(a.Nk) * D * 2.0;
+  p.kv_per_group = std::min<int64_t>(
+      a.B * a.Hkv, std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / (q_head_bytes * G))));
+  p.q_per_group = std::min<int64_t>(
+      a.B * a.H, std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / kv_head_bytes)));
 
   const int64_t rows = a.B * a.H * a.Nq;
   bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p.o, p.dout,
