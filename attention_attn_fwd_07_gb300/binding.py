@@ -51,7 +51,8 @@ class attn_params(ctypes.Structure):
                 ("query_offset", ctypes.c_int64), ("dev_status", ctypes.c_void_p),
                 ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
                 ("Hkv", ctypes.c_int64), ("qk_dtype", ctypes.c_int),
-                ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float)]
+                ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
+                ("dv", ctypes.c_int64)]
 
 
 class attn_bwd_params(ctypes.Structure):
@@ -139,25 +140,25 @@ def _require(t, dtype, name):
 
 
 def _shape(q, k, v=None):
-    """(B, H, Nq, Nk, d) of q [B, H, Nq, d] and k, v [B, Hkv, Nk, d]."""
+    """(B, H, Nq, Nk, d) of q [B, H, Nq, d], k [B, Hkv, Nk, d], v [B, Hkv, Nk, dv]."""
     if q.dim() != 4 or k.dim() != 4:
         raise ValueError("expected [B, H, N, d] tensors")
     _require(q, torch.bfloat16, "q")
     _require(k, torch.bfloat16, "k")
     if v is not None:
         _require(v, torch.bfloat16, "v")
-        if tuple(v.shape) != tuple(k.shape):
-            raise ValueError("k and v must have the same shape")
+        if v.dim() != 4 or tuple(v.shape[:3]) != tuple(k.shape[:3]):
+            raise ValueError("v must be [B, Hkv, Nk, dv] with the batch, heads and keys of k")
     B, H, Nq, d = q.shape
     if k.shape[0] != B or k.shape[3] != d:
         raise ValueError("k must be [B, Hkv, Nk, d] with the batch and head dim of q")
     return B, H, Nq, k.shape[2], d
 
 
-def _outputs(q, o, lse):
+def _outputs(q, o, lse, dv=None):
     B, H, Nq, d = q.shape
     if o is None:
-        o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+        o = torch.empty((B, H, Nq, dv or d), dtype=torch.bfloat16, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     _require(o, torch.bfloat16, "o")
@@ -170,7 +171,7 @@ def attn_fwd(q, k, v, causal: bool, scale: float, o=None, lse=None, stream=None)
 
     K/V with fewer heads than Q (grouped K/V heads) go through attn_fwd_ex."""
     B, H, Nq, Nk, d = _shape(q, k, v)
-    if k.shape[1] != H:
+    if k.shape[1] != H or v.shape[3] != d:
         return attn_fwd_ex(q, k, v, causal, scale, o=o, lse=lse, stream=stream)
     o, lse = _outputs(q, o, lse)
     rc = load_library().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
@@ -184,12 +185,12 @@ def make_params(q, k, v, o, lse, causal, scale, query_offset=0, flags=0, dev_sta
     B, H, Nq, Nk, d = _shape(q, k, v)
     return attn_params(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                        int(bool(causal)), float(scale), int(query_offset), _ptr(dev_status),
-                       int(flags), int(wait_timeout_us), int(k.shape[1]))
+                       int(flags), int(wait_timeout_us), int(k.shape[1]), dv=int(v.shape[3]))
 
 
 def attn_fwd_ex(q, k, v, causal: bool, scale: float, query_offset: int = 0, flags: int = 0,
                 dev_status=None, wait_timeout_us: int = 0, o=None, lse=None, stream=None):
-    o, lse = _outputs(q, o, lse)
+    o, lse = _outputs(q, o, lse, dv=v.shape[3])
     p = make_params(q, k, v, o, lse, causal, scale, query_offset, flags, dev_status,
                     wait_timeout_us)
     _check(load_library().attn_fwd_ex(ctypes.byref(p), _stream(stream)), "attn_fwd_ex")
@@ -241,7 +242,7 @@ def attn_fwd_splitkv(q, k, v, causal: bool, scale: float, num_splits: int, works
 
     K/V with fewer heads than Q (grouped K/V heads) go through attn_fwd_splitkv_ex."""
     B, H, Nq, Nk, d = _shape(q, k, v)
-    if k.shape[1] != H:
+    if k.shape[1] != H or v.shape[3] != d:
         return attn_fwd_splitkv_ex(q, k, v, causal, scale, num_splits, workspace=workspace,
                                    o=o, lse=lse, stream=stream)
     o, lse = _outputs(q, o, lse)
@@ -313,6 +314,8 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, query_offset: in
              flags: int = 0, workspace=None, dq=None, dk=None, dv=None, stream=None):
     """Backward pass: returns (dq, dk, dv) bf16 for the loss gradient dout on o."""
     B, H, Nq, Nk, d = _shape(q, k, v)
+    if tuple(v.shape) != tuple(k.shape):
+        raise ValueError("the backward needs v with the shape of k (dv = d)")
     _require(o, torch.bfloat16, "o")
     _require(dout, torch.bfloat16, "dout")
     _require(lse, torch.float32, "lse")

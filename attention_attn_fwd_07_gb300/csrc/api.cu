@@ -72,6 +72,8 @@ int validate(const attn_params* p) {
   if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
   if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->dv < 0) return ATTN_ERR_INVALID;
+  if (p->dv != 0 && p->dv != 64 && p->dv != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
       p->Nk > kMaxDim)
     return ATTN_ERR_UNSUPPORTED;
@@ -105,8 +107,9 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
     if (!std::isfinite(p->q_descale) || !(p->q_descale > 0.0f) ||
         !std::isfinite(p->k_descale) || !(p->k_descale > 0.0f))
       return ATTN_ERR_INVALID;
-    if (p->d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (p->d != 128 || (p->dv != 0 && p->dv != p->d)) return ATTN_ERR_UNSUPPORTED;
   }
+  const int64_t dv = p->dv > 0 ? p->dv : p->d;
 
   int* status = p->dev_status;
   if (status == nullptr && default_status_word(&status) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -118,7 +121,7 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   const int qk_bytes = fp8 ? 1 : 2;
   if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d, qk_bytes) ||
       !encode_map(enc, &tk, p->k, p->Nk, BHkv, p->d, qk_bytes) ||
-      !encode_map(enc, &tv, p->v, p->Nk, BHkv, p->d))
+      !encode_map(enc, &tv, p->v, p->Nk, BHkv, dv))
     return ATTN_ERR_CUDA;
 
   FwdArgs a;
@@ -132,6 +135,7 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
   a.H = p->H;
   a.group = p->H / Hkv;
   a.d = static_cast<int>(p->d);
+  a.dv = static_cast<int>(dv);
   a.causal = p->causal ? 1 : 0;
   a.fp8_qk = fp8 ? 1 : 0;
   a.scale = fp8 ? static_cast<float>(static_cast<double>(p->scale) * p->q_descale * p->k_descale)
@@ -198,6 +202,7 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   if (rc != ATTN_OK) return rc;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
   if (p->qk_dtype != ATTN_QK_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (p->dv != 0 && p->dv != p->d) return ATTN_ERR_UNSUPPORTED;
   const size_t need = attn_splitkv_workspace_bytes(p->B, p->H, p->Nq, p->d, num_splits);
   if (need == 0) return ATTN_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;

@@ -52,16 +52,18 @@ constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows by > 2^8
 
-template <int D, bool FP8>
+// D: head dim of Q and K; DV: head dim of V and O (the value dim may differ).
+template <int D, int DV, bool FP8>
 struct Cfg {
   static constexpr int kQKElem = FP8 ? 1 : 2;               // bytes per Q/K element
   static constexpr int kQKAtoms = D * kQKElem / 128;        // 128-byte swizzle atoms per Q/K row
-  static constexpr int kVAtoms = D / 64;                    // ... per V row (bf16)
+  static constexpr int kVAtoms = DV / 64;                   // ... per V row (bf16)
   static constexpr uint32_t kAtomBytes = 128u * 128u;       // one [128 rows][128 B] box
   static constexpr uint32_t kQBytes = BM * D * kQKElem;     // one Q tile
   static constexpr uint32_t kKBytes = BN * D * kQKElem;     // one K tile
-  static constexpr uint32_t kKVBytes = BN * D * 2;          // one ring stage (a V tile)
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr uint32_t kVBytes = BN * DV * 2;          // one V tile
+  static constexpr uint32_t kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // one ring stage
+  static constexpr int kStages = (kKVBytes >= 32768u) ? 4 : 8;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQBytes;
   static constexpr uint32_t kOffBar = kOffKV + kStages * kKVBytes;
@@ -77,10 +79,10 @@ struct Cfg {
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + 1 KiB alignment slack
   static constexpr uint32_t kColS = 0;      // + 128 * tile
-  static constexpr uint32_t kColO = 256;    // + D * tile
+  static constexpr uint32_t kColO = 256;    // + DV * tile
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescQK = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0);
-  static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, DV, 1);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kSmemBytes > 232448 / 2, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
 };
@@ -136,12 +138,12 @@ __device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
   return static_cast<int>(min(n_all, last_key / BN + 1));
 }
 
-template <int D, bool FP8>
+template <int D, int DV, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tcgen05_kernel(const __grid_constant__ CUtensorMap tq,
                             const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv, const KParams p) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, DV, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const bool is_v = (t & 1) != 0;
-        mbar_arrive_expect_tx(bar(C::kBarFull + s), is_v ? C::kKVBytes : C::kKBytes);
+        mbar_arrive_expect_tx(bar(C::kBarFull + s), is_v ? C::kVBytes : C::kKBytes);
         const int key0 = (t >> 1) * BN;
         const int atoms = is_v ? C::kVAtoms : C::kQKAtoms;
         const int per_atom = is_v ? 64 : 128 / C::kQKElem;  // elements per 128-byte row
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto pv = [&](int x, int stage, bool acc) {
-        const uint32_t d_tmem = tmem + C::kColO + D * x;
+        const uint32_t d_tmem = tmem + C::kColO + DV * x;
         const uint32_t p_tmem = tmem + C::kColS + 128 * x;
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t b =
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t row = row0 + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS + 128 * x;
-    const uint32_t tO = tmem + lane_off + C::kColO + D * x;
+    const uint32_t tO = tmem + lane_off + C::kColO + DV * x;
     const int n = ntile[x];
     // Last admissible key of this row and of the tile's first row.
     const int64_t lim = p.causal ? min(p.Nk - 1, row + p.qoff) : p.Nk - 1;
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_x64(tS, pk);
       if (__any_sync(0xffffffffu, rescale) && j > 0) {
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < DV / 32; ++cc) {
           uint32_t o[32];
           tmem_ld_x32(tO + cc * 32, o);
 #pragma unroll
@@ -444,9 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool empty = (n == 0) || !(l > 0.0f);
       if (n > 0) {
         const float inv = empty ? 0.0f : 1.0f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * D);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * DV);
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < DV / 32; ++cc) {
           uint32_t o[32];
           tmem_ld_x32(tO + cc * 32, o);
           if (valid) {
@@ -463,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * D);
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * DV);
+        for (int i = 0; i < DV / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       }
       if (valid)
         p.lse[bh * p.Nq + row] =
@@ -481,12 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool FP8>
+template <int D, int DV, bool FP8>
 cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                    const CUtensorMap& tv, cudaStream_t stream) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, DV, FP8>;
   static_assert(C::kSmemBytes < (1u << 20), "");
-  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, FP8>,
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, DV, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
   if (err != cudaSuccess) return err;
@@ -502,7 +504,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.n_qblk = static_cast<int>((a.Nq + 2 * BM - 1) / (2 * BM));
   // Scheduling groups: whole K/V heads whose K and V take about 48 MB of L2.
   const double kv_head_bytes =
-      static_cast<double>(a.Nk) * a.d * ((FP8 ? 1.0 : 2.0) + 2.0);
+      static_cast<double>(a.Nk) * (D * (FP8 ? 1.0 : 2.0) + DV * 2.0);
   const int64_t kv_fit = std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / kv_head_bytes));
   p.n_bh = a.BH;
   p.heads_per_group = std::min<int64_t>(a.BH, kv_fit * a.group);
@@ -511,7 +513,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.flags = a.flags;
   p.timeout_ns = a.timeout_ns;
   const int64_t blocks = a.BH * p.n_qblk;
-  attn_fwd_tcgen05_kernel<D, FP8><<<dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
+  attn_fwd_tcgen05_kernel<D, DV, FP8><<<dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
                                C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -520,9 +522,13 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream) {
-  if (a.fp8_qk) return launch<128, true>(a, tq, tk, tv, stream);
-  if (a.d == 64) return launch<64, false>(a, tq, tk, tv, stream);
-  return launch<128, false>(a, tq, tk, tv, stream);
+  if (a.fp8_qk) return launch<128, 128, true>(a, tq, tk, tv, stream);
+  if (a.d == 64) {
+    if (a.dv == 128) return launch<64, 128, false>(a, tq, tk, tv, stream);
+    return launch<64, 64, false>(a, tq, tk, tv, stream);
+  }
+  if (a.dv == 64) return launch<128, 64, false>(a, tq, tk, tv, stream);
+  return launch<128, 128, false>(a, tq, tk, tv, stream);
 }
 
 }  // namespace attn

@@ -17,7 +17,8 @@ struct FwdArgs {
   int64_t BH, Nq, Nk, query_offset;
   int64_t H, group;    // query heads per batch; query heads per K/V head
   int fp8_qk;          // Q and K are e4m3 (scale already includes the descales)
-  int d;
+  int d;               // head dim of Q and K
+  int dv;              // head dim of V and O
   int causal;
   float scale;
   uint32_t flags;

@@ -31,10 +31,15 @@ class Workload:
     k_boost_frac: float = 0.0
     splits: tuple = field(default=())
     Hkv: int = 0  # K/V heads (grouped-query attention); 0 = H
+    dv: int = 0   # head dim of V (and O); 0 = d
 
     @property
     def kv_heads(self) -> int:
         return self.Hkv or self.H
+
+    @property
+    def v_dim(self) -> int:
+        return self.dv or self.d
 
     @property
     def scale(self) -> float:
@@ -75,14 +80,14 @@ def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = N
     Nk = w.Nk if Nk is None else Nk
     g = torch.Generator(device=device).manual_seed(w.seed)
 
-    def draw(n, heads):
-        out = torch.empty((w.B, heads, n, w.d), dtype=torch.bfloat16, device=device)
+    def draw(n, heads, dim=w.d):
+        out = torch.empty((w.B, heads, n, dim), dtype=torch.bfloat16, device=device)
         for b in range(w.B):  # per batch keeps the float32 temporary small
-            out[b] = torch.randn((heads, n, w.d), generator=g, device=device,
+            out[b] = torch.randn((heads, n, dim), generator=g, device=device,
                                  dtype=torch.float32).to(torch.bfloat16)
         return out
 
-    q, k, v = draw(Nq, w.H), draw(Nk, w.kv_heads), draw(Nk, w.kv_heads)
+    q, k, v = draw(Nq, w.H), draw(Nk, w.kv_heads), draw(Nk, w.kv_heads, w.v_dim)
     if w.k_boost_frac > 0.0:
         n_boost = math.ceil(w.k_boost_frac * Nk)
         for b in range(w.B):

@@ -80,8 +80,8 @@ enum {
 typedef struct attn_params {
   const void* q;          /* bf16 [B][H][Nq][d], device                    */
   const void* k;          /* bf16 [B][Hkv][Nk][d], device                  */
-  const void* v;          /* bf16 [B][Hkv][Nk][d], device                  */
-  void* o;                /* bf16 [B][H][Nq][d], device, written           */
+  const void* v;          /* bf16 [B][Hkv][Nk][dv], device                 */
+  void* o;                /* bf16 [B][H][Nq][dv], device, written          */
   float* lse;             /* f32  [B][H][Nq],    device, written           */
   int64_t B, H, Nq, Nk, d;
   int causal;             /* nonzero: key j visible to row i iff j <= i + query_offset */
@@ -100,6 +100,10 @@ typedef struct attn_params {
                              <q, k>; V stays bf16.                          */
   float q_descale;        /* per-tensor factors of the FP8 Q and K; finite, */
   float k_descale;        /* > 0 (ignored for bf16)                         */
+  int64_t dv;             /* head dim of V and O; 0 = d.  dv may differ from d
+                             in attn_fwd_ex (bf16, d and dv in {64, 128});
+                             every other entry point needs dv = d
+                             (ATTN_ERR_UNSUPPORTED otherwise).              */
 } attn_params;
 
 /* attn_params.qk_dtype */

@@ -78,7 +78,7 @@ def test_fwd_rejects(lib, kw, code):
 def _params(**kw):
     base = dict(q=A16, k=A16, v=A16, o=A16, lse=A16, B=1, H=1, Nq=8, Nk=8, d=64, causal=1,
                 scale=0.125, query_offset=0, dev_status=None, flags=0, wait_timeout_us=0, Hkv=0,
-                qk_dtype=0, q_descale=0.0, k_descale=0.0)
+                qk_dtype=0, q_descale=0.0, k_descale=0.0, dv=0)
     base.update(kw)
     return binding.attn_params(**base)
 
@@ -199,3 +199,20 @@ def test_bwd_workspace_bytes(lib):
     assert lib.attn_bwd_workspace_bytes(2, 3, 100) % 256 == 0
     assert lib.attn_bwd_workspace_bytes(0, 3, 100) == 0
     assert lib.attn_bwd(None, A16, 1 << 20, None) == binding.ATTN_ERR_INVALID
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dv=-1), binding.ATTN_ERR_INVALID),
+    (dict(dv=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(dv=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=128, dv=64, qk_dtype=1, q_descale=1.0, k_descale=1.0), binding.ATTN_ERR_UNSUPPORTED),
+])
+def test_value_dim_rejects(lib, kw, code):
+    p = _params(**kw)
+    assert lib.attn_fwd_ex(ctypes.byref(p), None) == code
+
+
+def test_splitkv_rejects_value_dim(lib):
+    p = _params(d=128, dv=64)
+    assert lib.attn_fwd_splitkv_ex(ctypes.byref(p), 4, A16, 1 << 30, None) == \
+        binding.ATTN_ERR_UNSUPPORTED

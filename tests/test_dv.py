@@ -1,0 +1,79 @@
+"""GPU parity for a value head dim different from the key head dim (dv != d,
+which the online-softmax derivation allows: V only enters through P V).
+Prefill path, d and dv in {64, 128}; the other entry points reject dv != d."""
+import pytest
+import torch
+
+import oracle
+from attention_attn_fwd_07_gb300 import binding, build
+from attention_attn_fwd_07_gb300 import inputs as W
+from tests.parity_util import compare, check_guards, guarded
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    binding.load_library()
+    yield
+    assert binding.attn_get_device_status() == 0
+
+
+def run(q, k, v, causal, scale, query_offset=0):
+    B, H, Nq, _ = q.shape
+    dv = v.shape[3]
+    o, obuf, opad = guarded((B, H, Nq, dv), torch.bfloat16, DEV)
+    lse, lbuf, lpad = guarded((B, H, Nq), torch.float32, DEV)
+    flags = binding.ATTN_FLAG_ALLOW_NEG_OFFSET if query_offset < 0 else 0
+    binding.attn_fwd_ex(q, k, v, causal, scale, query_offset=query_offset, flags=flags, o=o,
+                        lse=lse)
+    torch.cuda.synchronize()
+    check_guards(obuf, opad, "O")
+    check_guards(lbuf, lpad, "LSE")
+    return o, lse
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 129, 333, 1003])
+def test_dv_prefill(d, dv, causal, n):
+    w = W.Workload("dv", 2, 3, n, n, d, causal, 3000 + n + d, dv=dv)
+    q, k, v = W.make_qkv(w)
+    assert v.shape[3] == dv
+    o, lse = run(*(t.to(DEV) for t in (q, k, v)), causal, w.scale)
+    compare(o, lse, *oracle.attention(q, k, v, causal=causal, scale=w.scale),
+            f"d={d} dv={dv} N={n} causal={causal}")
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64)])
+def test_dv_gqa_and_offsets(d, dv):
+    w = W.Workload("dv gqa", 1, 8, 300, 700, d, True, 3100 + d, Hkv=2, dv=dv)
+    q, k, v = W.make_qkv(w)
+    for off in (-120, 0, 400):
+        o, lse = run(*(t.to(DEV) for t in (q, k, v)), True, w.scale, query_offset=off)
+        compare(o, lse, *oracle.attention(q, k, v, causal=True, scale=w.scale, query_offset=off),
+                f"d={d} dv={dv} GQA offset={off}")
+
+
+def test_dv_long_prefill_sampled():
+    """Long causal prefill shape with dv = 64 (d = 128): sampled rows."""
+    w = W.Workload("dv long", 1, 8, 8192, 8192, 128, True, 3200, dv=64)
+    q, k, v = W.make_qkv(w, device=DEV)
+    o, lse = run(q, k, v, True, w.scale)
+    rows = torch.randint(0, w.H * w.Nq, (96,), generator=torch.Generator().manual_seed(5)).tolist()
+    ref_o, ref_l = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, scale=w.scale,
+                                    rows=rows)
+    idx = torch.tensor(rows)
+    compare(o.reshape(-1, 64)[idx], lse.reshape(-1)[idx], ref_o, ref_l, "dv long sampled")
+
+
+def test_dv_other_entry_points_reject():
+    w = W.Workload("dv rej", 1, 2, 64, 64, 128, False, 3300, dv=64)
+    q, k, v = (t.to(DEV) for t in W.make_qkv(w))
+    with pytest.raises(binding.AttnError) as e:
+        binding.attn_fwd_splitkv(q, k, v, False, w.scale, 4)
+    assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
