@@ -49,31 +49,39 @@ constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
 constexpr uint32_t kTileBytes = T * D * 2;    // one [128][128] bf16 tile (2 atoms)
-constexpr int kStages = 2;                    // streamed tiles of each kind in flight
+constexpr int kStagesA = 3;  // ring A (Q tiles in the dK/dV kernel, K tiles in the dQ kernel)
+constexpr int kStagesB = 2;  // ring B (dO tiles, respectively V tiles)
 constexpr uint32_t kIdescSS = idesc_bf16_f32(T, T, 0);  // both operands K-major
 constexpr uint32_t kIdescTS = idesc_bf16_f32(T, D, 1);  // B (N = d) MN-major
 constexpr float kLog2e = 1.4426950408889634074f;
 
-// Shared memory: 2 resident tiles, then two rings of kStages streamed tiles
-// each (ring A: Q tiles in the dK/dV kernel, K tiles in the dQ kernel; ring
-// B: dO, respectively V), then the per-tile row statistics, barriers and
-// bookkeeping.  The two rings have their own barriers, so a slot is refilled
-// as soon as the last MMA that reads it is done.
+// Shared memory: 2 resident tiles, then ring A (kStagesA tiles: the operand
+// the next S needs, so it is prefetched deepest) and ring B (kStagesB tiles),
+// then the per-tile row statistics, barriers and bookkeeping.  The rings
+// have their own barriers, so a slot is refilled as soon as the last MMA
+// that reads it is done.  The dynamic shared memory is declared 1024-byte
+// aligned (the 128-byte swizzle needs it) and the kernels check that it is,
+// which leaves no room for an alignment slack: 231,592 of 232,448 bytes.
 constexpr uint32_t kOffRes = 0;
 constexpr uint32_t kOffRingA = 2 * kTileBytes;
-constexpr uint32_t kOffRingB = kOffRingA + kStages * kTileBytes;
-constexpr uint32_t kOffStat = kOffRingB + kStages * kTileBytes;  // 2 x [2][128] floats
+constexpr uint32_t kOffRingB = kOffRingA + kStagesA * kTileBytes;
+constexpr uint32_t kOffStat = kOffRingB + kStagesB * kTileBytes;  // 2 x [2][128] floats
 constexpr uint32_t kOffBar = kOffStat + 2 * 2 * T * 4;
-// barriers: res_full, full_a[2], full_b[2], empty_a[2], empty_b[2], s_full,
+// barriers: res_full, full_a[3], full_b[2], empty_a[3], empty_b[2], s_full,
 // dp_full, p (dK/dV kernel: P stored; dQ kernel: S read, its columns free),
 // ds (dS stored), acc_full, drain, stats_ready[2] (dK/dV kernel: per-tile row
 // statistics written by the elementwise threads, one arrival each)
-constexpr int kBarRes = 0, kBarFullA = 1, kBarFullB = 3, kBarEmptyA = 5, kBarEmptyB = 7,
-              kBarS = 9, kBarDP = 10, kBarP = 11, kBarDS = 12, kBarAcc = 13, kBarDrain = 14,
-              kBarStat = 15, kNumBars = 17;
+constexpr int kBarRes = 0, kBarFullA = 1, kBarFullB = kBarFullA + kStagesA,
+              kBarEmptyA = kBarFullB + kStagesB, kBarEmptyB = kBarEmptyA + kStagesA,
+              kBarS = kBarEmptyB + kStagesB, kBarDP = kBarS + 1, kBarP = kBarDP + 1,
+              kBarDS = kBarP + 1, kBarAcc = kBarDS + 1, kBarDrain = kBarAcc + 1,
+              kBarStat = kBarDrain + 1, kNumBars = kBarStat + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;
+constexpr uint32_t kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448 && kSmemBytes > 232448 / 2, "one CTA per SM");
+// Status word bit set (and the kernel skipped) if the dynamic shared memory
+// were ever not 1024-byte aligned.
+constexpr int kStatusMisaligned = 2;
 
 // Column of the packed bf16 operand (P or dS, two values per 32-bit column)
 // that holds K step kk (16 values): column half h = kk / 4 packs its 64
@@ -142,19 +150,20 @@ struct Ctx {
   __device__ __forceinline__ uint32_t bar(int i) const { return sbase + kOffBar + 8u * i; }
 };
 
+// Callers have checked that smem_raw is 1024-byte aligned.
 __device__ __forceinline__ Ctx prologue(uint8_t* smem_raw, int warp) {
   Ctx c;
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-  c.smem = smem_raw + pad;
-  c.sbase = raw + pad;
+  c.smem = smem_raw;
+  c.sbase = smem_u32(smem_raw);
   c.abort_flag = reinterpret_cast<volatile int*>(c.smem + kOffMisc + 4);
   if (threadIdx.x == 0) {
     mbar_init(c.bar(kBarRes), 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesA; ++s) {
       mbar_init(c.bar(kBarFullA + s), 1);
-      mbar_init(c.bar(kBarFullB + s), 1);
       mbar_init(c.bar(kBarEmptyA + s), 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(c.bar(kBarFullB + s), 1);
       mbar_init(c.bar(kBarEmptyB + s), 1);
     }
     mbar_init(c.bar(kBarS), 1);
@@ -242,34 +251,37 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   if (lane == 0) delta[row] = acc;
 }
 
-// Loader of the two rings: tile n of ring B, then tile n of ring A, each
-// into slot n % kStages once the slot's previous tile is released.  Before
-// returning it waits for every copy it issued (the CTA must not exit with
-// copies in flight): per slot only the latest load's phase, which no later
-// load can have advanced.
+// Loader of the two rings: tile n of ring A, then tile n of ring B, each
+// into its slot once the slot's previous tile is released.  Before returning
+// it waits for every copy it issued (the CTA must not exit with copies in
+// flight): per slot only the latest load's phase, which no later load can
+// have advanced.
 template <typename LoadA, typename LoadB>
 __device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, const BwdParams& p,
                                            int64_t n_items, LoadA load_a, LoadB load_b) {
   int64_t last_a = -1, last_b = -1;
   for (int64_t n = 0; n < n_items; ++n) {
-    const int s = static_cast<int>(n % kStages);
-    const uint32_t par = static_cast<uint32_t>(((n / kStages) - 1) & 1);
-    if (n >= kStages && !wait(c.bar(kBarEmptyB + s), par)) break;
-    mbar_arrive_expect_tx(c.bar(kBarFullB + s), kTileBytes);
-    load_b(n, c.bar(kBarFullB + s));
-    last_b = n;
-    if (n >= kStages && !wait(c.bar(kBarEmptyA + s), par)) break;
-    mbar_arrive_expect_tx(c.bar(kBarFullA + s), kTileBytes);
-    load_a(n, c.bar(kBarFullA + s));
+    const int sa = static_cast<int>(n % kStagesA), sb = static_cast<int>(n % kStagesB);
+    if (n >= kStagesA &&
+        !wait(c.bar(kBarEmptyA + sa), static_cast<uint32_t>(((n / kStagesA) - 1) & 1)))
+      break;
+    mbar_arrive_expect_tx(c.bar(kBarFullA + sa), kTileBytes);
+    load_a(n, c.bar(kBarFullA + sa));
     last_a = n;
+    if (n >= kStagesB &&
+        !wait(c.bar(kBarEmptyB + sb), static_cast<uint32_t>(((n / kStagesB) - 1) & 1)))
+      break;
+    mbar_arrive_expect_tx(c.bar(kBarFullB + sb), kTileBytes);
+    load_b(n, c.bar(kBarFullB + sb));
+    last_b = n;
   }
   volatile int no_abort = 0;
   const Waiter own{&no_abort, p.status, p.timeout_ns};
   own(c.bar(kBarRes), 0);
-  for (int64_t n = last_a - kStages + 1; n <= last_a; ++n)
-    if (n >= 0) own(c.bar(kBarFullA + static_cast<int>(n % kStages)), (n / kStages) & 1);
-  for (int64_t n = last_b - kStages + 1; n <= last_b; ++n)
-    if (n >= 0) own(c.bar(kBarFullB + static_cast<int>(n % kStages)), (n / kStages) & 1);
+  for (int64_t n = last_a - kStagesA + 1; n <= last_a; ++n)
+    if (n >= 0) own(c.bar(kBarFullA + static_cast<int>(n % kStagesA)), (n / kStagesA) & 1);
+  for (int64_t n = last_b - kStagesB + 1; n <= last_b; ++n)
+    if (n >= 0) own(c.bar(kBarFullB + static_cast<int>(n % kStagesB)), (n / kStagesB) & 1);
 }
 
 // ======================================================================= dK, dV
@@ -277,8 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (smem_u32(smem_raw) & 1023u) {  // same for every thread: the whole CTA leaves
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusMisaligned);
+    return;
+  }
   const Ctx c = prologue(smem_raw, warp);
   const Waiter wait{c.abort_flag, p.status, p.timeout_ns};
 
@@ -313,10 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   const uint32_t sK = c.sbase + kOffRes, sV = sK + kTileBytes;
-  auto sQ = [&](int64_t n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStages) * kTileBytes; };
-  auto sdO = [&](int64_t n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStages) * kTileBytes; };
-  auto slot = [](int64_t n) { return static_cast<int>(n % kStages); };
-  auto par = [](int64_t n) { return static_cast<uint32_t>((n / kStages) & 1); };
+  auto sQ = [&](int64_t n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kTileBytes; };
+  auto sdO = [&](int64_t n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kTileBytes; };
+  auto slot_a = [](int64_t n) { return static_cast<int>(n % kStagesA); };
+  auto slot_b = [](int64_t n) { return static_cast<int>(n % kStagesB); };
+  auto par_a = [](int64_t n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
+  auto par_b = [](int64_t n) { return static_cast<uint32_t>((n / kStagesB) & 1); };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + 256, tdK = c.tmem + 384;
 
   if (warp == kWarpLoad) {
@@ -374,10 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dV += P^T dO
           mma_ts_w(tdV, tS + packed_col(kk), desc_mnmajor(sdO(n), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit_w(c.bar(kBarEmptyB + slot(n)));
+        mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
         const bool more = n + 1 < n_items;
         if (more) {
-          ok = wait_w(c.bar(kBarFullA + slot(n + 1)), par(n + 1));
+          ok = wait_w(c.bar(kBarFullA + slot_a(n + 1)), par_a(n + 1));
           if (!ok) break;
           tc_fence_after();
           issue_s(n + 1);
@@ -387,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dK += dS^T Q
           mma_ts_w(tdK, tdP + packed_col(kk), desc_mnmajor(sQ(n), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit_w(c.bar(kBarEmptyA + slot(n)));
+        mma_commit_w(c.bar(kBarEmptyA + slot_a(n)));
         if (more) {
-          ok = wait_w(c.bar(kBarFullB + slot(n + 1)), par(n + 1));
+          ok = wait_w(c.bar(kBarFullB + slot_b(n + 1)), par_b(n + 1));
           if (!ok) break;
           tc_fence_after();
           issue_dp(n + 1);
@@ -531,8 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (smem_u32(smem_raw) & 1023u) {  // same for every thread: the whole CTA leaves
+    if (threadIdx.x == 0) atomicOr(p.status, kStatusMisaligned);
+    return;
+  }
   const Ctx c = prologue(smem_raw, warp);
   const Waiter wait{c.abort_flag, p.status, p.timeout_ns};
 
@@ -558,10 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   const uint32_t sQ = c.sbase + kOffRes, sdO = sQ + kTileBytes;
-  auto sK = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStages) * kTileBytes; };
-  auto sV = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStages) * kTileBytes; };
-  auto slot = [](int n) { return n % kStages; };
-  auto par = [](int n) { return static_cast<uint32_t>((n / kStages) & 1); };
+  auto sK = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kTileBytes; };
+  auto sV = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kTileBytes; };
+  auto slot_a = [](int n) { return n % kStagesA; };
+  auto slot_b = [](int n) { return n % kStagesB; };
+  auto par_a = [](int n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
+  auto par_b = [](int n) { return static_cast<uint32_t>((n / kStagesB) & 1); };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdQ = c.tmem + 256;
 
   if (warp == kWarpLoad) {
@@ -597,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk)
           mma_ss_w(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
         mma_commit_w(c.bar(kBarDP));
-        mma_commit_w(c.bar(kBarEmptyB + slot(n)));
+        mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
       };
       bool ok = wait_w(c.bar(kBarRes), 0) && wait_w(c.bar(kBarFullA), 0);
       if (ok) {
@@ -612,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; n < n_kt && ok; ++n) {
         const bool more = n + 1 < n_kt;
         if (more) {
-          ok = wait_w(c.bar(kBarFullA + slot(n + 1)), par(n + 1)) &&
+          ok = wait_w(c.bar(kBarFullA + slot_a(n + 1)), par_a(n + 1)) &&
                wait_w(c.bar(kBarP), n & 1);  // S(n) read: its columns are free
           if (!ok) break;
           tc_fence_after();
@@ -623,9 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kk = 0; kk < T / 16; ++kk)  // dQ += dS K
           mma_ts_w(tdQ, tdP + packed_col(kk), desc_mnmajor(sK(n), kk), kIdescTS, (n > 0 || kk > 0));
-        mma_commit_w(c.bar(kBarEmptyA + slot(n)));
+        mma_commit_w(c.bar(kBarEmptyA + slot_a(n)));
         if (more) {
-          ok = wait_w(c.bar(kBarFullB + slot(n + 1)), par(n + 1));
+          ok = wait_w(c.bar(kBarFullB + slot_b(n + 1)), par_b(n + 1));
           if (!ok) break;
           tc_fence_after();
           issue_dp(n + 1);

@@ -179,7 +179,9 @@ typedef struct attn_bwd_params {
   int causal;
   float scale;
   int64_t query_offset;
-  int* dev_status;        /* as in attn_params                                */
+  int* dev_status;        /* as in attn_params; bit 1 is set (and nothing is
+                             computed) if a kernel finds its shared memory
+                             not 1024-byte aligned                          */
   uint32_t flags;         /* ATTN_FLAG_ALLOW_NEG_OFFSET only                  */
   uint32_t wait_timeout_us;
 } attn_bwd_params;
