@@ -261,9 +261,7 @@ constexpr uint32_t bulk_smem_bytes() {
 }
 
 template <int D, int QB>
-// 184 registers per thread (9 warps, one CTA per SM) leave the kernel free of
-// spills; __launch_bounds__(kBulkThreads, 1) lets ptxas settle at 168 with spills.
-__global__ void __maxnreg__(184)
+__global__ void __launch_bounds__(kBulkThreads, 1)
     splitkv_partial_bulk_kernel(const PartialParams p) {
   constexpr int LPR = D / 8;            // lanes per key row (16 B each)
   constexpr int G = 32 / LPR;           // key rows per warp instruction
