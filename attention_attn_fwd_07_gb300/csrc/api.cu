@@ -279,7 +279,7 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   if (p->query_offset < -kMaxOffset || p->query_offset > kMaxOffset) return ATTN_ERR_INVALID;
   if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
   if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
-  if (p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
       p->Nk > kMaxDim)
     return ATTN_ERR_UNSUPPORTED;
@@ -323,7 +323,9 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   a.causal = p->causal ? 1 : 0;
   a.scale = p->scale;
   a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
-  return launch_bwd(a, tq, tk, tv, tdo, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  const cudaError_t err = p->d == 64 ? launch_bwd_d<64>(a, tq, tk, tv, tdo, stream)
+                                     : launch_bwd_d<128>(a, tq, tk, tv, tdo, stream);
+  return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 extern "C" int attn_get_device_status(int* dev_status_host, cudaStream_t stream) {

@@ -30,6 +30,13 @@
 // while dP is computed, phase B turns dP into dS while the MMA that needs
 // only P (dV, or the next tile's S) runs.  Every mbarrier wait is bounded; a
 // timeout sets the status word and the CTA leaves cleanly.
+// The head dim d is a compile-time constant of this translation unit:
+// compiled alone it is 128; bwd_tcgen05_d64.cu defines ATTN_BWD_HEAD_DIM as
+// 64 and includes this file.  Each build exports launch_bwd_d<d>.
+#ifndef ATTN_BWD_HEAD_DIM
+#define ATTN_BWD_HEAD_DIM 128
+#endif
+
 #include <algorithm>
 #include <cuda_bf16.h>
 
@@ -40,7 +47,8 @@
 namespace attn {
 namespace {
 
-constexpr int D = 128;
+constexpr int D = ATTN_BWD_HEAD_DIM;       // head dim of Q, K, V, dO
+static_assert(D == 64 || D == 128, "head dims 64 and 128");
 constexpr int T = 128;                    // rows per query tile and per key tile
 constexpr int kEwWarps = 8;
 constexpr int kEwThreads = kEwWarps * 32;
@@ -48,7 +56,7 @@ constexpr int kThreads = kEwThreads + 64;
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
-constexpr uint32_t kTileBytes = T * D * 2;    // one [128][128] bf16 tile (2 atoms)
+constexpr uint32_t kTileBytes = T * D * 2;    // one [128][d] bf16 tile (d / 64 atoms)
 constexpr int kStagesA = 3;  // ring A (Q tiles in the dK/dV kernel, K tiles in the dQ kernel)
 constexpr int kStagesB = 2;  // ring B (dO tiles, respectively V tiles)
 constexpr uint32_t kIdescSS = idesc_bf16_f32(T, T, 0);  // both operands K-major
@@ -79,6 +87,8 @@ constexpr int kBarRes = 0, kBarFullA = 1, kBarFullB = kBarFullA + kStagesA,
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448 && kSmemBytes > 232448 / 2, "one CTA per SM");
+// TMEM columns of the dK/dV kernel's accumulators (after S^T and dP^T).
+constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 // Status word bit set (and the kernel skipped) if the dynamic shared memory
 // were ever not 1024-byte aligned.
 constexpr int kStatusMisaligned = 2;
@@ -137,7 +147,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                           int row, int64_t z) {
-  for (int a = 0; a < 2; ++a)
+  for (int a = 0; a < D / 64; ++a)
     tma_load_3d(dst + a * kAtomBytes, map, bar, a * 64, row, static_cast<int>(z));
 }
 
@@ -241,11 +251,18 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
   if (row >= rows) return;
-  const uint2 a = *reinterpret_cast<const uint2*>(o + row * D + 4 * lane);
-  const uint2 b = *reinterpret_cast<const uint2*>(dout + row * D + 4 * lane);
   auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
   auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-  float acc = lo(a.x) * lo(b.x) + hi(a.x) * hi(b.x) + lo(a.y) * lo(b.y) + hi(a.y) * hi(b.y);
+  float acc;
+  if constexpr (D == 128) {  // four elements per lane
+    const uint2 a = *reinterpret_cast<const uint2*>(o + row * D + 4 * lane);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + row * D + 4 * lane);
+    acc = lo(a.x) * lo(b.x) + hi(a.x) * hi(b.x) + lo(a.y) * lo(b.y) + hi(a.y) * hi(b.y);
+  } else {  // two elements per lane
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + row * D + 2 * lane);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + row * D + 2 * lane);
+    acc = lo(a) * lo(b) + hi(a) * hi(b);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) delta[row] = acc;
@@ -335,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto slot_b = [](int64_t n) { return static_cast<int>(n % kStagesB); };
   auto par_a = [](int64_t n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
   auto par_b = [](int64_t n) { return static_cast<uint32_t>((n / kStagesB) & 1); };
-  const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + 256, tdK = c.tmem + 384;
+  const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + kColDV,
+                 tdK = c.tmem + kColDK;
 
   if (warp == kWarpLoad) {
     if (lane == 0) {
@@ -525,10 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
+      // Each thread stores half of its row's d columns.
       const int64_t kv_row = bkv * p.Nk + j;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t col = static_cast<uint32_t>(col0 + 32 * cc);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const uint32_t col = static_cast<uint32_t>((D / 2) * half + 32 * cc);
         uint32_t kd[32] = {}, vd[32] = {};
         if (n_items > 0) {
           tmem_ld_x32(tdK + lane_off + col, kd);
@@ -741,10 +760,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
+      // Each thread stores half of its row's d columns.
       const bool valid = i < p.Nq;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t col = static_cast<uint32_t>(col0 + 32 * cc);
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const uint32_t col = static_cast<uint32_t>((D / 2) * half + 32 * cc);
         uint32_t qd[32] = {};
         if (n_kt > 0) tmem_ld_x32(tdQ + lane_off + col, qd);
         // A row with no admissible key stores +0 exactly (its dS is +-0).
@@ -759,8 +779,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
+template <>
+cudaError_t launch_bwd_d<D>(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
   BwdParams p;
   p.o = static_cast<const __nv_bfloat16*>(a.o);
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);

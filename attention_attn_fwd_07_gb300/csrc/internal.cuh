@@ -63,8 +63,16 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
-cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
+// Backward launches for head dim D (bwd_tcgen05.cu: 128, bwd_tcgen05_d64.cu: 64).
+template <int D>
+cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
+template <>
+cudaError_t launch_bwd_d<64>(const BwdArgs&, const CUtensorMap&, const CUtensorMap&,
+                             const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+template <>
+cudaError_t launch_bwd_d<128>(const BwdArgs&, const CUtensorMap&, const CUtensorMap&,
+                              const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream);

@@ -464,6 +464,12 @@ def main():
                            "ms_per_step": m, "frac_of_peak": tf / pk["bf16_tflops"],
                            "l2": "inputs > L2" if wo.Nq >= 8192 else
                                  "L2 flushed (256 MB rewrite) before each timed launch"})
+            if wo.d == 64:  # the d = 64 backward on the same inputs
+                rb = run_backward(wo, qq, kk, vv, oo, ll, dev, stream, args, pk, pk_src, world,
+                                  max_over_ranks)
+                rb["l2"] = "inputs (84 MB) fit in L2; not flushed"
+                others.append(rb)
+                launches += 3 * args.steps
 
         # ---- long prefill causal with FP8 (e4m3) Q K^T, P V in bf16
         wf = W.LONG_PREFILL_CAUSAL

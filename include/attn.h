@@ -175,7 +175,7 @@ typedef struct attn_bwd_params {
   void* dq;               /* bf16 [B][H][Nq][d], written                      */
   void* dk;               /* bf16 [B][Hkv][Nk][d], written                    */
   void* dv;               /* bf16 [B][Hkv][Nk][d], written                    */
-  int64_t B, H, Hkv, Nq, Nk, d;  /* Hkv = 0 means H; d must be 128           */
+  int64_t B, H, Hkv, Nq, Nk, d;  /* Hkv = 0 means H; d is 64 or 128          */
   int causal;
   float scale;
   int64_t query_offset;
@@ -199,7 +199,7 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq);
  * row can see get zero dK and dV.  Grouped K/V heads sum their group's
  * contributions.  Three launches on `stream` (row corrections, a dK/dV kernel
  * per 128-key tile, a dQ kernel per 128-query tile); no atomics, so the
- * result is deterministic.  d = 128 only (ATTN_ERR_UNSUPPORTED otherwise).
+ * result is deterministic.  d in {64, 128} (ATTN_ERR_UNSUPPORTED otherwise).
  * `workspace` (device, 16-byte aligned, caller-owned) must hold
  * attn_bwd_workspace_bytes(B, H, Nq) bytes.
  */

@@ -183,7 +183,7 @@ def _bwd_params(**kw):
     (dict(Hkv=3), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(Hkv=4), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(query_offset=-1), 1 << 20, binding.ATTN_ERR_INVALID),
-    (dict(d=64), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
     (dict(Nq=1 << 31), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
     (dict(dq=MIS), 1 << 20, binding.ATTN_ERR_ALIGN),
     (dict(lse=A16 + 2), 1 << 20, binding.ATTN_ERR_ALIGN),

@@ -63,8 +63,8 @@ def masks(B, H, Hkv, Nq, Nk, causal, off):
     return zq, zk
 
 
-def check_case(B, H, Hkv, Nq, Nk, causal, off, seed, what):
-    w = W.Workload(what, B, H, Nq, Nk, 128, causal, seed, Hkv=Hkv)
+def check_case(B, H, Hkv, Nq, Nk, causal, off, seed, what, d=128):
+    w = W.Workload(what, B, H, Nq, Nk, d, causal, seed, Hkv=Hkv)
     q, k, v = W.make_qkv(w)
     dout = W.make_dout(w)
     dq, dk, dv = run_bwd(*(t.to(DEV) for t in (q, k, v, dout)), causal, w.scale, off)
@@ -75,10 +75,11 @@ def check_case(B, H, Hkv, Nq, Nk, causal, off, seed, what):
             compare_grad(dv, rv, f"{what} dV", zk))
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [1, 100, 128, 129, 333])
-def test_bwd_square(n, causal):
-    check_case(2, 3, 3, n, n, causal, 0, 2000 + n, f"bwd N{n} causal={causal}")
+def test_bwd_square(n, causal, d):
+    check_case(2, 3, 3, n, n, causal, 0, 2000 + n + d, f"bwd N{n} d={d} causal={causal}", d=d)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -88,26 +89,52 @@ def test_bwd_rectangular(nq, nk, causal):
     check_case(1, 2, 2, nq, nk, causal, off, 2100 + nq + nk, f"bwd {nq}x{nk} off={off}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("hkv", [1, 2, 4])
 @pytest.mark.parametrize("causal", [False, True])
-def test_bwd_gqa(hkv, causal):
-    check_case(2, 8, hkv, 200, 270, causal, 0, 2200 + hkv, f"bwd GQA Hkv={hkv} causal={causal}")
+def test_bwd_gqa(hkv, causal, d):
+    check_case(2, 8, hkv, 200, 270, causal, 0, 2200 + hkv + d,
+               f"bwd GQA Hkv={hkv} d={d} causal={causal}", d=d)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("off", [-150, -1, 5, 400])
-def test_bwd_offsets(off):
+def test_bwd_offsets(off, d):
     # off < 0: the first -off rows see no key (dQ = 0) and the last keys no
     # row (dK = dV = 0); off >= Nk - Nq: every key visible to every row.
-    check_case(1, 2, 2, 300, 300, True, off, 2300 + off, f"bwd causal off={off}")
+    check_case(1, 2, 2, 300, 300, True, off, 2300 + off + d, f"bwd causal off={off} d={d}", d=d)
 
 
-def test_bwd_rejects_d64():
-    w = W.Workload("d64", 1, 1, 64, 64, 64, False, 7)
+def test_bwd_rejects_d96():
+    w = W.Workload("d96", 1, 1, 64, 64, 96, False, 7)
     q, k, v = (t.to(DEV) for t in W.make_qkv(w))
-    o, lse = binding.attn_fwd(q, k, v, False, w.scale)
+    o = torch.zeros_like(q)
+    lse = torch.zeros((1, 1, 64), dtype=torch.float32, device=DEV)
     with pytest.raises(binding.AttnError) as e:
         binding.attn_bwd(q, k, v, o, lse, torch.zeros_like(q), False, w.scale)
     assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_d64_prefill_sampled():
+    """B4 H16 N2048 d64 causal (the d = 64 prefill workload): dQ on sampled row
+    blocks against the oracle; dK and dV through the softmax identities."""
+    w = W.PREFILL
+    q, k, v = W.make_qkv(w, device=DEV)
+    dout = W.make_dout(w, device=DEV)
+    dq, dk, dv = run_bwd(q, k, v, dout, True, w.scale)
+    rng = np.random.default_rng(2600)
+    for _ in range(3):
+        b, h = int(rng.integers(w.B)), int(rng.integers(w.H))
+        r0 = int(rng.integers(w.Nq // 128)) * 128
+        sl = slice(r0, r0 + 128)
+        rq, _, _ = oracle.attention_bwd(q[b:b + 1, h:h + 1, sl].cpu(), k[b:b + 1, h:h + 1].cpu(),
+                                        v[b:b + 1, h:h + 1].cpu(), dout[b:b + 1, h:h + 1, sl].cpu(),
+                                        causal=True, scale=w.scale, query_offset=r0)
+        compare_grad(dq[b:b + 1, h:h + 1, sl], rq, f"d64 dQ b={b} h={h} rows {r0}+128")
+    sum_dk, sum_dv = dk.double().sum(dim=2), dv.double().sum(dim=2)
+    sum_do = dout.double().sum(dim=2)
+    assert (sum_dk.abs() <= 1e-2 * dk.double().abs().sum(dim=2) + 1e-3).all()
+    assert ((sum_dv - sum_do).abs() <= 1e-2 * dv.double().abs().sum(dim=2) + 1e-3).all()
 
 
 def test_bwd_deterministic():
