@@ -364,6 +364,129 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ consumers
+    float m[QB], l[QB], o[QB][8];
+    if constexpr (QB * UB == LPR && UB == U) {
+      // One score per lane (the UB = U keys of a stage at once): after packed
+      // partial dot products, a
+      // reduce-scatter over the LPR lanes of a key row leaves lane `sub` the
+      // full score of (row sub / UB, key sub % UB) of the current UB keys, so
+      // each exponential is computed once, the row max and sum take
+      // log2(UB) shuffles, and the P V update broadcasts p and alpha.
+      uint64_t q2[QB][4];
+#pragma unroll
+      for (int qi = 0; qi < QB; ++qi) {
+        int64_t position;
+        const uint4 r = ld_stream(p.q + row_of(qi, position) * D + 8 * sub);
+        float qf[8];
+        unpack8(r, qf);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) q2[qi][e] = f2_pack(qf[2 * e] * p.sc_log2, qf[2 * e + 1] * p.sc_log2);
+      }
+      const int own_row = sub / UB, own_u = sub % UB;
+      int lim_own = lim_rel[0];
+#pragma unroll
+      for (int qi = 1; qi < QB; ++qi) lim_own = (own_row == qi) ? lim_rel[qi] : lim_own;
+      float m_row = -INFINITY, l_row = 0.0f;  // state of row own_row (same in its UB lanes)
+      uint64_t o2[QB][4];
+#pragma unroll
+      for (int qi = 0; qi < QB; ++qi)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o2[qi][e] = 0ull;
+      for (int c = 0; c < n_chunks; ++c) {
+        const int st = c % kBulkStages;
+        if (!__all_sync(0xffffffffu, wait(full(st), (c / kBulkStages) & 1, true))) break;
+        const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
+        const int nk = static_cast<int>(min(static_cast<int64_t>(kChunk), k_hi - key0));
+        const uint16_t* ks = reinterpret_cast<const uint16_t*>(dyn + st * 2u * kChunkBytes);
+        const uint16_t* vs = ks + kChunk * D;
+        uint4 kr[UB], vr[UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          const int kk = warp * KPW + u * G + grp;
+          if (kk < nk) {
+            kr[u] = *reinterpret_cast<const uint4*>(ks + kk * D + 8 * sub);
+            vr[u] = *reinterpret_cast<const uint4*>(vs + kk * D + 8 * sub);
+          } else {
+            kr[u] = make_uint4(0u, 0u, 0u, 0u);
+            vr[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(st));  // release orders this warp's reads
+        float part[QB * UB];
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          float kf[8];
+          unpack8(kr[u], kf);
+#pragma unroll
+          for (int qi = 0; qi < QB; ++qi) {
+            uint64_t d2 = f2_mul(q2[qi][0], f2_pack(kf[0], kf[1]));
+            d2 = f2_fma(q2[qi][1], f2_pack(kf[2], kf[3]), d2);
+            d2 = f2_fma(q2[qi][2], f2_pack(kf[4], kf[5]), d2);
+            d2 = f2_fma(q2[qi][3], f2_pack(kf[6], kf[7]), d2);
+            float x0, x1;
+            f2_unpack(d2, x0, x1);
+            part[qi * UB + u] = x0 + x1;
+          }
+        }
+        // Reduce-scatter: at mask m the lane keeps the half of its values
+        // selected by bit m of sub and adds its partner's copy of that half.
+#pragma unroll
+        for (int m = LPR / 2, n = QB * UB; m >= 1; m >>= 1, n >>= 1) {
+          const bool upper = (sub & m) != 0;
+#pragma unroll
+          for (int i = 0; i < n / 2; ++i) {
+            const float keep = upper ? part[i + n / 2] : part[i];
+            const float send = upper ? part[i] : part[i + n / 2];
+            part[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+        const int kk_own = warp * KPW + own_u * G + grp;
+        const int key_rel = static_cast<int>(key0 - k_lo) + kk_own;
+        const float s_own = (kk_own < nk && key_rel <= lim_own) ? part[0] : -INFINITY;
+        float mx = s_own;
+#pragma unroll
+        for (int m = 1; m < UB; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        const float m_new = fmaxf(m_row, mx);
+        const bool live = m_new != -INFINITY;
+        const float alpha_own = live ? ex2_approx(m_row - m_new) : 1.0f;  // 0 when m_row = -inf
+        const float p_own = live ? ex2_approx(s_own - m_new) : 0.0f;
+        float ps = p_own;
+#pragma unroll
+        for (int m = 1; m < UB; m <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, m);
+        l_row = l_row * alpha_own + ps;
+        if (live) m_row = m_new;
+        // P V: every lane updates its 8 d-columns of every row.
+        const int base = grp * LPR;
+#pragma unroll
+        for (int qi = 0; qi < QB; ++qi) {
+          const float al = __shfl_sync(0xffffffffu, alpha_own, base + qi * UB);
+          const uint64_t al2 = f2_pack(al, al);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o2[qi][e] = f2_mul(o2[qi][e], al2);
+        }
+#pragma unroll
+        for (int u = 0; u < UB; ++u) {
+          float vf[8];
+          unpack8(vr[u], vf);
+#pragma unroll
+          for (int qi = 0; qi < QB; ++qi) {
+            const float pu = __shfl_sync(0xffffffffu, p_own, base + qi * UB + u);
+            const uint64_t p2 = f2_pack(pu, pu);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o2[qi][e] = f2_fma(p2, f2_pack(vf[2 * e], vf[2 * e + 1]), o2[qi][e]);
+          }
+        }
+      }
+      // Per-row state of every row in every lane, for the merges below.
+#pragma unroll
+      for (int qi = 0; qi < QB; ++qi) {
+        m[qi] = __shfl_sync(0xffffffffu, m_row, grp * LPR + qi * UB);
+        l[qi] = __shfl_sync(0xffffffffu, l_row, grp * LPR + qi * UB);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f2_unpack(o2[qi][e], o[qi][2 * e], o[qi][2 * e + 1]);
+      }
+    } else {
     float qf[QB][8];
 #pragma unroll
     for (int qi = 0; qi < QB; ++qi) {
@@ -373,7 +496,6 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) qf[qi][e] *= p.sc_log2;
     }
-    float m[QB], l[QB], o[QB][8];
 #pragma unroll
     for (int qi = 0; qi < QB; ++qi) {
       m[qi] = -INFINITY;
@@ -449,6 +571,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         }
       }
     }
+    }  // old path
 #pragma unroll
     for (int off = LPR; off < 32; off <<= 1) {
 #pragma unroll
