@@ -250,19 +250,26 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
   }
 }
 
-constexpr int kBulkWarps = 8;                        // consumer warps
-constexpr int kBulkThreads = (kBulkWarps + 1) * 32;  // + one producer warp
-constexpr int kChunk = 64;                           // keys per pipeline stage
+// Consumer warps: twelve for four rows per K/V head (146 registers; more
+// warps hide the latency of the per-stage shuffle / exponential chain),
+// eight for eight rows (their 168 registers leave no room for more).
+__host__ __device__ constexpr int bulk_warps(int QB) { return QB == 4 ? 12 : 8; }
+__host__ __device__ constexpr int bulk_threads(int QB) { return (bulk_warps(QB) + 1) * 32; }  // + one producer warp
+constexpr int kKeysPerWarp = 8;                       // keys per consumer warp per stage
+__host__ __device__ constexpr int bulk_chunk(int QB) { return bulk_warps(QB) * kKeysPerWarp; }  // keys per stage
 constexpr int kBulkStages = 4;
 
-template <int D>
+template <int D, int QB>
 constexpr uint32_t bulk_smem_bytes() {
-  return kBulkStages * 2u * kChunk * D * 2u + 2u * kBulkStages * 8u + 16u;
+  return kBulkStages * 2u * bulk_chunk(QB) * D * 2u + 2u * kBulkStages * 8u + 16u;
 }
 
 template <int D, int QB>
-__global__ void __launch_bounds__(kBulkThreads, 1)
+__global__ void __launch_bounds__(bulk_threads(QB), 1)
     splitkv_partial_bulk_kernel(const PartialParams p) {
+  constexpr int kBulkWarps = bulk_warps(QB);
+  constexpr int kBulkThreads = bulk_threads(QB);
+  constexpr int kChunk = bulk_chunk(QB);
   constexpr int LPR = D / 8;            // lanes per key row (16 B each)
   constexpr int G = 32 / LPR;           // key rows per warp instruction
   constexpr int KPW = kChunk / kBulkWarps;  // keys per warp per stage
@@ -724,14 +731,14 @@ cudaError_t launch_partial_bulk(const SplitArgs& a, cudaStream_t stream) {
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.status = a.status;
   p.timeout_ns = a.timeout_ns;
-  constexpr uint32_t smem = bulk_smem_bytes<D>();
+  constexpr uint32_t smem = bulk_smem_bytes<D, QB>();
   cudaError_t err = cudaFuncSetAttribute(splitkv_partial_bulk_kernel<D, QB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   const int64_t blocks = (a.BH / p.G) * p.n_qb * a.splits;
   splitkv_partial_bulk_kernel<D, QB>
-      <<<dim3(static_cast<unsigned>(blocks)), kBulkThreads, smem, stream>>>(p);
+      <<<dim3(static_cast<unsigned>(blocks)), bulk_threads(QB), smem, stream>>>(p);
   return cudaGetLastError();
 }
 
