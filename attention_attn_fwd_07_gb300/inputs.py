@@ -57,10 +57,10 @@ LONG_PREFILL_CAUSAL = Workload("long prefill B2 H32 N8192 d128 causal, K x4 on 1
 LONG_PREFILL_NONCAUSAL = Workload("long prefill B2 H32 N8192 d128 non-causal, K x4 on 1% rows",
                                   2, 32, 8192, 8192, 128, False, 1003, k_boost_frac=0.01)
 DECODE = Workload("decode B16 H32 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768, 128, False,
-                  1004, splits=(16, 32, 64))
+                  1004, splits=(8, 16, 32, 64))
 # Grouped-query decode: 8 K/V heads shared by groups of 4 query heads.
 DECODE_GQA = Workload("decode GQA B16 H32 Hkv8 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768,
-                      128, False, 1005, splits=(16, 32, 64), Hkv=8)
+                      128, False, 1005, splits=(8, 16, 32, 64), Hkv=8)
 
 
 def ragged(n: int, causal: bool) -> Workload:
