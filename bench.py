@@ -272,6 +272,36 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU leg
+def init_ranks():
+    """(world, rank, local_rank, dist) from the torchrun environment.  With
+    more than one rank, gloo carries only the barrier around the timed region
+    and the max over ranks of the timing: the ranks are independent replicas
+    (no data-path collective)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+    return world, rank, local, dist
+
+
+def barrier(dist) -> None:
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    """The slowest rank's time: the job is done when every replica is."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_backward(w, q, k, v, o, lse, dev, stream, args, pk, pk_src, world, max_over_ranks):
     """Time attn_bwd (three launches) on the workload's forward outputs."""
     from attention_attn_fwd_07_gb300 import binding
@@ -311,13 +341,7 @@ def main():
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
+    world, rank, local, dist = init_ranks()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
@@ -327,16 +351,11 @@ def main():
     stream = torch.cuda.current_stream()
     pk, pk_src = peaks()
 
-    def barrier():
-        if dist is not None:
-            dist.barrier()
+    def barrier_():
+        barrier(dist)
 
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_over_ranks_(x: float) -> float:
+        return max_over_ranks(dist, x)
 
     launches = 0
 
@@ -392,14 +411,14 @@ def main():
         step()
     sampler = ClockSampler(local)
     sampler.start()
-    barrier()
+    barrier_()
     t0 = time.time()
     ms = event_time(step, args.steps, stream)
     t1 = time.time()
-    barrier()
+    barrier_()
     clocks = sampler.stop(t0, t1)
     launches += args.steps
-    ms = max_over_ranks(ms)
+    ms = max_over_ranks_(ms)
     flops = prefill_flops(w)
     value = world * flops / (ms / 1e3) / 1e12
     per_gpu = flops / (ms / 1e3) / 1e12
@@ -421,8 +440,8 @@ def main():
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(3):
         e2e_step()
-    barrier()
-    e2e_ms = max_over_ranks(event_time(e2e_step, e2e_steps, stream))
+    barrier_()
+    e2e_ms = max_over_ranks_(event_time(e2e_step, e2e_steps, stream))
     launches += e2e_steps
     h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p))
     d2h = o_p.numel() * o_p.element_size() + lse_p.numel() * lse_p.element_size()
@@ -452,11 +471,11 @@ def main():
                 st()
             if wo.Nq >= 8192:
                 n = args.steps
-                m = max_over_ranks(event_time(st, n, stream))
+                m = max_over_ranks_(event_time(st, n, stream))
             else:
                 n = args.steps
                 scratch = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
-                m = max_over_ranks(event_time_flushed(st, n, stream, scratch))
+                m = max_over_ranks_(event_time_flushed(st, n, stream, scratch))
                 del scratch
             launches += n
             tf = prefill_flops(wo) / (m / 1e3) / 1e12
@@ -466,7 +485,7 @@ def main():
                                  "L2 flushed (256 MB rewrite) before each timed launch"})
             if wo.d == 64:  # the d = 64 backward on the same inputs
                 rb = run_backward(wo, qq, kk, vv, oo, ll, dev, stream, args, pk, pk_src, world,
-                                  max_over_ranks)
+                                  max_over_ranks_)
                 rb["l2"] = "inputs (84 MB) fit in L2; not flushed"
                 others.append(rb)
                 launches += 3 * args.steps
@@ -484,7 +503,7 @@ def main():
 
         for _ in range(args.warmup):
             sf()
-        mf = max_over_ranks(event_time(sf, args.steps, stream))
+        mf = max_over_ranks_(event_time(sf, args.steps, stream))
         launches += args.steps
         tff = prefill_flops(wf) / (mf / 1e3) / 1e12
         others.append({"workload": wf.name + ", FP8 e4m3 Q K^T (P V bf16)", "metric": "TFLOPS",
@@ -495,7 +514,7 @@ def main():
 
         # ---- backward of the long causal prefill (dQ, dK, dV from O, LSE, dO)
         others.append(run_backward(w, q, k, v, o, lse, dev, stream, args, pk, pk_src, world,
-                                   max_over_ranks))
+                                   max_over_ranks_))
         launches += 3 * args.steps
 
         # ---- decode (split-KV + combine), memory bound; MHA and grouped K/V heads
@@ -516,7 +535,7 @@ def main():
                 for _ in range(args.warmup):
                     sd()
                 n = max(10, args.steps // 4)
-                m = max_over_ranks(event_time(sd, n, stream))
+                m = max_over_ranks_(event_time(sd, n, stream))
                 launches += 2 * n
                 gbs = decode_bytes(wd) / (m / 1e3) / 1e9
                 results.append({"splits": S, "ms_per_step": m, "GB/s": gbs,
