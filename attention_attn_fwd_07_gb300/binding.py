@@ -291,18 +291,63 @@ def attn_get_device_status(stream=None) -> int:
     return out.value
 
 
+_side_streams: dict = {}
+
+
+def _streams_for(device):
+    """Two side streams per device (uploads, downloads), created once."""
+    key = torch.device(device).index
+    if key not in _side_streams:
+        _side_streams[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _side_streams[key]
+
+
 def fwd_from_host(q_host, k_host, v_host, causal: bool, scale: float, q_dev, k_dev, v_dev,
-                  o_dev, lse_dev, o_host, lse_host, stream=None):
-    """End-to-end call with host buffers: pinned host -> device copies, attn_fwd,
-    device -> host copies of O and LSE, all enqueued on one stream."""
+                  o_dev, lse_dev, o_host, lse_host, stream=None, chunk_heads: int = 8):
+    """End-to-end call with pinned host buffers: host -> device copies of Q, K,
+    V, attn_fwd, device -> host copies of O and LSE.
+
+    The work is split into chunks of ``chunk_heads`` query heads of one batch
+    entry (whole K/V heads; every (b, h) slice is independent), and the chunks
+    are pipelined over three streams: uploads on a side stream, attn_fwd on
+    ``stream`` once its chunk has landed, downloads on another side stream once
+    its chunk is computed.  The host link is the bottleneck, so the compute and
+    most of the downloads hide behind the uploads.  ``stream`` waits for the
+    last download before this returns (the host buffers are valid once
+    ``stream`` is synchronised)."""
     s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        q_dev.copy_(q_host, non_blocking=True)
-        k_dev.copy_(k_host, non_blocking=True)
-        v_dev.copy_(v_host, non_blocking=True)
-        attn_fwd(q_dev, k_dev, v_dev, causal, scale, o=o_dev, lse=lse_dev, stream=s)
-        o_host.copy_(o_dev, non_blocking=True)
-        lse_host.copy_(lse_dev, non_blocking=True)
+    up, down = _streams_for(q_dev.device)
+    B, H = q_dev.shape[0], q_dev.shape[1]
+    Hkv = k_dev.shape[1]
+    G = H // Hkv
+    hc = max(G, (min(chunk_heads, H) // G) * G)  # whole groups of query heads
+    start = torch.cuda.Event()
+    start.record(s)
+    up.wait_event(start)
+    down.wait_event(start)
+    for b in range(B):
+        for h0 in range(0, H, hc):
+            h1 = min(H, h0 + hc)
+            g0, g1 = h0 // G, (h1 + G - 1) // G
+            loaded = torch.cuda.Event()
+            with torch.cuda.stream(up):
+                q_dev[b, h0:h1].copy_(q_host[b, h0:h1], non_blocking=True)
+                k_dev[b, g0:g1].copy_(k_host[b, g0:g1], non_blocking=True)
+                v_dev[b, g0:g1].copy_(v_host[b, g0:g1], non_blocking=True)
+                loaded.record(up)
+            s.wait_event(loaded)
+            attn_fwd(q_dev[b:b + 1, h0:h1], k_dev[b:b + 1, g0:g1], v_dev[b:b + 1, g0:g1],
+                     causal, scale, o=o_dev[b:b + 1, h0:h1], lse=lse_dev[b:b + 1, h0:h1],
+                     stream=s)
+            computed = torch.cuda.Event()
+            computed.record(s)
+            down.wait_event(computed)
+            with torch.cuda.stream(down):
+                o_host[b, h0:h1].copy_(o_dev[b, h0:h1], non_blocking=True)
+                lse_host[b, h0:h1].copy_(lse_dev[b, h0:h1], non_blocking=True)
+    done = torch.cuda.Event()
+    done.record(down)
+    s.wait_event(done)
     return o_host, lse_host
 
 
