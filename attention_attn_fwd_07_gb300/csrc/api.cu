@@ -306,7 +306,6 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
       !encode_map(enc, &tv, p->v, p->Nk, BHkv, p->d))
     return ATTN_ERR_CUDA;
   BwdArgs a;
-  a.q = p->q;
   a.o = p->o;
   a.dout = p->dout;
   a.lse = p->lse;

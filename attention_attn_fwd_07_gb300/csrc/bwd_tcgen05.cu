@@ -101,7 +101,7 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
 }
 
 struct BwdParams {
-  const __nv_bfloat16 *q, *o, *dout;
+  const __nv_bfloat16 *o, *dout;
   const float* lse;
   float* delta;
   __nv_bfloat16 *dq, *dk, *dv;
@@ -275,8 +275,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 // have advanced.
 template <typename LoadA, typename LoadB>
 __device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, const BwdParams& p,
-                                           int64_t n_items, bool res_loaded, LoadA load_a,
-                                           LoadB load_b) {
+                                           int64_t n_items, LoadA load_a, LoadB load_b) {
   int64_t last_a = -1, last_b = -1;
   for (int64_t n = 0; n < n_items; ++n) {
     const int sa = static_cast<int>(n % kStagesA), sb = static_cast<int>(n % kStagesB);
@@ -295,7 +294,7 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, con
   }
   volatile int no_abort = 0;
   const Waiter own{&no_abort, p.status, p.timeout_ns};
-  if (res_loaded) own(c.bar(kBarRes), 0);
+  own(c.bar(kBarRes), 0);
   for (int64_t n = last_a - kStagesA + 1; n <= last_a; ++n)
     if (n >= 0) own(c.bar(kBarFullA + static_cast<int>(n % kStagesA)), (n / kStagesA) & 1);
   for (int64_t n = last_b - kStagesB + 1; n <= last_b; ++n)
@@ -362,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_tile(sK, &tk, c.bar(kBarRes), static_cast<int>(k0), bkv);
       load_tile(sV, &tv, c.bar(kBarRes), static_cast<int>(k0), bkv);
       run_loader(
-          c, wait, p, n_items, true,
+          c, wait, p, n_items,
           [&](int64_t n, uint32_t bar) {
             int64_t bh, q0;
             item_rows(n, bh, q0);
@@ -599,21 +598,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_kt = last_key < 0 ? 0 : static_cast<int>(min(static_cast<int64_t>(n_kt), last_key / T + 1));
   }
 
+  const uint32_t sQ = c.sbase + kOffRes, sdO = sQ + kTileBytes;
   auto sK = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kTileBytes; };
   auto sV = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kTileBytes; };
   auto slot_a = [](int n) { return n % kStagesA; };
   auto slot_b = [](int n) { return n % kStagesB; };
   auto par_a = [](int n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
   auto par_b = [](int n) { return static_cast<uint32_t>((n / kStagesB) & 1); };
-  // TMEM: S [0,128) dP [128,256) dQ [256,256+d); Q and dO of the tile stay
-  // in TMEM as bf16 pairs (d/2 columns each), the A operands of S and dP.
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdQ = c.tmem + 256;
-  const uint32_t tQ = c.tmem + 384, tdO = c.tmem + 384 + D / 2;
 
   if (warp == kWarpLoad) {
     if (lane == 0 && n_kt > 0) {
+      mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
+      load_tile(sQ, &tq, c.bar(kBarRes), static_cast<int>(q0), bh);
+      load_tile(sdO, &tdo, c.bar(kBarRes), static_cast<int>(q0), bh);
       run_loader(
-          c, wait, p, n_kt, false,
+          c, wait, p, n_kt,
           [&](int64_t n, uint32_t bar) {
             load_tile(sK(static_cast<int>(n)), &tk, bar, static_cast<int>(n) * T, bkv);
           },
@@ -631,20 +631,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, wait(b, parity));
     };
     if (n_kt > 0) {
-      auto issue_s = [&](int n) {  // S = Q K^T, A = Q from TMEM
+      auto issue_s = [&](int n) {  // S = Q K^T
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts_w(tS, tQ + 8 * kk, desc_kmajor(sK(n), kk), kIdescSS, kk > 0);
+          mma_ss_w(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(n), kk), kIdescSS, kk > 0);
         mma_commit_w(c.bar(kBarS));
       };
-      auto issue_dp = [&](int n) {  // dP = dO V^T, A = dO from TMEM
+      auto issue_dp = [&](int n) {  // dP = dO V^T
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ts_w(tdP, tdO + 8 * kk, desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
+          mma_ss_w(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
         mma_commit_w(c.bar(kBarDP));
         mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
       };
-      // Q and dO written to TMEM by the elementwise threads (one arrival each
-      // on the statistics barrier, which this kernel does not otherwise use).
-      bool ok = wait_w(c.bar(kBarStat), 0) && wait_w(c.bar(kBarFullA), 0);
+      bool ok = wait_w(c.bar(kBarRes), 0) && wait_w(c.bar(kBarFullA), 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -694,38 +692,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lse = p.lse[bh * p.Nq + i];
       nl2 = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
       nd = -p.delta[bh * p.Nq + i];
-    }
-    {
-      // This thread's row of Q and dO, half h of its d columns, into TMEM:
-      // a bf16 pair per 32-bit column is exactly the MMA's A layout (and the
-      // memory layout), so the words go in unchanged.  Rows past Nq are 0.
-      constexpr int kWords = D / 4;  // 32-bit words per half row
-      uint32_t wq[kWords], wd[kWords];
-      if (i < p.Nq) {
-        const uint4* gq = reinterpret_cast<const uint4*>(p.q + (bh * p.Nq + i) * D + (D / 2) * half);
-        const uint4* gd =
-            reinterpret_cast<const uint4*>(p.dout + (bh * p.Nq + i) * D + (D / 2) * half);
-#pragma unroll
-        for (int v = 0; v < kWords / 4; ++v) {
-          const uint4 a = gq[v], d4 = gd[v];
-          wq[4 * v] = a.x; wq[4 * v + 1] = a.y; wq[4 * v + 2] = a.z; wq[4 * v + 3] = a.w;
-          wd[4 * v] = d4.x; wd[4 * v + 1] = d4.y; wd[4 * v + 2] = d4.z; wd[4 * v + 3] = d4.w;
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < kWords; ++v) wq[v] = wd[v] = 0u;
-      }
-      // (the kernel is not a template, so both branches must type-check)
-      if constexpr (kWords == 32) {
-        tmem_st_x32(tQ + lane_off + kWords * half, *reinterpret_cast<const uint32_t(*)[32]>(wq));
-        tmem_st_x32(tdO + lane_off + kWords * half, *reinterpret_cast<const uint32_t(*)[32]>(wd));
-      } else {
-        tmem_st_x16(tQ + lane_off + kWords * half, *reinterpret_cast<const uint32_t(*)[16]>(wq));
-        tmem_st_x16(tdO + lane_off + kWords * half, *reinterpret_cast<const uint32_t(*)[16]>(wd));
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(c.bar(kBarStat));
     }
     const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
     const uint64_t l22 = f2_pack(nl2, nl2);
@@ -817,7 +783,6 @@ template <>
 cudaError_t launch_bwd_d<D>(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
   BwdParams p;
-  p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.o = static_cast<const __nv_bfloat16*>(a.o);
   p.dout = static_cast<const __nv_bfloat16*>(a.dout);
   p.lse = a.lse;

@@ -52,7 +52,7 @@ inline int64_t splitkv_rows_per_cta(int64_t rows_per_kv_head) {
 
 // Arguments of one backward pass (d = 128), already validated.
 struct BwdArgs {
-  const void *q, *o, *dout;  // bf16 [B][H][Nq][d]
+  const void *o, *dout;  // bf16 [B][H][Nq][d]
   const float* lse;      // f32 [B][H][Nq] from the forward pass
   float* delta;          // workspace f32 [B][H][Nq]: rowsum(dO * O)
   void *dq, *dk, *dv;    // bf16 outputs, [B][H][Nq][d] and [B][Hkv][Nk][d]
