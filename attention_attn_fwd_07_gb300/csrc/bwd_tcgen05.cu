@@ -93,12 +93,10 @@ constexpr uint32_t kColDV = 256, kColDK = 256 + D;
 // were ever not 1024-byte aligned.
 constexpr int kStatusMisaligned = 2;
 
-// Column of the packed bf16 operand (P or dS, two values per 32-bit column)
-// that holds K step kk (16 values): column half h = kk / 4 packs its 64
-// values into the first 32 columns of its own 64-column range.
-__device__ __forceinline__ uint32_t packed_col(int kk) {
-  return static_cast<uint32_t>(64 * (kk >> 2) + 8 * (kk & 3));
-}
+// Packed bf16 operands (P or dS, two values per 32-bit column) are stored
+// by column half: half h of a 128-wide row packs its 64 values into the
+// first 32 columns of its own 64-column range, so K step kk (16 values)
+// sits at column 64 (kk / 4) + 8 (kk % 4).
 
 struct BwdParams {
   const __nv_bfloat16 *o, *dout;
@@ -143,6 +141,23 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
 // MN-major SW128 operand (rows = K, N = d contiguous): K step kk (16 rows).
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   return sdesc_sw128(tile + kk * 16 * 128, kAtomBytes, 1024);
+}
+
+// D = A B^T over the d columns of two K-major [128][d] tiles: d / 16 MMAs
+// from one elect.sync.
+__device__ __forceinline__ void mma_ss_tiles_w(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
+  if constexpr (D == 128)
+    mma_ss_run8_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
+  else
+    mma_ss_run4_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
+}
+// D (+)= A B over 128 K rows: A is a packed bf16 operand in tensor memory
+// (by column half, as above), B an MN-major [128][d] tile; eight MMAs from
+// one elect.sync.
+__device__ __forceinline__ void mma_ts_tile_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_tile,
+                                              bool accumulate) {
+  static_assert(T == 128, "eight K steps of 16");
+  mma_ts_run8_halves_w(d_tmem, a_tmem, desc_mnmajor(b_tile, 0), kIdescTS, accumulate ? 1u : 0u);
 }
 
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
@@ -385,13 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (n_items > 0) {
       auto issue_s = [&](int64_t n) {  // S^T = K Q^T
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tS, desc_kmajor(sK, kk), desc_kmajor(sQ(n), kk), kIdescSS, kk > 0);
+        mma_ss_tiles_w(tS, sK, sQ(n));
         mma_commit_w(c.bar(kBarS));
       };
       auto issue_dp = [&](int64_t n) {  // dP^T = V dO^T
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tdP, desc_kmajor(sV, kk), desc_kmajor(sdO(n), kk), kIdescSS, kk > 0);
+        mma_ss_tiles_w(tdP, sV, sdO(n));
         mma_commit_w(c.bar(kBarDP));
       };
       bool ok = wait_w(c.bar(kBarRes), 0) && wait_w(c.bar(kBarFullA), 0);
@@ -408,8 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_w(c.bar(kBarP), n & 1);
         if (!ok) break;
         tc_fence_after();
-        for (int kk = 0; kk < T / 16; ++kk)  // dV += P^T dO
-          mma_ts_w(tdV, tS + packed_col(kk), desc_mnmajor(sdO(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_ts_tile_w(tdV, tS, sdO(n), n > 0);
         mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
         const bool more = n + 1 < n_items;
         if (more) {
@@ -421,8 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_w(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
-        for (int kk = 0; kk < T / 16; ++kk)  // dK += dS^T Q
-          mma_ts_w(tdK, tdP + packed_col(kk), desc_mnmajor(sQ(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_ts_tile_w(tdK, tdP, sQ(n), n > 0);
         mma_commit_w(c.bar(kBarEmptyA + slot_a(n)));
         if (more) {
           ok = wait_w(c.bar(kBarFullB + slot_b(n + 1)), par_b(n + 1));
@@ -632,13 +643,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (n_kt > 0) {
       auto issue_s = [&](int n) {  // S = Q K^T
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tS, desc_kmajor(sQ, kk), desc_kmajor(sK(n), kk), kIdescSS, kk > 0);
+        mma_ss_tiles_w(tS, sQ, sK(n));
         mma_commit_w(c.bar(kBarS));
       };
       auto issue_dp = [&](int n) {  // dP = dO V^T
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_w(tdP, desc_kmajor(sdO, kk), desc_kmajor(sV(n), kk), kIdescSS, kk > 0);
+        mma_ss_tiles_w(tdP, sdO, sV(n));
         mma_commit_w(c.bar(kBarDP));
         mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
       };
@@ -664,8 +673,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_w(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
-        for (int kk = 0; kk < T / 16; ++kk)  // dQ += dS K
-          mma_ts_w(tdQ, tdP + packed_col(kk), desc_mnmajor(sK(n), kk), kIdescTS, (n > 0 || kk > 0));
+        mma_ts_tile_w(tdQ, tdP, sK(n), n > 0);
         mma_commit_w(c.bar(kBarEmptyA + slot_a(n)));
         if (more) {
           ok = wait_w(c.bar(kBarFullB + slot_b(n + 1)), par_b(n + 1));

@@ -263,33 +263,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs this loop (waits made warp-uniform); the MMA and
-    // commit calls elect one lane to issue.
+    // The whole warp runs this loop (waits made warp-uniform); each run of
+    // MMAs and each commit elects one lane to issue.
     auto wait_w = [&](uint32_t b, uint32_t parity) {
       return __all_sync(0xffffffffu, wait(b, parity));
     };
+    auto commit = [&](uint32_t b) { mma_commit_w(b); };
     if (n_kv > 0) {
       auto qk = [&](int x, int stage) {
         const uint32_t d_tmem = tmem + C::kColS + 128 * x;
+        const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes, 16, 1024);
+        const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, 16, 1024);
         // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
-        for (int kk = 0; kk < D * C::kQKElem / 32; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kAtomBytes + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes + off, 16, 1024);
-          const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes + off, 16, 1024);
-          if constexpr (FP8)
-            mma_ss_f8_w(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
-          else
-            mma_ss_w(d_tmem, a, b, C::kIdescQK, kk > 0 ? 1u : 0u);
-        }
+        if constexpr (FP8)
+          mma_ss_f8_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
+        else if constexpr (D == 128)
+          mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
+        else
+          mma_ss_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
       };
       auto pv = [&](int x, int stage, bool acc) {
         const uint32_t d_tmem = tmem + C::kColO + DV * x;
         const uint32_t p_tmem = tmem + C::kColS + 128 * x;
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t b =
-              sdesc_sw128(sKV + stage * C::kKVBytes + kk * 16 * 128, C::kAtomBytes, 1024);
-          mma_ts_w(d_tmem, p_tmem + kk * 8, b, C::kIdescPV, (acc || kk > 0) ? 1u : 0u);
-        }
+        const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, C::kAtomBytes, 1024);
+        static_assert(BN == 128, "eight K steps of 16 keys");
+        mma_ts_run8_w(d_tmem, p_tmem, b, C::kIdescPV, acc ? 1u : 0u);
       };
       bool ok = wait_w(bar(C::kBarQ), 0);
       if (ok) ok = wait_w(bar(C::kBarFull + 0), 0);
@@ -298,10 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int x = 0; x < 2; ++x) {
           if (ntile[x] > 0) {
             qk(x, 0);
-            mma_commit_w(bar(C::kBarS + x));
+            commit(bar(C::kBarS + x));
           }
         }
-        mma_commit_w(bar(C::kBarEmpty + 0));
+        commit(bar(C::kBarEmpty + 0));
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int tV = 2 * j + 1, sV = tV % C::kStages;
@@ -316,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           pv(x, sV, j > 0);
-          if (j == ntile[x] - 1) mma_commit_w(bar(C::kBarO + x));
+          if (j == ntile[x] - 1) commit(bar(C::kBarO + x));
           if (j + 1 < ntile[x]) {
             if (!k_ready) {
               ok = wait_w(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
@@ -325,22 +323,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               k_ready = true;
             }
             qk(x, sK);
-            mma_commit_w(bar(C::kBarS + x));
+            commit(bar(C::kBarS + x));
           }
         }
         if (!ok) break;
-        mma_commit_w(bar(C::kBarEmpty + sV));
+        commit(bar(C::kBarEmpty + sV));
         if (next) {
           if (!k_ready) {  // K(j+1) is used by no tile: still consume it in order
             ok = wait_w(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
             if (!ok) break;
           }
-          mma_commit_w(bar(C::kBarEmpty + sK));
+          commit(bar(C::kBarEmpty + sK));
         }
       }
       // All issued MMAs must complete before TMEM is released (bounded wait
       // that ignores the abort flag).
-      mma_commit_w(bar(C::kBarDrain));
+      commit(bar(C::kBarDrain));
       volatile int no_abort = 0;
       const Waiter own{&no_abort, p.status, p.timeout_ns};
       own(bar(C::kBarDrain), 0);

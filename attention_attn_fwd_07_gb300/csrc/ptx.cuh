@@ -182,6 +182,135 @@ __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
       : "memory");
 }
 
+// Runs of K steps from one elect.sync: the whole converged warp executes
+// one asm block, the elected lane issues every MMA of the run.  Step 0 uses
+// the caller's accumulate flag, later steps accumulate.  Descriptor and
+// tensor-memory offsets per step are immediates (16-byte units for shared
+// memory descriptors, columns for tensor memory).
+#define ATTN_MMA_SS_STEP(KIND, OFF)                              \
+  "add.s64 a, %1, " #OFF ";\n\tadd.s64 b, %2, " #OFF ";\n\t"      \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a, b, %3, t;\n\t"
+#define ATTN_MMA_RUN_HEAD(KIND)                                 \
+  "{\n\t.reg .pred p, e, t;\n\t.reg .b64 a, b;\n\t"             \
+  "elect.sync _|e, 0xffffffff;\n\t"                              \
+  "setp.ne.b32 p, %4, 0;\n\t"                                    \
+  "setp.eq.b32 t, %4, %4;\n\t"                                   \
+  "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], %1, %2, %3, p;\n\t"
+
+// Eight K steps over two 128-byte-swizzle atoms of K-major operands
+// (bf16, 128 values per row): offsets 0, 32, 64, 96 bytes inside an atom,
+// then the next 16 KB atom.
+__device__ __forceinline__ void mma_ss_run8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(ATTN_MMA_RUN_HEAD("f16") ATTN_MMA_SS_STEP("f16", 2) ATTN_MMA_SS_STEP("f16", 4)
+                   ATTN_MMA_SS_STEP("f16", 6) ATTN_MMA_SS_STEP("f16", 1024)
+                       ATTN_MMA_SS_STEP("f16", 1026) ATTN_MMA_SS_STEP("f16", 1028)
+                           ATTN_MMA_SS_STEP("f16", 1030) "}"
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+// Four K steps inside one atom (bf16 with 64 values per row).
+__device__ __forceinline__ void mma_ss_run4_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(ATTN_MMA_RUN_HEAD("f16") ATTN_MMA_SS_STEP("f16", 2) ATTN_MMA_SS_STEP("f16", 4)
+                   ATTN_MMA_SS_STEP("f16", 6) "}"
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+// Four K steps of 32 e4m3 values inside one atom (FP8, 128 values per row).
+__device__ __forceinline__ void mma_ss_f8_run4_w(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(ATTN_MMA_RUN_HEAD("f8f6f4") ATTN_MMA_SS_STEP("f8f6f4", 2)
+                   ATTN_MMA_SS_STEP("f8f6f4", 4) ATTN_MMA_SS_STEP("f8f6f4", 6) "}"
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
+#define ATTN_MMA_TS_STEP(COLS, OFF)                                            \
+  "add.u32 ta, %1, " #COLS ";\n\tadd.s64 b, %2, " #OFF ";\n\t"                    \
+  "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
+// Eight K steps of D += A[tmem] B[smem]: A advances 8 columns (16 bf16) per
+// step, B is MN-major with 16 rows of 128 bytes per step.
+__device__ __forceinline__ void mma_ts_run8_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384)
+      ATTN_MMA_TS_STEP(32, 512) ATTN_MMA_TS_STEP(40, 640) ATTN_MMA_TS_STEP(48, 768)
+      ATTN_MMA_TS_STEP(56, 896) "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Same, with A packed two 64-column halves apart (K step k at column
+// 64 (k / 4) + 8 (k % 4)): the layout in which a warp pair stores the bf16
+// halves of a 128-wide operand row into 32 columns each.
+__device__ __forceinline__ void mma_ts_run8_halves_w(uint32_t d_tmem, uint32_t a_tmem,
+                                                     uint64_t b_desc, uint32_t idesc,
+                                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384)
+      ATTN_MMA_TS_STEP(64, 512) ATTN_MMA_TS_STEP(72, 640) ATTN_MMA_TS_STEP(80, 768)
+      ATTN_MMA_TS_STEP(88, 896) "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Leader forms: the converged warp executes the call and the lane whose
+// `leader` is nonzero (exactly one, the same lane for the warp's lifetime)
+// issues.  Same instruction as the elect.sync forms without an elect per
+// MMA, so a run of MMAs costs fewer issue slots on a busy SMSP.
+__device__ __forceinline__ void mma_ss_l(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
+                                         uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 e, %5, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_f8_l(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
+                                            uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 e, %5, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_l(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
+                                         uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 e, %5, 0;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_l(uint32_t leader, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "setp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      ::"r"(bar), "r"(leader)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so
 // far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -197,15 +326,30 @@ __device__ __forceinline__ void tmem_st_wait() {
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), fixed version field 1 at bit 46, and
 // the 128-byte swizzle layout code 2 at bits 61-63.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
+__host__ __device__ constexpr uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
 }
+// The same descriptor as two 32-bit words, so that a loop over K steps
+// advances the start address with one 32-bit add (address >> 4 stays below
+// 2^14 for any shared-memory address, so the add never carries out of the
+// 14-bit field).
+__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__host__ __device__ constexpr uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+static_assert(sdesc_join(sdesc_lo(0x12400u + 0x2020u, 16), sdesc_hi_sw128(1024)) ==
+                  sdesc_sw128(0x12400u + 0x2020u, 16, 1024) &&
+              sdesc_join(sdesc_lo(0x4000u, 16384) + 0x300u, sdesc_hi_sw128(1024)) ==
+                  sdesc_sw128(0x4000u + 0x3000u, 16384, 1024),
+              "split descriptor words");
 
 // Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulator.
 // b_mn_major = 1 when B is stored with N contiguous (e.g. V as [keys][d]).
