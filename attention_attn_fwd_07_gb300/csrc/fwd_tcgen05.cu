@@ -26,7 +26,10 @@
 //   warps 0-3   softmax of tile A; warps 4-7 softmax of tile B.  One thread
 //               per query row (TMEM lane = row): tcgen05.ld of the 128-score
 //               row, mask, row max, exp2, row sum, bf16 P written back into the
-//               S columns with tcgen05.st; O rescaled in TMEM only when the
+//               S columns with tcgen05.st in two halves of 64 keys, each
+//               announced on its own barrier so that O += P V starts on the
+//               first half while the second is computed; O rescaled in TMEM
+//               only when the
 //               row maximum grew by more than 2^8 (otherwise the stale
 //               reference is kept; o and l share it, so o / l is unchanged).
 //               Epilogue: O / l -> bf16 global, LSE -> f32 global.
@@ -67,13 +70,15 @@ struct Cfg {
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQBytes;
   static constexpr uint32_t kOffBar = kOffKV + kStages * kKVBytes;
-  // barriers: full[S], empty[S], q_full, s_full[2], p_ready[2], o_full[2], drain
+  // barriers: full[S], empty[S], q_full, s_full[2], p_ready[2] (keys 0-63 of
+  // P stored), p2_ready[2] (keys 64-127), o_full[2], drain
   static constexpr int kBarFull = 0;
   static constexpr int kBarEmpty = kStages;
   static constexpr int kBarQ = 2 * kStages;
   static constexpr int kBarS = kBarQ + 1;
   static constexpr int kBarP = kBarS + 2;
-  static constexpr int kBarO = kBarP + 2;
+  static constexpr int kBarP2 = kBarP + 2;
+  static constexpr int kBarO = kBarP2 + 2;
   static constexpr int kBarDrain = kBarO + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
@@ -190,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::kBarS + x), 1);
       mbar_init(bar(C::kBarP + x), 4);  // one arrival per softmax warp
+      mbar_init(bar(C::kBarP2 + x), 4);
       mbar_init(bar(C::kBarO + x), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
@@ -282,12 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           mma_ss_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
       };
-      auto pv = [&](int x, int stage, bool acc) {
+      // O_X += P_X V over keys 64 h .. 64 h + 63 (four K steps of 16 keys;
+      // P's bf16 pairs for those keys sit in columns 32 h .. 32 h + 31).
+      auto pv_half = [&](int x, int stage, int h, bool acc) {
         const uint32_t d_tmem = tmem + C::kColO + DV * x;
-        const uint32_t p_tmem = tmem + C::kColS + 128 * x;
-        const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, C::kAtomBytes, 1024);
-        static_assert(BN == 128, "eight K steps of 16 keys");
-        mma_ts_run8_w(d_tmem, p_tmem, b, C::kIdescPV, acc ? 1u : 0u);
+        const uint32_t p_tmem = tmem + C::kColS + 128 * x + 32 * h;
+        const uint64_t b =
+            sdesc_sw128(sKV + stage * C::kKVBytes + h * 64 * 128, C::kAtomBytes, 1024);
+        static_assert(BN == 128, "two halves of four K steps of 16 keys");
+        mma_ts_run4_w(d_tmem, p_tmem, b, C::kIdescPV, acc ? 1u : 0u);
       };
       bool ok = wait_w(bar(C::kBarQ), 0);
       if (ok) ok = wait_w(bar(C::kBarFull + 0), 0);
@@ -313,7 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_w(bar(C::kBarP + x), j & 1);
           if (!ok) break;
           tc_fence_after();
-          pv(x, sV, j > 0);
+          pv_half(x, sV, 0, j > 0);
+          ok = wait_w(bar(C::kBarP2 + x), j & 1);
+          if (!ok) break;
+          tc_fence_after();
+          pv_half(x, sV, 1, true);
           if (j == ntile[x] - 1) commit(bar(C::kBarO + x));
           if (j + 1 < ntile[x]) {
             if (!k_ready) {
@@ -400,40 +413,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_ref = (m_ref == -INFINITY) ? 0.0f : -m_ref;
       // p = 2^(s * scale * log2 e - m_ref), two lanes per instruction; the
-      // row sum uses four independent packed accumulators.
+      // row sum uses four independent packed accumulators.  P goes back to
+      // tensor memory in two halves (keys 0-63, then 64-127), each announced
+      // on its own barrier, so the first half of P V starts while the second
+      // half is exponentiated.  The rare O rescale lands before the first
+      // announcement.
       const uint64_t scale2 = f2_pack(p.sc_log2, p.sc_log2);
       const uint64_t bias2 = f2_pack(neg_ref, neg_ref);
       uint64_t acc2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc2[i] = 0ull;
-      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x0, x1;
-        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), scale2, bias2), x0, x1);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
-        pk[c] = pack_bf16x2(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int cc = 32 * h + c;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(s[2 * cc], s[2 * cc + 1]), scale2, bias2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x32(tS + 32 * h, pk);
+        if (h == 0 && __any_sync(0xffffffffu, rescale) && j > 0) {
+#pragma unroll 1
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + cc * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_x32(tO + cc * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar((h == 0 ? C::kBarP : C::kBarP2) + x));
       }
       float sum_lo, sum_hi;
       f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
       l += sum_lo + sum_hi;
-      tmem_st_x64(tS, pk);
-      if (__any_sync(0xffffffffu, rescale) && j > 0) {
-#pragma unroll 1
-        for (int cc = 0; cc < DV / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld_x32(tO + cc * 32, o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st_x32(tO + cc * 32, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::kBarP + x));
     }
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, wait(bar(C::kBarO + x), 0));

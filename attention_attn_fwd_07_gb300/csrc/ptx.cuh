@@ -246,6 +246,20 @@ __device__ __forceinline__ void mma_ts_run8_w(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
+// Four such K steps (half of a 128-key P tile).
+__device__ __forceinline__ void mma_ts_run4_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384) "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Same, with A packed two 64-column halves apart (K step k at column
 // 64 (k / 4) + 8 (k % 4)): the layout in which a warp pair stores the bf16
 // halves of a 128-wide operand row into 32 columns each.
