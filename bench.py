@@ -94,14 +94,14 @@ def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(path=PROFILE_TXT, sources=KERNEL_SOURCES):
+def recorded_traffic(path=PROFILE_TXT, sources=KERNEL_SOURCES, key="traffic_bytes_per_launch"):
     """DRAM bytes per launch (full-size workload) from a committed ncu
     summary, if it was taken on the current kernel source (else None)."""
     if not os.path.exists(path):
         return None
     txt = open(path).read()
-    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
-    tb = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", txt)
+    src = re.search(r"^kernel_source_sha256_16:\s*([0-9a-f]+)", txt, re.M)
+    tb = re.search(r"^" + re.escape(key) + r":\s*([0-9]+)", txt, re.M)
     if not src or not tb or src.group(1) != kernel_source_hash(sources):
         return None
     return int(tb.group(1))
@@ -552,8 +552,10 @@ def main():
                                  "peak": pk["hbm_gbs"], "unit": "GB/s",
                                  "frac": best["GB/s"] / pk["hbm_gbs"],
                                  "peak_source": f"{pk_src} copy bandwidth",
-                                 "traffic": recorded_traffic(DECODE_PROFILE_TXT, DECODE_SOURCES)
-                                 if wd is W.DECODE else None},
+                                 "traffic": recorded_traffic(
+                                     DECODE_PROFILE_TXT, DECODE_SOURCES,
+                                     "traffic_bytes_per_launch" if wd is W.DECODE
+                                     else "gqa_traffic_bytes_per_launch")},
                     "l2": f"inputs {decode_bytes(wd) / 1e9:.1f} GB > L2"}
 
         decode = run_decode(W.DECODE)
