@@ -100,79 +100,16 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]; bf16 inputs, f32 accumulate.
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[smem] * B[smem]; FP8 (e4m3) inputs, f32 accumulate.
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]; A is read from tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Whole-warp forms of the MMA and commit calls: every lane of a converged
-// warp executes the call and elect.sync picks the one lane that issues it.
-// In a fully converged warp elect.sync always picks the lowest lane, so the
-// commits track the same thread's MMAs.  Issuing this way is cheaper than
-// from a single lane inside a divergent branch (measured ~41 vs ~56 cycles
-// per MMA on sm_103a), which matters because one 128x128x16 MMA runs for
-// only ~64 cycles.
-__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
+// Issue from the whole converged warp: every lane executes the call and
+// elect.sync picks the one lane that issues.  In a fully converged warp
+// elect.sync always picks the lowest lane, so commits track the same
+// thread's MMAs.  Issuing this way is cheaper than from a single lane in a
+// divergent branch (measured ~41 vs ~56 cycles per MMA on sm_103a), which
+// matters because one 128x128x16 MMA runs for only ~64 cycles; the MMA
+// calls below go further and issue a whole run of K steps per elect.sync.
+//
+// Arrive (once) on `bar` when every tcgen05 operation the elected lane
+// issued so far has completed.
 __device__ __forceinline__ void mma_commit_w(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -229,24 +166,9 @@ __device__ __forceinline__ void mma_ss_f8_run4_w(uint32_t d_tmem, uint64_t a_des
 #define ATTN_MMA_TS_STEP(COLS, OFF)                                            \
   "add.u32 ta, %1, " #COLS ";\n\tadd.s64 b, %2, " #OFF ";\n\t"                    \
   "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], b, %3, t;\n\t"
-// Eight K steps of D += A[tmem] B[smem]: A advances 8 columns (16 bf16) per
-// step, B is MN-major with 16 rows of 128 bytes per step.
-__device__ __forceinline__ void mma_ts_run8_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 b;\n\t.reg .b32 ta;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "setp.eq.b32 t, %4, %4;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      ATTN_MMA_TS_STEP(8, 128) ATTN_MMA_TS_STEP(16, 256) ATTN_MMA_TS_STEP(24, 384)
-      ATTN_MMA_TS_STEP(32, 512) ATTN_MMA_TS_STEP(40, 640) ATTN_MMA_TS_STEP(48, 768)
-      ATTN_MMA_TS_STEP(56, 896) "}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Four such K steps (half of a 128-key P tile).
+// Four K steps of D += A[tmem] B[smem] (half of a 128-key P tile): A
+// advances 8 columns (16 bf16) per step, B is MN-major with 16 rows of 128
+// bytes per step.
 __device__ __forceinline__ void mma_ts_run4_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -260,7 +182,8 @@ __device__ __forceinline__ void mma_ts_run4_w(uint32_t d_tmem, uint32_t a_tmem, 
       : "memory");
 }
 
-// Same, with A packed two 64-column halves apart (K step k at column
+// Eight K steps of the same kind, with A packed two 64-column halves apart
+// (K step k at column
 // 64 (k / 4) + 8 (k % 4)): the layout in which a warp pair stores the bf16
 // halves of a 128-wide operand row into 32 columns each.
 __device__ __forceinline__ void mma_ts_run8_halves_w(uint32_t d_tmem, uint32_t a_tmem,
@@ -279,60 +202,6 @@ __device__ __forceinline__ void mma_ts_run8_halves_w(uint32_t d_tmem, uint32_t a
       : "memory");
 }
 
-// Leader forms: the converged warp executes the call and the lane whose
-// `leader` is nonzero (exactly one, the same lane for the warp's lifetime)
-// issues.  Same instruction as the elect.sync forms without an elect per
-// MMA, so a run of MMAs costs fewer issue slots on a busy SMSP.
-__device__ __forceinline__ void mma_ss_l(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
-                                         uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 e, %5, 0;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ss_f8_l(uint32_t leader, uint32_t d_tmem, uint64_t a_desc,
-                                            uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 e, %5, 0;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_l(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem,
-                                         uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 e, %5, 0;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_l(uint32_t leader, uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "setp.ne.b32 e, %1, 0;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-      ::"r"(bar), "r"(leader)
-      : "memory");
-}
-
-// Arrive (once) on `bar` when every tcgen05 operation this thread issued so
-// far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -346,24 +215,6 @@ __host__ __device__ constexpr uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo,
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
-// The same descriptor as two 32-bit words, so that a loop over K steps
-// advances the start address with one 32-bit add (address >> 4 stays below
-// 2^14 for any shared-memory address, so the add never carries out of the
-// 14-bit field).
-__host__ __device__ constexpr uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo) {
-  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
-}
-__host__ __device__ constexpr uint32_t sdesc_hi_sw128(uint32_t sbo) {
-  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
-}
-__host__ __device__ constexpr uint64_t sdesc_join(uint32_t lo, uint32_t hi) {
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-static_assert(sdesc_join(sdesc_lo(0x12400u + 0x2020u, 16), sdesc_hi_sw128(1024)) ==
-                  sdesc_sw128(0x12400u + 0x2020u, 16, 1024) &&
-              sdesc_join(sdesc_lo(0x4000u, 16384) + 0x300u, sdesc_hi_sw128(1024)) ==
-                  sdesc_sw128(0x4000u + 0x3000u, 16384, 1024),
-              "split descriptor words");
 
 // Instruction descriptor for kind::f16 with bf16 A/B and f32 accumulator.
 // b_mn_major = 1 when B is stored with N contiguous (e.g. V as [keys][d]).
@@ -485,15 +336,4 @@ __device__ __forceinline__ void tmem_st_x64(uint32_t taddr, const uint32_t (&r)[
       : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
       : "memory");
 }
-
-// Stores 16 consecutive 32-bit TMEM columns of this thread's lane (32x32b).
-// Completion is awaited separately with tmem_st_wait().
-__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n"
-      :
-      : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
 }  // namespace attn
