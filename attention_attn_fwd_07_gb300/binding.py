@@ -228,9 +228,10 @@ def attn_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: in
     return int(load_library().attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
 
 
-def _workspace(q, num_splits, workspace):
+def _workspace(q, num_splits, workspace, dv=None):
+    """Split-KV workspace (partials are as wide as V: ``dv``, default d)."""
     B, H, Nq, d = q.shape
-    need = attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+    need = attn_splitkv_workspace_bytes(B, H, Nq, dv or d, num_splits)
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
     return workspace, workspace.numel() * workspace.element_size()
@@ -257,8 +258,9 @@ def attn_fwd_splitkv(q, k, v, causal: bool, scale: float, num_splits: int, works
 def attn_fwd_splitkv_ex(q, k, v, causal: bool, scale: float, num_splits: int,
                         query_offset: int = 0, flags: int = 0, workspace=None, o=None, lse=None,
                         stream=None):
-    o, lse = _outputs(q, o, lse)
-    ws, ws_bytes = _workspace(q, num_splits, workspace)
+    dv = v.shape[3]
+    o, lse = _outputs(q, o, lse, dv)
+    ws, ws_bytes = _workspace(q, num_splits, workspace, dv)
     p = make_params(q, k, v, o, lse, causal, scale, query_offset, flags)
     rc = load_library().attn_fwd_splitkv_ex(ctypes.byref(p), int(num_splits), _ptr(ws), ws_bytes,
                                             _stream(stream))

@@ -202,15 +202,16 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   if (rc != ATTN_OK) return rc;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
   if (p->qk_dtype != ATTN_QK_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (p->dv != 0 && p->dv != p->d) return ATTN_ERR_UNSUPPORTED;
-  const size_t need = attn_splitkv_workspace_bytes(p->B, p->H, p->Nq, p->d, num_splits);
+  const int64_t dv = p->dv > 0 ? p->dv : p->d;  // width of V, O and the partials
+  const size_t need = attn_splitkv_workspace_bytes(p->B, p->H, p->Nq, dv, num_splits);
   if (need == 0) return ATTN_ERR_UNSUPPORTED;
   if (workspace == nullptr || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return ATTN_ERR_ALIGN;
   const int64_t BH = p->B * p->H;
   const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
   const int64_t rows = (p->H / Hkv) * p->Nq;  // query rows sharing one K/V head
-  const int64_t qb = splitkv_rows_per_cta(rows);
+  // dv != d: the register-streaming partial kernel, one query row per CTA.
+  const int64_t qb = dv != p->d ? 1 : splitkv_rows_per_cta(rows);
   if (p->B * Hkv * ((rows + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
 
   const size_t part_rows = static_cast<size_t>(BH) * num_splits * static_cast<size_t>(p->Nq);
@@ -220,7 +221,7 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   a.v = p->v;
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        align256(part_rows * static_cast<size_t>(p->d) * 4));
+                                        align256(part_rows * static_cast<size_t>(dv) * 4));
   a.BH = BH;
   a.H = p->H;
   a.Hkv = Hkv;
@@ -229,6 +230,7 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   a.query_offset = p->query_offset;
   a.keys_per_split = keys_per_split(p->Nk, num_splits);
   a.d = static_cast<int>(p->d);
+  a.dv = static_cast<int>(dv);
   a.splits = num_splits;
   a.causal = p->causal ? 1 : 0;
   a.scale = p->scale;
@@ -236,7 +238,7 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   if (a.status == nullptr && default_status_word(&a.status) != cudaSuccess) return ATTN_ERR_CUDA;
   a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
   if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (launch_combine(a.o_part, a.lse_part, p->o, p->lse, BH, p->Nq, a.d, num_splits, stream) !=
+  if (launch_combine(a.o_part, a.lse_part, p->o, p->lse, BH, p->Nq, a.dv, num_splits, stream) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;

@@ -27,13 +27,14 @@ struct FwdArgs {
 
 // Arguments of one split-KV decode launch pair, already validated.
 struct SplitArgs {
-  const void *q, *k, *v;  // bf16 q [B][H][Nq][d], k/v [B][Hkv][Nk][d]
-  float* o_part;          // f32 [BH][S][Nq][d]
+  const void *q, *k, *v;  // bf16 q [B][H][Nq][d], k [B][Hkv][Nk][d], v [B][Hkv][Nk][dv]
+  float* o_part;          // f32 [BH][S][Nq][dv]
   float* lse_part;        // f32 [BH][S][Nq]
   int64_t BH, Nq, Nk, query_offset;  // BH: batch x query heads
   int64_t H, Hkv;                     // query heads and K/V heads per batch
   int64_t keys_per_split;
   int d;
+  int dv = 0;  // value head dim (0 = d); dv != d runs one query row per partial CTA
   int splits;
   int causal;
   float scale;

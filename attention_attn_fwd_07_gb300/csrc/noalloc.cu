@@ -104,6 +104,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   const int64_t per = (Nk + num_splits - 1) / num_splits;
   a.keys_per_split = (per + 127) / 128 * 128;
   a.d = static_cast<int>(d);
+  a.dv = a.d;
   a.splits = num_splits;
   a.causal = causal ? 1 : 0;
   a.scale = scale;

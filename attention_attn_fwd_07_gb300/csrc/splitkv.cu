@@ -61,6 +61,15 @@ __device__ __forceinline__ uint4 ld_stream(const uint16_t* ptr) {
   return r;
 }
 
+// 8-byte form, for value rows narrower than the key rows.
+__device__ __forceinline__ uint2 ld_stream8(const uint16_t* ptr) {
+  uint2 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];"
+      : "=r"(r.x), "=r"(r.y)
+      : "l"(ptr));
+  return r;
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -72,27 +81,62 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
 }
 
 // Merge state (m2, l2, o2) into (m, l, o); all in log2 units.
-__device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[8], float m2, float l2,
-                                            const float (&o2)[8]) {
+template <int E>
+__device__ __forceinline__ void merge_state(float& m, float& l, float (&o)[E], float m2, float l2,
+                                            const float (&o2)[E]) {
   const float mn = fmaxf(m, m2);
   if (mn == -INFINITY) return;  // both empty
   const float a = ex2_approx(m - mn);
   const float b = ex2_approx(m2 - mn);
   l = l * a + l2 * b;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = o[e] * a + o2[e] * b;
+  for (int e = 0; e < E; ++e) o[e] = o[e] * a + o2[e] * b;
   m = mn;
 }
 
-template <int D, int QB, int U, int MINB>
+// The VE values of a value row this lane owns (VE = 4, 8 or 16 bf16), as
+// bf16 pairs, and their f32 widening.
+template <int VE>
+struct VSlice {
+  uint32_t w[VE / 2];
+  __device__ __forceinline__ void load(const uint16_t* ptr) {
+    if constexpr (VE == 4) {
+      const uint2 r = ld_stream8(ptr);
+      w[0] = r.x; w[1] = r.y;
+    } else {
+#pragma unroll
+      for (int c = 0; c < VE / 8; ++c) {
+        const uint4 r = ld_stream(ptr + 8 * c);
+        w[4 * c] = r.x; w[4 * c + 1] = r.y; w[4 * c + 2] = r.z; w[4 * c + 3] = r.w;
+      }
+    }
+  }
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int i = 0; i < VE / 2; ++i) w[i] = 0u;
+  }
+  __device__ __forceinline__ void widen(float (&f)[VE]) const {
+#pragma unroll
+    for (int i = 0; i < VE / 2; ++i) {
+      f[2 * i] = bf_lo(w[i]);
+      f[2 * i + 1] = bf_hi(w[i]);
+    }
+  }
+};
+
+// D: key head dim; DV: value head dim (the lanes of a key row also own the
+// value row, DV / (D / 8) values each).
+template <int D, int DV, int QB, int U, int MINB>
 __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const PartialParams p) {
   constexpr int LPR = D / 8;      // lanes per key row (16 B each)
   constexpr int G = 32 / LPR;     // key rows per warp instruction
   constexpr int STEP = kWarps * G * U;
+  constexpr int VE = DV / LPR;    // values of a value row per lane
+  static_assert(VE == 4 || VE == 8 || VE == 16, "value dims 64 and 128");
 
   __shared__ float sm_m[kWarps][QB];
   __shared__ float sm_l[kWarps][QB];
-  __shared__ __align__(16) float sm_o[kWarps][QB][D];
+  __shared__ __align__(16) float sm_o[kWarps][QB][DV];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, sub = lane % LPR;
@@ -134,29 +178,30 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
     for (int e = 0; e < 8; ++e) qf[qi][e] *= p.sc_log2;
   }
 
-  float m[QB], l[QB], o[QB][8];
+  float m[QB], l[QB], o[QB][VE];
 #pragma unroll
   for (int qi = 0; qi < QB; ++qi) {
     m[qi] = -INFINITY;
     l[qi] = 0.0f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[qi][e] = 0.0f;
+    for (int e = 0; e < VE; ++e) o[qi][e] = 0.0f;
   }
 
   const uint16_t* kbase = p.k + bkv * p.Nk * D + 8 * sub;
-  const uint16_t* vbase = p.v + bkv * p.Nk * D + 8 * sub;
+  const uint16_t* vbase = p.v + bkv * p.Nk * DV + VE * sub;
   for (int64_t base = k_lo; base < k_hi; base += STEP) {
-    uint4 kr[U], vr[U];
+    uint4 kr[U];
+    VSlice<VE> vr[U];
     int64_t key[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       key[u] = base + u * (kWarps * G) + warp * G + grp;
       if (key[u] < k_hi) {
         kr[u] = ld_stream(kbase + key[u] * D);
-        vr[u] = ld_stream(vbase + key[u] * D);
+        vr[u].load(vbase + key[u] * DV);
       } else {
         kr[u] = make_uint4(0u, 0u, 0u, 0u);
-        vr[u] = make_uint4(0u, 0u, 0u, 0u);
+        vr[u].zero();
       }
     }
     float sc[QB][U];
@@ -185,16 +230,16 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
       const float alpha = ex2_approx(m[qi] - m_new);
       l[qi] *= alpha;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[qi][e] *= alpha;
+      for (int e = 0; e < VE; ++e) o[qi][e] *= alpha;
       m[qi] = m_new;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float pu = ex2_approx(sc[qi][u] - m_new);
         l[qi] += pu;
-        float vf[8];
-        unpack8(vr[u], vf);
+        float vf[VE];
+        vr[u].widen(vf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[qi][e] = fmaf(pu, vf[e], o[qi][e]);
+        for (int e = 0; e < VE; ++e) o[qi][e] = fmaf(pu, vf[e], o[qi][e]);
       }
     }
   }
@@ -206,17 +251,17 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
     for (int qi = 0; qi < QB; ++qi) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m[qi], off);
       const float l2 = __shfl_xor_sync(0xffffffffu, l[qi], off);
-      float o2[8];
+      float o2[VE];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[qi][e], off);
-      merge_state(m[qi], l[qi], o[qi], m2, l2, o2);
+      for (int e = 0; e < VE; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[qi][e], off);
+      merge_state<VE>(m[qi], l[qi], o[qi], m2, l2, o2);
     }
   }
   if (grp == 0) {
 #pragma unroll
     for (int qi = 0; qi < QB; ++qi) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) sm_o[warp][qi][8 * sub + e] = o[qi][e];
+      for (int e = 0; e < VE; ++e) sm_o[warp][qi][VE * sub + e] = o[qi][e];
       if (sub == 0) {
         sm_m[warp][qi] = m[qi];
         sm_l[warp][qi] = l[qi];
@@ -226,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
   __syncthreads();
 
   // Merge the warps and write the split's normalised output and LSE.
-  for (int idx = threadIdx.x; idx < QB * D; idx += kThreads) {
-    const int qi = idx / D, e = idx % D;
+  for (int idx = threadIdx.x; idx < QB * DV; idx += kThreads) {
+    const int qi = idx / DV, e = idx % DV;
     if (r0 + qi >= p.R) continue;
     float M = -INFINITY;
 #pragma unroll
@@ -245,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
     // partial slot of (batch * H + query head, split s, position)
     const int64_t bh = qrow[qi] / p.Nq;
     const int64_t slot = (bh * p.S + s) * p.Nq + pos[qi];
-    p.o_part[slot * D + e] = empty ? 0.0f : acc / L;
+    p.o_part[slot * DV + e] = empty ? 0.0f : acc / L;
     if (e == 0) p.lse_part[slot] = empty ? -INFINITY : (M + log2f(L)) * kLn2;
   }
 }
@@ -683,7 +728,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   if (lane == 0) lse[row] = empty ? -INFINITY : M + logf(W);
 }
 
-template <int D, int QB, int U, int MINB>
+template <int D, int DV, int QB, int U, int MINB>
 cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
   PartialParams p;
   p.q = static_cast<const uint16_t*>(a.q);
@@ -704,7 +749,7 @@ cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   const int64_t blocks = (a.BH / p.G) * p.n_qb * a.splits;
-  splitkv_partial_kernel<D, QB, U, MINB>
+  splitkv_partial_kernel<D, DV, QB, U, MINB>
       <<<dim3(static_cast<unsigned>(blocks)), kThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
@@ -747,13 +792,18 @@ cudaError_t launch_partial_bulk(const SplitArgs& a, cudaStream_t stream) {
 cudaError_t launch_splitkv_partial(const SplitArgs& a, cudaStream_t stream) {
   // One row per K/V head: register streaming.  Several rows (GQA groups,
   // Nq > 1): the bulk-copy pipeline, which reads each K/V byte once per CTA.
+  // A value dim different from the key dim: register streaming, one row per
+  // CTA (the caller sized the grid for that).
+  if (a.dv > 0 && a.dv != a.d)
+    return a.d == 64 ? launch_partial<64, 128, 1, 4, 2>(a, stream)
+                     : launch_partial<128, 64, 1, 4, 2>(a, stream);
   const int64_t qb = splitkv_rows_per_cta((a.H / a.Hkv) * a.Nq);
   if (a.d == 64) {
-    if (qb == 1) return launch_partial<64, 1, 4, 2>(a, stream);
+    if (qb == 1) return launch_partial<64, 64, 1, 4, 2>(a, stream);
     if (qb == 4) return launch_partial_bulk<64, 4>(a, stream);
     return launch_partial_bulk<64, 8>(a, stream);
   }
-  if (qb == 1) return launch_partial<128, 1, 4, 2>(a, stream);
+  if (qb == 1) return launch_partial<128, 128, 1, 4, 2>(a, stream);
   if (qb == 4) return launch_partial_bulk<128, 4>(a, stream);
   return launch_partial_bulk<128, 8>(a, stream);
 }

@@ -101,9 +101,9 @@ typedef struct attn_params {
   float q_descale;        /* per-tensor factors of the FP8 Q and K; finite, */
   float k_descale;        /* > 0 (ignored for bf16)                         */
   int64_t dv;             /* head dim of V and O; 0 = d.  dv may differ from d
-                             in attn_fwd_ex (bf16, d and dv in {64, 128});
-                             every other entry point needs dv = d
-                             (ATTN_ERR_UNSUPPORTED otherwise).              */
+                             in attn_fwd_ex and attn_fwd_splitkv_ex (bf16, d
+                             and dv in {64, 128}); every other entry point
+                             needs dv = d (ATTN_ERR_UNSUPPORTED otherwise). */
 } attn_params;
 
 /* attn_params.qk_dtype */
@@ -123,7 +123,9 @@ int attn_fwd_ex(const attn_params* p, cudaStream_t stream);
 /*
  * Bytes of workspace attn_fwd_splitkv needs: float32 partial outputs
  * [B][H][num_splits][Nq][d] followed (at a 256-byte boundary) by float32
- * partial log-sum-exps [B][H][num_splits][Nq].  Returns 0 for invalid sizes.
+ * partial log-sum-exps [B][H][num_splits][Nq].  `d` is the width of the
+ * partials, i.e. the head dim of V and O (dv when attn_fwd_splitkv_ex is
+ * given dv != d).  Returns 0 for invalid sizes.
  */
 size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
                                     int num_splits);
@@ -144,10 +146,12 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      int causal, float scale, int num_splits, void* workspace,
                      size_t workspace_bytes, cudaStream_t stream);
 
-/* attn_fwd_splitkv with query_offset, Hkv, flags, dev_status and
+/* attn_fwd_splitkv with query_offset, Hkv, dv, flags, dev_status and
  * wait_timeout_us from `p` (the latter two apply to the pipelined partial
  * kernel used when several query rows share a K/V head; ATTN_FLAG_TEST_SKIP_LOAD
- * applies to the prefill kernel only). */
+ * applies to the prefill kernel only).  With dv != d every query row gets
+ * its own partial CTAs, so a K/V head shared by several rows is read once
+ * per row; the workspace holds dv-wide partials. */
 int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream);
 

@@ -212,7 +212,15 @@ def test_value_dim_rejects(lib, kw, code):
     assert lib.attn_fwd_ex(ctypes.byref(p), None) == code
 
 
-def test_splitkv_rejects_value_dim(lib):
-    p = _params(d=128, dv=64)
+def test_splitkv_value_dim_workspace(lib):
+    # Split-KV partials are as wide as V: a workspace sized for d is too
+    # small when dv > d, and value dims other than 64 and 128 are refused.
+    small = lib.attn_splitkv_workspace_bytes(1, 1, 8, 64, 4)
+    need = lib.attn_splitkv_workspace_bytes(1, 1, 8, 128, 4)
+    assert need > small > 0
+    p = _params(d=64, dv=128)
+    assert lib.attn_fwd_splitkv_ex(ctypes.byref(p), 4, A16, small, None) == \
+        binding.ATTN_ERR_WORKSPACE
+    p = _params(d=64, dv=96)
     assert lib.attn_fwd_splitkv_ex(ctypes.byref(p), 4, A16, 1 << 30, None) == \
         binding.ATTN_ERR_UNSUPPORTED

@@ -1,6 +1,7 @@
 """GPU parity for a value head dim different from the key head dim (dv != d,
 which the online-softmax derivation allows: V only enters through P V).
-Prefill path, d and dv in {64, 128}; the other entry points reject dv != d."""
+Prefill and split-KV paths, d and dv in {64, 128}; FP8 and the backward
+reject dv != d."""
 import pytest
 import torch
 
@@ -71,9 +72,54 @@ def test_dv_long_prefill_sampled():
     compare(o.reshape(-1, 64)[idx], lse.reshape(-1)[idx], ref_o, ref_l, "dv long sampled")
 
 
-def test_dv_other_entry_points_reject():
+def run_splitkv(q, k, v, causal, scale, splits, query_offset=0):
+    B, H, Nq, _ = q.shape
+    dv = v.shape[3]
+    o, obuf, opad = guarded((B, H, Nq, dv), torch.bfloat16, DEV)
+    lse, lbuf, lpad = guarded((B, H, Nq), torch.float32, DEV)
+    flags = binding.ATTN_FLAG_ALLOW_NEG_OFFSET if query_offset < 0 else 0
+    binding.attn_fwd_splitkv_ex(q, k, v, causal, scale, splits, query_offset=query_offset,
+                                flags=flags, o=o, lse=lse)
+    torch.cuda.synchronize()
+    check_guards(obuf, opad, "O")
+    check_guards(lbuf, lpad, "LSE")
+    return o, lse
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64)])
+@pytest.mark.parametrize("nk", [1, 700, 4099])
+@pytest.mark.parametrize("splits", [1, 3, 16])
+def test_dv_splitkv_decode(d, dv, nk, splits):
+    """One query row per head against nk keys (decode), plain and causal at
+    the last position."""
+    w = W.Workload("dv decode", 2, 4, 1, nk, d, False, 3400 + nk + d + splits, dv=dv)
+    q, k, v = W.make_qkv(w)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    o, lse = run_splitkv(qd, kd, vd, False, w.scale, splits)
+    compare(o, lse, *oracle.attention(q, k, v, causal=False, scale=w.scale),
+            f"split-KV d={d} dv={dv} Nk={nk} S={splits}")
+    o, lse = run_splitkv(qd, kd, vd, True, w.scale, splits, query_offset=nk - 1)
+    compare(o, lse, *oracle.attention(q, k, v, causal=True, scale=w.scale, query_offset=nk - 1),
+            f"split-KV causal d={d} dv={dv} Nk={nk} S={splits}")
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64)])
+def test_dv_splitkv_gqa_rows_and_offsets(d, dv):
+    """Grouped K/V heads and several query positions (chunked decode), with
+    offsets that leave whole splits, and (negative offset) whole rows,
+    without an admissible key."""
+    w = W.Workload("dv split gqa", 2, 8, 5, 1000, d, True, 3500 + d, Hkv=2, dv=dv)
+    q, k, v = W.make_qkv(w)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    for off in (-3, 0, 400, 995):
+        o, lse = run_splitkv(qd, kd, vd, True, w.scale, 6, query_offset=off)
+        compare(o, lse, *oracle.attention(q, k, v, causal=True, scale=w.scale, query_offset=off),
+                f"split-KV d={d} dv={dv} GQA offset={off}")
+
+
+def test_dv_backward_rejects():
     w = W.Workload("dv rej", 1, 2, 64, 64, 128, False, 3300, dv=64)
     q, k, v = (t.to(DEV) for t in W.make_qkv(w))
-    with pytest.raises(binding.AttnError) as e:
-        binding.attn_fwd_splitkv(q, k, v, False, w.scale, 4)
-    assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
+    o, lse = binding.attn_fwd_ex(q, k, v, False, w.scale)
+    with pytest.raises((ValueError, binding.AttnError)):
+        binding.attn_bwd(q, k, v, o, lse, torch.ones_like(q), False, w.scale)
