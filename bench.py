@@ -39,6 +39,11 @@ from attention_attn_fwd_07_gb300 import inputs as W  # noqa: E402
 METRIC = "attention fwd TFLOPS (prefill) / HBM GB/s (decode) at 1 GB300, % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_TXT = os.path.join(ROOT, "profiles", "fwd_tcgen05_long_prefill_causal.md")
+# Query heads per pipelined chunk of the end-to-end call (8: measured fastest
+# of 1, 2, 4, 8, 16; smaller chunks make the host's per-chunk issue cost the
+# bottleneck, larger ones leave more of the last compute and download
+# exposed).
+E2E_CHUNK_HEADS = 8
 KERNEL_SOURCES = ["fwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
 DECODE_PROFILE_TXT = os.path.join(ROOT, "profiles", "splitkv_decode.md")
 DECODE_SOURCES = ["splitkv.cu", "ptx.cuh", "internal.cuh"]
@@ -435,14 +440,14 @@ def main():
 
     def e2e_step():
         binding.fwd_from_host(q_p, k_p, v_p, True, w.scale, q, k, v, o, lse, o_p, lse_p,
-                              stream=stream)
+                              stream=stream, chunk_heads=E2E_CHUNK_HEADS)
 
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(3):
         e2e_step()
     barrier_()
     e2e_ms = max_over_ranks_(event_time(e2e_step, e2e_steps, stream))
-    launches += e2e_steps
+    launches += e2e_steps * w.B * -(-w.H // E2E_CHUNK_HEADS)  # one attn_fwd per chunk
     h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p))
     d2h = o_p.numel() * o_p.element_size() + lse_p.numel() * lse_p.element_size()
     e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS",
