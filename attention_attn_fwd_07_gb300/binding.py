@@ -200,8 +200,8 @@ def attn_fwd_ex(q, k, v, causal: bool, scale: float, query_offset: int = 0, flag
 def attn_fwd_fp8(q8, k8, v, causal: bool, scale: float, q_descale: float, k_descale: float,
                  query_offset: int = 0, o=None, lse=None, stream=None):
     """Prefill with FP8 Q K^T: q8 [B,H,Nq,128], k8 [B,Hkv,Nk,128] e4m3 codes
-    (uint8 or float8_e4m3fn tensors), v bf16; scores are
-    scale * q_descale * k_descale * <q, k>.  Calls attn_fwd_ex."""
+    (uint8 or float8_e4m3fn tensors), v bf16 [B,Hkv,Nk,dv] (dv 64 or 128);
+    scores are scale * q_descale * k_descale * <q, k>.  Calls attn_fwd_ex."""
     for name, t in (("q8", q8), ("k8", k8)):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
@@ -209,17 +209,19 @@ def attn_fwd_fp8(q8, k8, v, causal: bool, scale: float, q_descale: float, k_desc
             raise ValueError(f"{name} must hold e4m3 codes (uint8 or float8_e4m3fn)")
     _require(v, torch.bfloat16, "v")
     B, H, Nq, d = q8.shape
-    if k8.dim() != 4 or tuple(v.shape) != tuple(k8.shape) or k8.shape[0] != B or k8.shape[3] != d:
-        raise ValueError("k8 and v must be [B, Hkv, Nk, d]")
+    if (k8.dim() != 4 or v.dim() != 4 or tuple(v.shape[:3]) != tuple(k8.shape[:3])
+            or k8.shape[0] != B or k8.shape[3] != d):
+        raise ValueError("k8 must be [B, Hkv, Nk, d] and v [B, Hkv, Nk, dv]")
+    dv = v.shape[3]
     if o is None:
-        o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+        o = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=q8.device)
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
     _require(o, torch.bfloat16, "o")
     _require(lse, torch.float32, "lse")
     p = attn_params(_ptr(q8), _ptr(k8), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, k8.shape[2], d,
                     int(bool(causal)), float(scale), int(query_offset), 0, 0, 0,
-                    int(k8.shape[1]), ATTN_QK_E4M3, float(q_descale), float(k_descale))
+                    int(k8.shape[1]), ATTN_QK_E4M3, float(q_descale), float(k_descale), int(dv))
     _check(load_library().attn_fwd_ex(ctypes.byref(p), _stream(stream)), "attn_fwd_ex (fp8)")
     return o, lse
 

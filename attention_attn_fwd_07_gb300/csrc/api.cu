@@ -107,7 +107,7 @@ extern "C" int attn_fwd_ex(const attn_params* p, cudaStream_t stream) {
     if (!std::isfinite(p->q_descale) || !(p->q_descale > 0.0f) ||
         !std::isfinite(p->k_descale) || !(p->k_descale > 0.0f))
       return ATTN_ERR_INVALID;
-    if (p->d != 128 || (p->dv != 0 && p->dv != p->d)) return ATTN_ERR_UNSUPPORTED;
+    if (p->d != 128) return ATTN_ERR_UNSUPPORTED;
   }
   const int64_t dv = p->dv > 0 ? p->dv : p->d;
 

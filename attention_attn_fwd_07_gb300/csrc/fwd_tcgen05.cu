@@ -541,7 +541,9 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream) {
-  if (a.fp8_qk) return launch<128, 128, true>(a, tq, tk, tv, stream);
+  if (a.fp8_qk)
+    return a.dv == 64 ? launch<128, 64, true>(a, tq, tk, tv, stream)
+                      : launch<128, 128, true>(a, tq, tk, tv, stream);
   if (a.d == 64) {
     if (a.dv == 128) return launch<64, 128, false>(a, tq, tk, tv, stream);
     return launch<64, 64, false>(a, tq, tk, tv, stream);

@@ -119,8 +119,8 @@ def make_qkv_fp8(w: Workload, device: str | torch.device = "cpu", Nq: int | None
     Nk = w.Nk if Nk is None else Nk
     g = torch.Generator(device=device).manual_seed(w.seed + 7919)
 
-    def draw(n, heads):
-        return torch.randn((w.B, heads, n, w.d), generator=g, device=device, dtype=torch.float32)
+    def draw(n, heads, width=w.d):
+        return torch.randn((w.B, heads, n, width), generator=g, device=device, dtype=torch.float32)
 
     def quantise(x):
         descale = float(x.abs().max()) / 448.0
@@ -136,5 +136,5 @@ def make_qkv_fp8(w: Workload, device: str | torch.device = "cpu", Nq: int | None
                 rows = torch.randperm(Nk, generator=g, device=device)[:n_boost]
                 k32[b, h, rows] *= 4
     k8, kd = quantise(k32)
-    v = draw(Nk, w.kv_heads).to(torch.bfloat16)
+    v = draw(Nk, w.kv_heads, w.v_dim).to(torch.bfloat16)
     return q8, k8, v, qd, kd

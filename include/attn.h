@@ -101,9 +101,11 @@ typedef struct attn_params {
   float q_descale;        /* per-tensor factors of the FP8 Q and K; finite, */
   float k_descale;        /* > 0 (ignored for bf16)                         */
   int64_t dv;             /* head dim of V and O; 0 = d.  dv may differ from d
-                             in attn_fwd_ex and attn_fwd_splitkv_ex (bf16, d
-                             and dv in {64, 128}); every other entry point
-                             needs dv = d (ATTN_ERR_UNSUPPORTED otherwise). */
+                             in attn_fwd_ex (d and dv in {64, 128}; FP8: d =
+                             128, dv in {64, 128}) and attn_fwd_splitkv_ex
+                             (bf16, d and dv in {64, 128}); every other entry
+                             point needs dv = d (ATTN_ERR_UNSUPPORTED
+                             otherwise).                                    */
 } attn_params;
 
 /* attn_params.qk_dtype */

@@ -205,7 +205,7 @@ def test_bwd_workspace_bytes(lib):
     (dict(dv=-1), binding.ATTN_ERR_INVALID),
     (dict(dv=96), binding.ATTN_ERR_UNSUPPORTED),
     (dict(dv=256), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(d=128, dv=64, qk_dtype=1, q_descale=1.0, k_descale=1.0), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=64, dv=128, qk_dtype=1, q_descale=1.0, k_descale=1.0), binding.ATTN_ERR_UNSUPPORTED),
 ])
 def test_value_dim_rejects(lib, kw, code):
     p = _params(**kw)

@@ -31,7 +31,7 @@ def oracle_inputs(q8, k8, v):
 
 def run_fp8(q8, k8, v, causal, scale, qd, kd, query_offset=0):
     B, H, Nq, d = q8.shape
-    o, obuf, opad = guarded((B, H, Nq, d), torch.bfloat16, DEV)
+    o, obuf, opad = guarded((B, H, Nq, v.shape[3]), torch.bfloat16, DEV)
     lse, lbuf, lpad = guarded((B, H, Nq), torch.float32, DEV)
     binding.attn_fwd_fp8(q8.to(DEV), k8.to(DEV), v.to(DEV), causal, scale, qd, kd,
                          query_offset=query_offset, o=o, lse=lse)
@@ -50,6 +50,19 @@ def test_fp8_prefill(n, hkv, causal):
     qo, ko, vo = oracle_inputs(q8, k8, v)
     ref = oracle.attention(qo, ko, vo, causal=causal, scale=w.scale * qd * kd)
     compare(o, lse, *ref, f"fp8 n={n} Hkv={hkv} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [129, 1003])
+def test_fp8_value_dim_64(n, causal):
+    """FP8 Q K^T (d = 128) with a 64-wide value head."""
+    w = W.Workload("fp8 dv64", 2, 4, n, n, 128, causal, 560 + n, Hkv=2, dv=64)
+    q8, k8, v, qd, kd = W.make_qkv_fp8(w)
+    assert v.shape[3] == 64
+    o, lse = run_fp8(q8, k8, v, causal, w.scale, qd, kd)
+    qo, ko, vo = oracle_inputs(q8, k8, v)
+    ref = oracle.attention(qo, ko, vo, causal=causal, scale=w.scale * qd * kd)
+    compare(o, lse, *ref, f"fp8 dv=64 n={n} causal={causal}")
 
 
 def test_fp8_query_offset():
