@@ -78,8 +78,8 @@ def _declare(lib) -> None:
     lib.oracle_plant.restype = ctypes.c_int
     b = lib.oracle_attention_bwd
     b.restype = ctypes.c_int
-    b.argtypes = [vp, vp, vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, ctypes.c_int, i64,
-                  ctypes.c_double, vp, vp, vp, ctypes.c_int]
+    b.argtypes = [vp, vp, vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                  i64, ctypes.c_double, vp, vp, vp, ctypes.c_int]
 
 
 def _as_array(x):
@@ -162,7 +162,8 @@ def attention(q, k, v, *, causal: bool, scale: float, query_offset: int = 0,
 def attention_bwd(q, k, v, dout, *, causal: bool, scale: float, query_offset: int = 0,
                   threads: int | None = None, lib=None):
     """Dense fp64 gradients (dq, dk, dv) of softmax attention for the loss
-    gradient ``dout`` on O; q, dout [B, H, Nq, d], k, v [B, Hkv, Nk, d]."""
+    gradient ``dout`` on O; q [B, H, Nq, d], k [B, Hkv, Nk, d], v
+    [B, Hkv, Nk, dv], dout [B, H, Nq, dv] (dv may differ from d)."""
     lib = lib or load()
     qa, qe = _as_array(q)
     ka, ke = _as_array(k)
@@ -172,13 +173,15 @@ def attention_bwd(q, k, v, dout, *, causal: bool, scale: float, query_offset: in
         raise ValueError("q, k, v and dout must share one element type")
     B, H, Nq, d = qa.shape
     Bk, Hkv, Nk, dk_ = ka.shape
-    if (Bk, dk_) != (B, d) or va.shape != ka.shape or da.shape != qa.shape or H % Hkv != 0:
+    e = va.shape[3]
+    if ((Bk, dk_) != (B, d) or va.shape[:3] != ka.shape[:3] or da.shape != (B, H, Nq, e)
+            or H % Hkv != 0):
         raise ValueError("incompatible shapes")
     dq = np.empty((B, H, Nq, d), dtype=np.float64)
     dk = np.empty((B, Hkv, Nk, d), dtype=np.float64)
-    dv = np.empty((B, Hkv, Nk, d), dtype=np.float64)
+    dv = np.empty((B, Hkv, Nk, e), dtype=np.float64)
     rc = lib.oracle_attention_bwd(qa.ctypes.data, ka.ctypes.data, va.ctypes.data,
-                                  da.ctypes.data, qe, B, H, Hkv, Nq, Nk, d, int(bool(causal)),
+                                  da.ctypes.data, qe, B, H, Hkv, Nq, Nk, d, e, int(bool(causal)),
                                   int(query_offset), float(scale), dq.ctypes.data,
                                   dk.ctypes.data, dv.ctypes.data,
                                   int(threads or default_threads()))

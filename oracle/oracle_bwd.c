@@ -19,6 +19,10 @@
  * Grouped K/V heads: query head h of batch b uses K/V head b*Hkv + h/(H/Hkv),
  * so dK/dV of a K/V head sum the contributions of its whole group.  Work is
  * split over K/V heads, so no two threads write the same dK/dV row.
+ *
+ * The value width dv may differ from the key width d (V enters only through
+ * O = P V, so the formulas above hold unchanged): V, dO and dV have dv
+ * columns, Q, K, dQ and dK have d.
  */
 #include <math.h>
 #include <pthread.h>
@@ -35,7 +39,7 @@ enum { BWD_F64 = 0, BWD_BF16 = 1 };
 typedef struct {
   const void *q, *k, *v, *dout;
   int elem;
-  int64_t B, H, Hkv, Nq, Nk, d;
+  int64_t B, H, Hkv, Nq, Nk, d, dv_dim;
   int causal;
   int64_t query_offset;
   double scale;
@@ -53,7 +57,7 @@ static double ld(const void *base, int elem, int64_t idx) {
 
 static void *bwd_worker(void *arg) {
   const bwd_job_t *J = (const bwd_job_t *)arg;
-  const int64_t Nk = J->Nk, d = J->d, G = J->H / J->Hkv;
+  const int64_t Nk = J->Nk, d = J->d, e = J->dv_dim, G = J->H / J->Hkv;
   double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
   double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
   double *dp = (double *)malloc(sizeof(double) * (size_t)Nk);
@@ -88,8 +92,8 @@ static void *bwd_worker(void *arg) {
         for (int64_t j = 0; j < Nk; ++j) {
           p[j] /= Z;
           double acc = 0.0;
-          for (int64_t c = 0; c < d; ++c)
-            acc += ld(J->dout, J->elem, qrow * d + c) * ld(J->v, J->elem, (kv_row0 + j) * d + c);
+          for (int64_t c = 0; c < e; ++c)
+            acc += ld(J->dout, J->elem, qrow * e + c) * ld(J->v, J->elem, (kv_row0 + j) * e + c);
           dp[j] = acc;
           corr += p[j] * dp[j];
         }
@@ -108,8 +112,9 @@ static void *bwd_worker(void *arg) {
 #else
             J->dk[(kv_row0 + j) * d + c] += J->scale * ds * qc;
 #endif
-            J->dv[(kv_row0 + j) * d + c] += p[j] * ld(J->dout, J->elem, qrow * d + c);
           }
+          for (int64_t c = 0; c < e; ++c)
+            J->dv[(kv_row0 + j) * e + c] += p[j] * ld(J->dout, J->elem, qrow * e + c);
         }
       }
     }
@@ -119,21 +124,22 @@ static void *bwd_worker(void *arg) {
 }
 
 /*
- * q, dout: [B][H][Nq][d]; k, v: [B][Hkv][Nk][d] (contiguous, same element
- * type).  Writes dq [B][H][Nq][d], dk and dv [B][Hkv][Nk][d] (double).
+ * q: [B][H][Nq][d]; k: [B][Hkv][Nk][d]; v: [B][Hkv][Nk][dv_dim]; dout:
+ * [B][H][Nq][dv_dim] (contiguous, same element type).  Writes dq
+ * [B][H][Nq][d], dk [B][Hkv][Nk][d] and dv [B][Hkv][Nk][dv_dim] (double).
  * Returns 0, -1 on invalid arguments, -2 on allocation failure.
  */
 int oracle_attention_bwd(const void *q, const void *k, const void *v, const void *dout,
                          int elem, int64_t B, int64_t H, int64_t Hkv, int64_t Nq, int64_t Nk,
-                         int64_t d, int causal, int64_t query_offset, double scale, double *dq,
-                         double *dk, double *dv, int n_threads) {
+                         int64_t d, int64_t dv_dim, int causal, int64_t query_offset,
+                         double scale, double *dq, double *dk, double *dv, int n_threads) {
   if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
   if (elem != BWD_F64 && elem != BWD_BF16) return -1;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return -1;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || dv_dim < 1) return -1;
   if (Hkv < 1 || Hkv > H || H % Hkv != 0 || !isfinite(scale)) return -1;
   const int64_t n_kv = B * Hkv;
   memset(dk, 0, sizeof(double) * (size_t)(n_kv * Nk * d));
-  memset(dv, 0, sizeof(double) * (size_t)(n_kv * Nk * d));
+  memset(dv, 0, sizeof(double) * (size_t)(n_kv * Nk * dv_dim));
   if (n_threads < 1) n_threads = 1;
   if (n_threads > 256) n_threads = 256;
   if (n_kv < n_threads) n_threads = (int)n_kv;
@@ -142,8 +148,8 @@ int oracle_attention_bwd(const void *q, const void *k, const void *v, const void
   int started[256] = {0};
   int status = 0;
   for (int t = 0; t < n_threads; ++t) {
-    bwd_job_t J = {q, k, v, dout, elem, B, H, Hkv, Nq, Nk, d, causal, query_offset, scale,
-                   dq, dk, dv, n_kv * t / n_threads, n_kv * (t + 1) / n_threads};
+    bwd_job_t J = {q, k, v, dout, elem, B, H, Hkv, Nq, Nk, d, dv_dim, causal, query_offset,
+                   scale, dq, dk, dv, n_kv * t / n_threads, n_kv * (t + 1) / n_threads};
     jobs[t] = J;
     if (n_threads > 1 && pthread_create(&tids[t], NULL, bwd_worker, &jobs[t]) == 0)
       started[t] = 1;

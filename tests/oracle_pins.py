@@ -341,10 +341,15 @@ def pin_bwd_finite_differences(lib):
     q = rng.normal(size=(1, 4, 6, 4)); k = rng.normal(size=(1, 2, 9, 4))
     v = rng.normal(size=(1, 2, 9, 4))
     cases += [(q, k, v, False, 0), (q, k, v, True, 3)]
+    # value width different from the key width (dv 3 and 7 against d 5)
+    q, k = (rng.normal(size=s)[None, None] for s in ((7, 5), (11, 5)))
+    for e in (3, 7):
+        v = rng.normal(size=(11, e))[None, None]
+        cases += [(q, k, v, True, 1), (q, k, v, False, 0)]
     eps = 1e-5
     for q, k, v, causal, off in cases:
         scale = 0.6
-        g = rng.normal(size=q.shape)
+        g = rng.normal(size=q.shape[:3] + v.shape[3:])
         dq, dk, dv = _bwd(lib, q, k, v, g, causal, scale, off)
 
         def loss(qq, kk, vv):
