@@ -63,7 +63,8 @@ class attn_bwd_params(ctypes.Structure):
                 ("Nq", ctypes.c_int64), ("Nk", ctypes.c_int64), ("d", ctypes.c_int64),
                 ("causal", ctypes.c_int), ("scale", ctypes.c_float),
                 ("query_offset", ctypes.c_int64), ("dev_status", ctypes.c_void_p),
-                ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
+                ("value_dim", ctypes.c_int64)]
 
 
 def load_library(path: str | None = None):
@@ -363,13 +364,12 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, query_offset: in
              flags: int = 0, workspace=None, dq=None, dk=None, dv=None, stream=None):
     """Backward pass: returns (dq, dk, dv) bf16 for the loss gradient dout on o."""
     B, H, Nq, Nk, d = _shape(q, k, v)
-    if tuple(v.shape) != tuple(k.shape):
-        raise ValueError("the backward needs v with the shape of k (dv = d)")
+    dvw = v.shape[3]  # value head dim: V, O, dO and dV
     _require(o, torch.bfloat16, "o")
     _require(dout, torch.bfloat16, "dout")
     _require(lse, torch.float32, "lse")
-    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
-        raise ValueError("o and dout must have the shape of q")
+    if tuple(o.shape) != (B, H, Nq, dvw) or tuple(dout.shape) != (B, H, Nq, dvw):
+        raise ValueError("o and dout must be [B, H, Nq, dv]")
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -380,7 +380,7 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: float, query_offset: in
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
     p = attn_bwd_params(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                         _ptr(dk), _ptr(dv), B, H, k.shape[1], Nq, Nk, d, int(bool(causal)),
-                        float(scale), int(query_offset), 0, int(flags), 0)
+                        float(scale), int(query_offset), 0, int(flags), 0, int(dvw))
     rc = load_library().attn_bwd(ctypes.byref(p), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_bwd")

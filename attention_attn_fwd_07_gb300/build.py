@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
 SOURCES = ["api.cu", "fwd_tcgen05.cu", "splitkv.cu", "noalloc.cu", "bwd_tcgen05.cu",
-           "bwd_tcgen05_d64.cu"]
+           "bwd_tcgen05_d64.cu",
+           "bwd_tcgen05_d64_v128.cu", "bwd_tcgen05_d128_v64.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

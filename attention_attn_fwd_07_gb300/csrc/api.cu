@@ -282,6 +282,9 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
   if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
   if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->value_dim < 0) return ATTN_ERR_INVALID;
+  const int64_t dv = p->value_dim > 0 ? p->value_dim : p->d;
+  if (dv != 64 && dv != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
       p->Nk > kMaxDim)
     return ATTN_ERR_UNSUPPORTED;
@@ -303,9 +306,9 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   if (enc == nullptr) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo;
   if (!encode_map(enc, &tq, p->q, p->Nq, BH, p->d) ||
-      !encode_map(enc, &tdo, p->dout, p->Nq, BH, p->d) ||
+      !encode_map(enc, &tdo, p->dout, p->Nq, BH, dv) ||
       !encode_map(enc, &tk, p->k, p->Nk, BHkv, p->d) ||
-      !encode_map(enc, &tv, p->v, p->Nk, BHkv, p->d))
+      !encode_map(enc, &tv, p->v, p->Nk, BHkv, dv))
     return ATTN_ERR_CUDA;
   BwdArgs a;
   a.o = p->o;
@@ -325,8 +328,13 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   a.causal = p->causal ? 1 : 0;
   a.scale = p->scale;
   a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
-  const cudaError_t err = p->d == 64 ? launch_bwd_d<64>(a, tq, tk, tv, tdo, stream)
-                                     : launch_bwd_d<128>(a, tq, tk, tv, tdo, stream);
+  cudaError_t err;
+  if (p->d == 64)
+    err = dv == 64 ? launch_bwd<64, 64>(a, tq, tk, tv, tdo, stream)
+                   : launch_bwd<64, 128>(a, tq, tk, tv, tdo, stream);
+  else
+    err = dv == 64 ? launch_bwd<128, 64>(a, tq, tk, tv, tdo, stream)
+                   : launch_bwd<128, 128>(a, tq, tk, tv, tdo, stream);
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

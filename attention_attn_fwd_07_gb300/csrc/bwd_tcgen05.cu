@@ -1,4 +1,4 @@
-// bwd_tcgen05.cu -- attention backward (dQ, dK, dV) for sm_103a, d = 128.
+// bwd_tcgen05.cu -- attention backward (dQ, dK, dV) for sm_103a.
 //
 // Gradients of O = softmax(S) V with S = scale * Q K^T [causal], from
 // "GPU Engineering: Correctness, Throughput, and Attention" (sections 22.5
@@ -30,11 +30,16 @@
 // while dP is computed, phase B turns dP into dS while the MMA that needs
 // only P (dV, or the next tile's S) runs.  Every mbarrier wait is bounded; a
 // timeout sets the status word and the CTA leaves cleanly.
-// The head dim d is a compile-time constant of this translation unit:
-// compiled alone it is 128; bwd_tcgen05_d64.cu defines ATTN_BWD_HEAD_DIM as
-// 64 and includes this file.  Each build exports launch_bwd_d<d>.
+// The head dims are compile-time constants of this translation unit: d of
+// Q, K (and dQ, dK) and dv of V, O, dO (and dV).  Compiled alone both are
+// 128; the bwd_tcgen05_d*.cu files define ATTN_BWD_HEAD_DIM and
+// ATTN_BWD_VALUE_DIM and include this file.  Each build exports
+// launch_bwd<d, dv>.
 #ifndef ATTN_BWD_HEAD_DIM
 #define ATTN_BWD_HEAD_DIM 128
+#endif
+#ifndef ATTN_BWD_VALUE_DIM
+#define ATTN_BWD_VALUE_DIM ATTN_BWD_HEAD_DIM
 #endif
 
 #include <algorithm>
@@ -47,8 +52,9 @@
 namespace attn {
 namespace {
 
-constexpr int D = ATTN_BWD_HEAD_DIM;       // head dim of Q, K, V, dO
-static_assert(D == 64 || D == 128, "head dims 64 and 128");
+constexpr int D = ATTN_BWD_HEAD_DIM;       // head dim of Q and K
+constexpr int DV = ATTN_BWD_VALUE_DIM;     // head dim of V, O and dO
+static_assert((D == 64 || D == 128) && (DV == 64 || DV == 128), "head dims 64 and 128");
 constexpr int T = 128;                    // rows per query tile and per key tile
 constexpr int kEwWarps = 8;
 constexpr int kEwThreads = kEwWarps * 32;
@@ -56,11 +62,13 @@ constexpr int kThreads = kEwThreads + 64;
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
-constexpr uint32_t kTileBytes = T * D * 2;    // one [128][d] bf16 tile (d / 64 atoms)
+constexpr uint32_t kQKTileBytes = T * D * 2;  // one [128][d] bf16 tile (d / 64 atoms): Q, K
+constexpr uint32_t kVTileBytes = T * DV * 2;  // one [128][dv] bf16 tile: V, dO
 constexpr int kStagesA = 3;  // ring A (Q tiles in the dK/dV kernel, K tiles in the dQ kernel)
 constexpr int kStagesB = 2;  // ring B (dO tiles, respectively V tiles)
 constexpr uint32_t kIdescSS = idesc_bf16_f32(T, T, 0);  // both operands K-major
-constexpr uint32_t kIdescTS = idesc_bf16_f32(T, D, 1);  // B (N = d) MN-major
+constexpr uint32_t kIdescTS = idesc_bf16_f32(T, D, 1);   // B (N = d) MN-major: dK, dQ
+constexpr uint32_t kIdescTSV = idesc_bf16_f32(T, DV, 1); // B (N = dv) MN-major: dV
 constexpr float kLog2e = 1.4426950408889634074f;
 
 // Shared memory: 2 resident tiles, then ring A (kStagesA tiles: the operand
@@ -70,10 +78,13 @@ constexpr float kLog2e = 1.4426950408889634074f;
 // that reads it is done.  The dynamic shared memory is declared 1024-byte
 // aligned (the 128-byte swizzle needs it) and the kernels check that it is,
 // which leaves no room for an alignment slack: 231,592 of 232,448 bytes.
+// Resident: a d-wide tile (K, respectively Q) then a dv-wide one (V, dO);
+// ring A holds d-wide tiles (Q, respectively K), ring B dv-wide ones (dO, V).
 constexpr uint32_t kOffRes = 0;
-constexpr uint32_t kOffRingA = 2 * kTileBytes;
-constexpr uint32_t kOffRingB = kOffRingA + kStagesA * kTileBytes;
-constexpr uint32_t kOffStat = kOffRingB + kStagesB * kTileBytes;  // 2 x [2][128] floats
+constexpr uint32_t kOffRes2 = kQKTileBytes;
+constexpr uint32_t kOffRingA = kQKTileBytes + kVTileBytes;
+constexpr uint32_t kOffRingB = kOffRingA + kStagesA * kQKTileBytes;
+constexpr uint32_t kOffStat = kOffRingB + kStagesB * kVTileBytes;  // 2 x [2][128] floats
 constexpr uint32_t kOffBar = kOffStat + 2 * 2 * T * 4;
 // barriers: res_full, full_a[3], full_b[2], empty_a[3], empty_b[2], s_full,
 // dp_full, p (dK/dV kernel: P stored; dQ kernel: S read, its columns free),
@@ -88,7 +99,8 @@ constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffMisc + 16;
 static_assert(kSmemBytes <= 232448 && kSmemBytes > 232448 / 2, "one CTA per SM");
 // TMEM columns of the dK/dV kernel's accumulators (after S^T and dP^T).
-constexpr uint32_t kColDV = 256, kColDK = 256 + D;
+constexpr uint32_t kColDV = 256, kColDK = 256 + DV;
+static_assert(kColDK + D <= 512, "tensor memory budget");
 // Status word bit set (and the kernel skipped) if the dynamic shared memory
 // were ever not 1024-byte aligned.
 constexpr int kStatusMisaligned = 2;
@@ -143,26 +155,30 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   return sdesc_sw128(tile + kk * 16 * 128, kAtomBytes, 1024);
 }
 
-// D = A B^T over the d columns of two K-major [128][d] tiles: d / 16 MMAs
+// D = A B^T over the W columns of two K-major [128][W] tiles: W / 16 MMAs
 // from one elect.sync.
+template <int W>
 __device__ __forceinline__ void mma_ss_tiles_w(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
-  if constexpr (D == 128)
+  static_assert(W == 64 || W == 128, "tile widths 64 and 128");
+  if constexpr (W == 128)
     mma_ss_run8_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
   else
     mma_ss_run4_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
 }
 // D (+)= A B over 128 K rows: A is a packed bf16 operand in tensor memory
-// (by column half, as above), B an MN-major [128][d] tile; eight MMAs from
-// one elect.sync.
+// (by column half, as above), B an MN-major [128][N] tile (N = d or dv, as
+// `idesc` says); eight MMAs from one elect.sync.
 __device__ __forceinline__ void mma_ts_tile_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_tile,
-                                              bool accumulate) {
+                                              uint32_t idesc, bool accumulate) {
   static_assert(T == 128, "eight K steps of 16");
-  mma_ts_run8_halves_w(d_tmem, a_tmem, desc_mnmajor(b_tile, 0), kIdescTS, accumulate ? 1u : 0u);
+  mma_ts_run8_halves_w(d_tmem, a_tmem, desc_mnmajor(b_tile, 0), idesc, accumulate ? 1u : 0u);
 }
 
+// One [128][W] bf16 tile (W / 64 swizzle atoms).
+template <int W>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                           int row, int64_t z) {
-  for (int a = 0; a < D / 64; ++a)
+  for (int a = 0; a < W / 64; ++a)
     tma_load_3d(dst + a * kAtomBytes, map, bar, a * 64, row, static_cast<int>(z));
 }
 
@@ -268,14 +284,14 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
   if (row >= rows) return;
   auto lo = [](uint32_t w) { return __uint_as_float(w << 16); };
   auto hi = [](uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); };
-  float acc;
-  if constexpr (D == 128) {  // four elements per lane
-    const uint2 a = *reinterpret_cast<const uint2*>(o + row * D + 4 * lane);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + row * D + 4 * lane);
+  float acc;  // O and dO rows are dv wide
+  if constexpr (DV == 128) {  // four elements per lane
+    const uint2 a = *reinterpret_cast<const uint2*>(o + row * DV + 4 * lane);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + row * DV + 4 * lane);
     acc = lo(a.x) * lo(b.x) + hi(a.x) * hi(b.x) + lo(a.y) * lo(b.y) + hi(a.y) * hi(b.y);
   } else {  // two elements per lane
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + row * D + 2 * lane);
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + row * D + 2 * lane);
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + row * DV + 2 * lane);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + row * DV + 2 * lane);
     acc = lo(a) * lo(b) + hi(a) * hi(b);
   }
 #pragma unroll
@@ -297,13 +313,13 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, con
     if (n >= kStagesA &&
         !wait(c.bar(kBarEmptyA + sa), static_cast<uint32_t>(((n / kStagesA) - 1) & 1)))
       break;
-    mbar_arrive_expect_tx(c.bar(kBarFullA + sa), kTileBytes);
+    mbar_arrive_expect_tx(c.bar(kBarFullA + sa), kQKTileBytes);
     load_a(n, c.bar(kBarFullA + sa));
     last_a = n;
     if (n >= kStagesB &&
         !wait(c.bar(kBarEmptyB + sb), static_cast<uint32_t>(((n / kStagesB) - 1) & 1)))
       break;
-    mbar_arrive_expect_tx(c.bar(kBarFullB + sb), kTileBytes);
+    mbar_arrive_expect_tx(c.bar(kBarFullB + sb), kVTileBytes);
     load_b(n, c.bar(kBarFullB + sb));
     last_b = n;
   }
@@ -360,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     q0 = (qt_first + n % per_head) * T;
   };
 
-  const uint32_t sK = c.sbase + kOffRes, sV = sK + kTileBytes;
-  auto sQ = [&](int64_t n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kTileBytes; };
-  auto sdO = [&](int64_t n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kTileBytes; };
+  const uint32_t sK = c.sbase + kOffRes, sV = c.sbase + kOffRes2;
+  auto sQ = [&](int64_t n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kQKTileBytes; };
+  auto sdO = [&](int64_t n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kVTileBytes; };
   auto slot_a = [](int64_t n) { return static_cast<int>(n % kStagesA); };
   auto slot_b = [](int64_t n) { return static_cast<int>(n % kStagesB); };
   auto par_a = [](int64_t n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
@@ -372,20 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
-      load_tile(sK, &tk, c.bar(kBarRes), static_cast<int>(k0), bkv);
-      load_tile(sV, &tv, c.bar(kBarRes), static_cast<int>(k0), bkv);
+      mbar_arrive_expect_tx(c.bar(kBarRes), kQKTileBytes + kVTileBytes);
+      load_tile<D>(sK, &tk, c.bar(kBarRes), static_cast<int>(k0), bkv);
+      load_tile<DV>(sV, &tv, c.bar(kBarRes), static_cast<int>(k0), bkv);
       run_loader(
           c, wait, p, n_items,
           [&](int64_t n, uint32_t bar) {
             int64_t bh, q0;
             item_rows(n, bh, q0);
-            load_tile(sQ(n), &tq, bar, static_cast<int>(q0), bh);
+            load_tile<D>(sQ(n), &tq, bar, static_cast<int>(q0), bh);
           },
           [&](int64_t n, uint32_t bar) {
             int64_t bh, q0;
             item_rows(n, bh, q0);
-            load_tile(sdO(n), &tdo, bar, static_cast<int>(q0), bh);
+            load_tile<DV>(sdO(n), &tdo, bar, static_cast<int>(q0), bh);
           });
     }
   } else if (warp == kWarpMma) {
@@ -400,11 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (n_items > 0) {
       auto issue_s = [&](int64_t n) {  // S^T = K Q^T
-        mma_ss_tiles_w(tS, sK, sQ(n));
+        mma_ss_tiles_w<D>(tS, sK, sQ(n));
         mma_commit_w(c.bar(kBarS));
       };
       auto issue_dp = [&](int64_t n) {  // dP^T = V dO^T
-        mma_ss_tiles_w(tdP, sV, sdO(n));
+        mma_ss_tiles_w<DV>(tdP, sV, sdO(n));
         mma_commit_w(c.bar(kBarDP));
       };
       bool ok = wait_w(c.bar(kBarRes), 0) && wait_w(c.bar(kBarFullA), 0);
@@ -421,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_w(c.bar(kBarP), n & 1);
         if (!ok) break;
         tc_fence_after();
-        mma_ts_tile_w(tdV, tS, sdO(n), n > 0);
+        mma_ts_tile_w(tdV, tS, sdO(n), kIdescTSV, n > 0);
         mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
         const bool more = n + 1 < n_items;
         if (more) {
@@ -433,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_w(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
-        mma_ts_tile_w(tdK, tdP, sQ(n), n > 0);
+        mma_ts_tile_w(tdK, tdP, sQ(n), kIdescTS, n > 0);
         mma_commit_w(c.bar(kBarEmptyA + slot_a(n)));
         if (more) {
           ok = wait_w(c.bar(kBarFullB + slot_b(n + 1)), par_b(n + 1));
@@ -554,20 +570,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
-      // Each thread stores half of its row's d columns.
+      // Each thread stores half of its row's d columns of dK and half of its
+      // dv columns of dV.
       const int64_t kv_row = bkv * p.Nk + j;
 #pragma unroll 1
       for (int cc = 0; cc < D / 64; ++cc) {
         const uint32_t col = static_cast<uint32_t>((D / 2) * half + 32 * cc);
-        uint32_t kd[32] = {}, vd[32] = {};
-        if (n_items > 0) {
-          tmem_ld_x32(tdK + lane_off + col, kd);
-          tmem_ld_x32(tdV + lane_off + col, vd);
-        }
-        if (row_live) {
-          store_row_bf16(p.dk + kv_row * D + col, kd, p.scale, n_items == 0);
-          store_row_bf16(p.dv + kv_row * D + col, vd, 1.0f, n_items == 0);
-        }
+        uint32_t kd[32] = {};
+        if (n_items > 0) tmem_ld_x32(tdK + lane_off + col, kd);
+        if (row_live) store_row_bf16(p.dk + kv_row * D + col, kd, p.scale, n_items == 0);
+      }
+#pragma unroll 1
+      for (int cc = 0; cc < DV / 64; ++cc) {
+        const uint32_t col = static_cast<uint32_t>((DV / 2) * half + 32 * cc);
+        uint32_t vd[32] = {};
+        if (n_items > 0) tmem_ld_x32(tdV + lane_off + col, vd);
+        if (row_live) store_row_bf16(p.dv + kv_row * DV + col, vd, 1.0f, n_items == 0);
       }
     }
   }
@@ -609,9 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_kt = last_key < 0 ? 0 : static_cast<int>(min(static_cast<int64_t>(n_kt), last_key / T + 1));
   }
 
-  const uint32_t sQ = c.sbase + kOffRes, sdO = sQ + kTileBytes;
-  auto sK = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kTileBytes; };
-  auto sV = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kTileBytes; };
+  const uint32_t sQ = c.sbase + kOffRes, sdO = c.sbase + kOffRes2;
+  auto sK = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kQKTileBytes; };
+  auto sV = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kVTileBytes; };
   auto slot_a = [](int n) { return n % kStagesA; };
   auto slot_b = [](int n) { return n % kStagesB; };
   auto par_a = [](int n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
@@ -620,16 +638,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpLoad) {
     if (lane == 0 && n_kt > 0) {
-      mbar_arrive_expect_tx(c.bar(kBarRes), 2 * kTileBytes);
-      load_tile(sQ, &tq, c.bar(kBarRes), static_cast<int>(q0), bh);
-      load_tile(sdO, &tdo, c.bar(kBarRes), static_cast<int>(q0), bh);
+      mbar_arrive_expect_tx(c.bar(kBarRes), kQKTileBytes + kVTileBytes);
+      load_tile<D>(sQ, &tq, c.bar(kBarRes), static_cast<int>(q0), bh);
+      load_tile<DV>(sdO, &tdo, c.bar(kBarRes), static_cast<int>(q0), bh);
       run_loader(
           c, wait, p, n_kt,
           [&](int64_t n, uint32_t bar) {
-            load_tile(sK(static_cast<int>(n)), &tk, bar, static_cast<int>(n) * T, bkv);
+            load_tile<D>(sK(static_cast<int>(n)), &tk, bar, static_cast<int>(n) * T, bkv);
           },
           [&](int64_t n, uint32_t bar) {
-            load_tile(sV(static_cast<int>(n)), &tv, bar, static_cast<int>(n) * T, bkv);
+            load_tile<DV>(sV(static_cast<int>(n)), &tv, bar, static_cast<int>(n) * T, bkv);
           });
     }
   } else if (warp == kWarpMma) {
@@ -643,11 +661,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (n_kt > 0) {
       auto issue_s = [&](int n) {  // S = Q K^T
-        mma_ss_tiles_w(tS, sQ, sK(n));
+        mma_ss_tiles_w<D>(tS, sQ, sK(n));
         mma_commit_w(c.bar(kBarS));
       };
       auto issue_dp = [&](int n) {  // dP = dO V^T
-        mma_ss_tiles_w(tdP, sdO, sV(n));
+        mma_ss_tiles_w<DV>(tdP, sdO, sV(n));
         mma_commit_w(c.bar(kBarDP));
         mma_commit_w(c.bar(kBarEmptyB + slot_b(n)));
       };
@@ -673,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_w(c.bar(kBarDS), n & 1);
         if (!ok) break;
         tc_fence_after();
-        mma_ts_tile_w(tdQ, tdP, sK(n), n > 0);
+        mma_ts_tile_w(tdQ, tdP, sK(n), kIdescTS, n > 0);
         mma_commit_w(c.bar(kBarEmptyA + slot_a(n)));
         if (more) {
           ok = wait_w(c.bar(kBarFullB + slot_b(n + 1)), par_b(n + 1));
@@ -788,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 template <>
-cudaError_t launch_bwd_d<D>(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_bwd<D, DV>(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream) {
   BwdParams p;
   p.o = static_cast<const __nv_bfloat16*>(a.o);
@@ -813,8 +831,8 @@ cudaError_t launch_bwd_d<D>(const BwdArgs& a, const CUtensorMap& tq, const CUten
   // its query heads for the dK/dV kernel, K and V for the dQ kernel) take
   // about 48 MB of L2.
   const int64_t G = a.H / a.Hkv;
-  const double q_head_bytes = 2.0 * static_cast<double>(a.Nq) * D * 2.0;
-  const double kv_head_bytes = 2.0 * static_cast<double>(a.Nk) * D * 2.0;
+  const double q_head_bytes = static_cast<double>(a.Nq) * (D + DV) * 2.0;
+  const double kv_head_bytes = static_cast<double>(a.Nk) * (D + DV) * 2.0;
   p.kv_per_group = std::min<int64_t>(
       a.B * a.Hkv, std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / (q_head_bytes * G))));
   p.q_per_group = std::min<int64_t>(

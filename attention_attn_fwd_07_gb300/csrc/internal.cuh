@@ -51,12 +51,12 @@ inline int64_t splitkv_rows_per_cta(int64_t rows_per_kv_head) {
   return rows_per_kv_head == 1 ? 1 : (rows_per_kv_head <= 4 ? 4 : 8);
 }
 
-// Arguments of one backward pass (d = 128), already validated.
+// Arguments of one backward pass, already validated.
 struct BwdArgs {
-  const void *o, *dout;  // bf16 [B][H][Nq][d]
+  const void *o, *dout;  // bf16 [B][H][Nq][dv]
   const float* lse;      // f32 [B][H][Nq] from the forward pass
   float* delta;          // workspace f32 [B][H][Nq]: rowsum(dO * O)
-  void *dq, *dk, *dv;    // bf16 outputs, [B][H][Nq][d] and [B][Hkv][Nk][d]
+  void *dq, *dk, *dv;    // bf16 outputs, [B][H][Nq][d], [B][Hkv][Nk][d], [B][Hkv][Nk][dv]
   int* status;
   int64_t B, H, Hkv, Nq, Nk, query_offset;
   int causal;
@@ -64,16 +64,21 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
-// Backward launches for head dim D (bwd_tcgen05.cu: 128, bwd_tcgen05_d64.cu: 64).
-template <int D>
-cudaError_t launch_bwd_d(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
-template <>
-cudaError_t launch_bwd_d<64>(const BwdArgs&, const CUtensorMap&, const CUtensorMap&,
-                             const CUtensorMap&, const CUtensorMap&, cudaStream_t);
-template <>
-cudaError_t launch_bwd_d<128>(const BwdArgs&, const CUtensorMap&, const CUtensorMap&,
-                              const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+// Backward launches for key head dim D and value head dim DV, one
+// translation unit each (bwd_tcgen05.cu: 128/128, bwd_tcgen05_d64.cu: 64/64,
+// bwd_tcgen05_d64_v128.cu, bwd_tcgen05_d128_v64.cu).
+template <int D, int DV>
+cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
+#define ATTN_DECLARE_BWD(D_, DV_)                                                        \
+  template <>                                                                            \
+  cudaError_t launch_bwd<D_, DV_>(const BwdArgs&, const CUtensorMap&, const CUtensorMap&, \
+                                  const CUtensorMap&, const CUtensorMap&, cudaStream_t);
+ATTN_DECLARE_BWD(64, 64)
+ATTN_DECLARE_BWD(128, 128)
+ATTN_DECLARE_BWD(64, 128)
+ATTN_DECLARE_BWD(128, 64)
+#undef ATTN_DECLARE_BWD
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream);

@@ -98,13 +98,14 @@ def make_qkv(w: Workload, device: str | torch.device = "cpu", Nq: int | None = N
 
 
 def make_dout(w: Workload, device: str | torch.device = "cpu", Nq: int | None = None):
-    """Loss gradient on O for the backward pass: dO [B, H, Nq, d] bfloat16,
-    standard normal entries from its own seed (the workload's seed + 104729)."""
+    """Loss gradient on O for the backward pass: dO [B, H, Nq, dv] bfloat16
+    (dv = the value head dim), standard normal entries from its own seed (the
+    workload's seed + 104729)."""
     Nq = w.Nq if Nq is None else Nq
     g = torch.Generator(device=device).manual_seed(w.seed + 104729)
-    out = torch.empty((w.B, w.H, Nq, w.d), dtype=torch.bfloat16, device=device)
+    out = torch.empty((w.B, w.H, Nq, w.v_dim), dtype=torch.bfloat16, device=device)
     for b in range(w.B):
-        out[b] = torch.randn((w.H, Nq, w.d), generator=g, device=device,
+        out[b] = torch.randn((w.H, Nq, w.v_dim), generator=g, device=device,
                              dtype=torch.float32).to(torch.bfloat16)
     return out
 

@@ -174,13 +174,13 @@ int attn_combine(const float* o_part, const float* lse_part, void* o, float* lse
 typedef struct attn_bwd_params {
   const void* q;          /* bf16 [B][H][Nq][d], the forward's inputs         */
   const void* k;          /* bf16 [B][Hkv][Nk][d]                             */
-  const void* v;          /* bf16 [B][Hkv][Nk][d]                             */
-  const void* o;          /* bf16 [B][H][Nq][d], the forward's output         */
-  const void* dout;       /* bf16 [B][H][Nq][d], loss gradient on O           */
+  const void* v;          /* bf16 [B][Hkv][Nk][dv]                            */
+  const void* o;          /* bf16 [B][H][Nq][dv], the forward's output        */
+  const void* dout;       /* bf16 [B][H][Nq][dv], loss gradient on O          */
   const float* lse;       /* f32  [B][H][Nq], the forward's log-sum-exp       */
   void* dq;               /* bf16 [B][H][Nq][d], written                      */
   void* dk;               /* bf16 [B][Hkv][Nk][d], written                    */
-  void* dv;               /* bf16 [B][Hkv][Nk][d], written                    */
+  void* dv;               /* bf16 [B][Hkv][Nk][dv], written                   */
   int64_t B, H, Hkv, Nq, Nk, d;  /* Hkv = 0 means H; d is 64 or 128          */
   int causal;
   float scale;
@@ -190,6 +190,8 @@ typedef struct attn_bwd_params {
                              not 1024-byte aligned                          */
   uint32_t flags;         /* ATTN_FLAG_ALLOW_NEG_OFFSET only                  */
   uint32_t wait_timeout_us;
+  int64_t value_dim;      /* dv, the head dim of V, O, dO and dV: 64 or 128;
+                             0 = d                                          */
 } attn_bwd_params;
 
 /* Bytes of workspace attn_bwd needs: f32 [B][H][Nq] (the row corrections
@@ -205,7 +207,8 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq);
  * row can see get zero dK and dV.  Grouped K/V heads sum their group's
  * contributions.  Three launches on `stream` (row corrections, a dK/dV kernel
  * per 128-key tile, a dQ kernel per 128-query tile); no atomics, so the
- * result is deterministic.  d in {64, 128} (ATTN_ERR_UNSUPPORTED otherwise).
+ * result is deterministic.  d and dv in {64, 128} (ATTN_ERR_UNSUPPORTED
+ * otherwise; dv may differ from d).
  * `workspace` (device, 16-byte aligned, caller-owned) must hold
  * attn_bwd_workspace_bytes(B, H, Nq) bytes.
  */

@@ -169,7 +169,7 @@ def test_missing_library_fails_loudly(tmp_path):
 def _bwd_params(**kw):
     base = dict(q=A16, k=A16, v=A16, o=A16, dout=A16, lse=A16, dq=A16, dk=A16, dv=A16, B=1, H=2,
                 Hkv=0, Nq=8, Nk=8, d=128, causal=1, scale=0.125, query_offset=0,
-                dev_status=None, flags=0, wait_timeout_us=0)
+                dev_status=None, flags=0, wait_timeout_us=0, value_dim=0)
     base.update(kw)
     return binding.attn_bwd_params(**base)
 
@@ -184,6 +184,9 @@ def _bwd_params(**kw):
     (dict(Hkv=4), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(query_offset=-1), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(d=96), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(value_dim=-1), 1 << 20, binding.ATTN_ERR_INVALID),
+    (dict(value_dim=96), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(value_dim=256), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
     (dict(Nq=1 << 31), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
     (dict(dq=MIS), 1 << 20, binding.ATTN_ERR_ALIGN),
     (dict(lse=A16 + 2), 1 << 20, binding.ATTN_ERR_ALIGN),

@@ -4,7 +4,8 @@ The CUDA side runs the product path a user runs: the prefill kernel's O and
 LSE, then attn_bwd.  The oracle recomputes everything from q, k, v and dO in
 fp64 (its row correction from the definition rowsum(P * dP), not from O).
 Cases span several 128-row tiles with ragged tails, causal and not, grouped
-K/V heads, decode-style and negative query offsets (rows with no admissible
+K/V heads, value head dims different from the key head dim, decode-style
+and negative query offsets (rows with no admissible
 key, keys no row sees), and the long causal prefill at full size (dQ on
 sampled row blocks; dK and dV through identities that hold at any size).
 """
@@ -63,8 +64,8 @@ def masks(B, H, Hkv, Nq, Nk, causal, off):
     return zq, zk
 
 
-def check_case(B, H, Hkv, Nq, Nk, causal, off, seed, what, d=128):
-    w = W.Workload(what, B, H, Nq, Nk, d, causal, seed, Hkv=Hkv)
+def check_case(B, H, Hkv, Nq, Nk, causal, off, seed, what, d=128, dv=0):
+    w = W.Workload(what, B, H, Nq, Nk, d, causal, seed, Hkv=Hkv, dv=dv)
     q, k, v = W.make_qkv(w)
     dout = W.make_dout(w)
     dq, dk, dv = run_bwd(*(t.to(DEV) for t in (q, k, v, dout)), causal, w.scale, off)
@@ -103,6 +104,21 @@ def test_bwd_offsets(off, d):
     # off < 0: the first -off rows see no key (dQ = 0) and the last keys no
     # row (dK = dV = 0); off >= Nk - Nq: every key visible to every row.
     check_case(1, 2, 2, 300, 300, True, off, 2300 + off + d, f"bwd causal off={off} d={d}", d=d)
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 129, 333])
+def test_bwd_value_dim(n, causal, d, dv):
+    """Value head dim different from the key head dim."""
+    check_case(2, 3, 3, n, n, causal, 0, 8100 + n + d, f"bwd d={d} dv={dv} N={n}", d=d, dv=dv)
+
+
+@pytest.mark.parametrize("d,dv", [(64, 128), (128, 64)])
+def test_bwd_value_dim_gqa_offsets(d, dv):
+    for off in (-40, 0, 300):
+        check_case(1, 4, 2, 200, 500, True, off, 8200 + d, f"bwd d={d} dv={dv} off={off}",
+                   d=d, dv=dv)
 
 
 def test_bwd_rejects_d96():
