@@ -45,10 +45,12 @@ struct SplitArgs {
 // Query rows per CTA of the prefill kernel (two 128-row tiles).
 constexpr int kFwdRowsPerCta = 256;
 
-// Query rows one split-KV partial CTA serves, out of the rows that share one
-// K/V head (query heads of the group x query positions).
+// Query rows one split-KV partial work item serves, out of the rows that
+// share one K/V head (query heads of the group x query positions): one, or
+// blocks of four (the pipelined kernel's reduce-scatter layout; larger
+// groups take several blocks, which read the same K/V slice back to back).
 inline int64_t splitkv_rows_per_cta(int64_t rows_per_kv_head) {
-  return rows_per_kv_head == 1 ? 1 : (rows_per_kv_head <= 4 ? 4 : 8);
+  return rows_per_kv_head == 1 ? 1 : 4;
 }
 
 // Arguments of one backward pass, already validated.

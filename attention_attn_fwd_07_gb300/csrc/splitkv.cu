@@ -17,15 +17,19 @@
 //
 // Pipelined variant (several query rows per K/V head: GQA groups or Nq > 1):
 // a producer warp streams the split's contiguous K and V slices into a
-// 4-stage shared-memory ring with 1-D bulk copies (64 keys per stage), so
-// the bytes in flight do not depend on registers; eight consumer warps run
-// the same online-softmax arithmetic from shared memory.  Its waits are
-// bounded like the prefill kernel's (timeout -> status word, clean exit).
+// 4-stage shared-memory ring with 1-D bulk copies, so the bytes in flight do
+// not depend on registers; the consumer warps run the same online-softmax
+// arithmetic from shared memory.  It is persistent: one CTA per SM walks
+// the (K/V head, row block, split) items, and the ring runs on from one
+// item to the next, so no CTA start or pipeline refill separates them.  Its
+// waits are bounded like the prefill kernel's (timeout -> status word,
+// clean exit).
 //
 // Combine kernel: one warp per (batch*head, query row) merges the splits:
 // M = max lse_s, w_s = exp(lse_s - M), O = sum w_s o_s / sum w_s (-> bf16),
 // LSE = M + ln sum w_s; M = -inf gives O = +0.0, LSE = -inf (the section 22.7
 // lab's policy for a row with no admissible key).
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "internal.cuh"
@@ -48,6 +52,7 @@ struct PartialParams {
   int64_t Nq, Nk, qoff, L;
   int64_t H, Hkv, G, R;  // query heads, K/V heads, group size, rows per K/V head
   int S, n_qb, causal;
+  int64_t n_items;  // pipelined kernel: (K/V head, row block, split) work items
   float sc_log2;
   int* status;
   uint64_t timeout_ns;
@@ -141,10 +146,12 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, sub = lane % LPR;
   const int64_t lin = blockIdx.x;
-  const int s = static_cast<int>(lin % p.S);
-  const int64_t rest = lin / p.S;
-  const int qb = static_cast<int>(rest % p.n_qb);
-  const int64_t bkv = rest / p.n_qb;  // batch * Hkv + K/V head
+  // lin = (bkv * S + s) * n_qb + qb: the row blocks of one K/V slice are
+  // neighbours, so they run together and read the slice once from memory.
+  const int qb = static_cast<int>(lin % p.n_qb);
+  const int64_t rest = lin / p.n_qb;
+  const int s = static_cast<int>(rest % p.S);
+  const int64_t bkv = rest / p.S;  // batch * Hkv + K/V head
   const int64_t r0 = static_cast<int64_t>(qb) * QB;
   // Row r of this K/V head: query head (group member r / Nq), position r % Nq.
   int64_t qrow[QB], pos[QB];
@@ -295,10 +302,29 @@ __global__ void __launch_bounds__(kThreads, MINB) splitkv_partial_kernel(const P
   }
 }
 
-// Consumer warps: twelve for four rows per K/V head (146 registers; more
-// warps hide the latency of the per-stage shuffle / exponential chain),
-// eight for eight rows (their 168 registers leave no room for more).
-__host__ __device__ constexpr int bulk_warps(int QB) { return QB == 4 ? 12 : 8; }
+// Barrier 1 among the first `nthreads` threads (the consumer warps; the
+// producer warp, numbered after them, never takes part).
+__device__ __forceinline__ void consumers_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+// Same barrier, returning the OR of `pred` over the participants (so every
+// consumer takes the same branch after it).
+__device__ __forceinline__ bool consumers_sync_or(bool pred, int nthreads) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Consumer warps: twelve for a block of four rows (more warps hide the
+// latency of the per-stage shuffle / exponential chain).
+__host__ __device__ constexpr int bulk_warps(int QB) { return QB == 4 ? 12 : 0; }
 __host__ __device__ constexpr int bulk_threads(int QB) { return (bulk_warps(QB) + 1) * 32; }  // + one producer warp
 constexpr int kKeysPerWarp = 8;                       // keys per consumer warp per stage
 __host__ __device__ constexpr int bulk_chunk(int QB) { return bulk_warps(QB) * kKeysPerWarp; }  // keys per stage
@@ -313,13 +339,13 @@ template <int D, int QB>
 __global__ void __launch_bounds__(bulk_threads(QB), 1)
     splitkv_partial_bulk_kernel(const PartialParams p) {
   constexpr int kBulkWarps = bulk_warps(QB);
-  constexpr int kBulkThreads = bulk_threads(QB);
+  constexpr int kConsumerThreads = kBulkWarps * 32;
   constexpr int kChunk = bulk_chunk(QB);
   constexpr int LPR = D / 8;            // lanes per key row (16 B each)
   constexpr int G = 32 / LPR;           // key rows per warp instruction
   constexpr int KPW = kChunk / kBulkWarps;  // keys per warp per stage
   constexpr int U = KPW / G;            // key rows per lane group per stage
-  constexpr int UB = (QB >= 8 && U > 1) ? 1 : U;  // rows per online-softmax step
+  constexpr int UB = U;  // key rows per online-softmax step
   constexpr uint32_t kChunkBytes = kChunk * D * 2;
   static_assert(U >= 1 && KPW % G == 0, "stage split");
 
@@ -336,35 +362,41 @@ __global__ void __launch_bounds__(bulk_threads(QB), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane / LPR, sub = lane % LPR;
-  const int64_t lin = blockIdx.x;
-  const int s = static_cast<int>(lin % p.S);
-  const int64_t rest = lin / p.S;
-  const int qb = static_cast<int>(rest % p.n_qb);
-  const int64_t bkv = rest / p.n_qb;
-  const int64_t r0 = static_cast<int64_t>(qb) * QB;
-  // Row qi of this CTA: query row index (batch*H + head)*Nq + position.
+  // Work item lin = (K/V head bkv, block qb of QB rows, split s); this CTA
+  // takes items blockIdx.x, blockIdx.x + gridDim.x, ...  The producer's ring
+  // position and the consumers' run on across items, so the next item's
+  // K/V stream in while the consumers finish the current one.
+  int s = 0;
+  int64_t bkv = 0, r0 = 0, k_lo = 0, k_hi = 0;
+  int n_chunks = 0;
+  int lim_rel[QB];  // last admissible key of each row, relative to k_lo (clamped)
+  // Row qi of the current item: query row index (batch*H + head)*Nq + position.
   auto row_of = [&](int qi, int64_t& position) -> int64_t {
     const int64_t r = min(r0 + qi, p.R - 1);
     position = r % p.Nq;
     const int64_t h = (bkv % p.Hkv) * p.G + r / p.Nq;
     return ((bkv / p.Hkv) * p.H + h) * p.Nq + position;
   };
-  const int64_t k_lo = static_cast<int64_t>(s) * p.L;
-  int64_t k_hi = min(k_lo + p.L, p.Nk);
-  // Last admissible key of each row, relative to k_lo (clamped to int).
-  int lim_rel[QB];
-  int64_t top = -1;
+  auto set_item = [&](int64_t lin) {
+    r0 = (lin % p.n_qb) * QB;  // same item order as the register-streaming kernel
+    const int64_t rest = lin / p.n_qb;
+    s = static_cast<int>(rest % p.S);
+    bkv = rest / p.S;
+    k_lo = static_cast<int64_t>(s) * p.L;
+    k_hi = min(k_lo + p.L, p.Nk);
+    int64_t top = -1;
 #pragma unroll
-  for (int qi = 0; qi < QB; ++qi) {
-    int64_t position;
-    row_of(qi, position);
-    const int64_t lim = p.causal ? min(p.Nk - 1, position + p.qoff) : p.Nk - 1;
-    top = max(top, lim);
-    const int64_t rel = lim - k_lo;
-    lim_rel[qi] = static_cast<int>(rel < -1 ? -1 : (rel > (1 << 30) ? (1 << 30) : rel));
-  }
-  k_hi = min(k_hi, top + 1);
-  const int n_chunks = k_hi > k_lo ? static_cast<int>((k_hi - k_lo + kChunk - 1) / kChunk) : 0;
+    for (int qi = 0; qi < QB; ++qi) {
+      int64_t position;
+      row_of(qi, position);
+      const int64_t lim = p.causal ? min(p.Nk - 1, position + p.qoff) : p.Nk - 1;
+      top = max(top, lim);
+      const int64_t rel = lim - k_lo;
+      lim_rel[qi] = static_cast<int>(rel < -1 ? -1 : (rel > (1 << 30) ? (1 << 30) : rel));
+    }
+    k_hi = min(k_hi, top + 1);
+    n_chunks = k_hi > k_lo ? static_cast<int>((k_hi - k_lo + kChunk - 1) / kChunk) : 0;
+  };
 
   if (threadIdx.x == 0) {
     for (int st = 0; st < kBulkStages; ++st) {
@@ -396,28 +428,41 @@ __global__ void __launch_bounds__(bulk_threads(QB), 1)
   if (warp == kBulkWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int last[kBulkStages];
+      int64_t last[kBulkStages];
       for (int st = 0; st < kBulkStages; ++st) last[st] = -1;
-      const uint16_t* kg = p.k + bkv * p.Nk * D;
-      const uint16_t* vg = p.v + bkv * p.Nk * D;
-      for (int c = 0; c < n_chunks; ++c) {
-        const int st = c % kBulkStages;
-        if (c >= kBulkStages && !wait(empty(st), ((c / kBulkStages) - 1) & 1, true)) break;
-        const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
-        const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kChunk), k_hi - key0)) * D * 2;
-        mbar_arrive_expect_tx(full(st), 2 * bytes);
-        bulk_load(sbase + st * 2u * kChunkBytes, kg + key0 * D, bytes, full(st));
-        bulk_load(sbase + st * 2u * kChunkBytes + kChunkBytes, vg + key0 * D, bytes, full(st));
-        last[st] = c;
+      int64_t gc = 0;  // ring position over all items
+      bool ok = true;
+      for (int64_t lin = blockIdx.x; lin < p.n_items && ok; lin += gridDim.x) {
+        set_item(lin);
+        const uint16_t* kg = p.k + bkv * p.Nk * D;
+        const uint16_t* vg = p.v + bkv * p.Nk * D;
+        for (int c = 0; c < n_chunks; ++c, ++gc) {
+          const int st = static_cast<int>(gc % kBulkStages);
+          if (gc >= kBulkStages &&
+              !wait(empty(st), static_cast<uint32_t>(((gc / kBulkStages) - 1) & 1), true)) {
+            ok = false;
+            break;
+          }
+          const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
+          const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(kChunk), k_hi - key0)) * D * 2;
+          mbar_arrive_expect_tx(full(st), 2 * bytes);
+          bulk_load(sbase + st * 2u * kChunkBytes, kg + key0 * D, bytes, full(st));
+          bulk_load(sbase + st * 2u * kChunkBytes + kChunkBytes, vg + key0 * D, bytes, full(st));
+          last[st] = gc;
+        }
       }
       // Copies in flight must land before the CTA exits (bounded, ignores abort).
       for (int st = 0; st < kBulkStages; ++st)
-        if (last[st] >= 0) wait(full(st), (last[st] / kBulkStages) & 1, false);
+        if (last[st] >= 0) wait(full(st), static_cast<uint32_t>((last[st] / kBulkStages) & 1), false);
     }
   } else {
     // ------------------------------------------------------------ consumers
-    float m[QB], l[QB], o[QB][8];
-    if constexpr (QB * UB == LPR && UB == U) {
+    int64_t gc = 0;  // ring position of the current item's first chunk
+    for (int64_t lin = blockIdx.x; lin < p.n_items; lin += gridDim.x) {
+      set_item(lin);
+      bool ok = true;
+      float m[QB], l[QB], o[QB][8];
+      static_assert(QB * UB == LPR && UB == U, "four rows of a K/V head per item");
       // One score per lane (the UB = U keys of a stage at once): after packed
       // partial dot products, a
       // reduce-scatter over the LPR lanes of a key row leaves lane `sub` the
@@ -445,8 +490,12 @@ __global__ void __launch_bounds__(bulk_threads(QB), 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o2[qi][e] = 0ull;
       for (int c = 0; c < n_chunks; ++c) {
-        const int st = c % kBulkStages;
-        if (!__all_sync(0xffffffffu, wait(full(st), (c / kBulkStages) & 1, true))) break;
+        const int st = static_cast<int>((gc + c) % kBulkStages);
+        if (!__all_sync(0xffffffffu,
+                        wait(full(st), static_cast<uint32_t>(((gc + c) / kBulkStages) & 1), true))) {
+          ok = false;
+          break;
+        }
         const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
         const int nk = static_cast<int>(min(static_cast<int64_t>(kChunk), k_hi - key0));
         const uint16_t* ks = reinterpret_cast<const uint16_t*>(dyn + st * 2u * kChunkBytes);
@@ -538,139 +587,58 @@ __global__ void __launch_bounds__(bulk_threads(QB), 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) f2_unpack(o2[qi][e], o[qi][2 * e], o[qi][2 * e + 1]);
       }
-    } else {
-    float qf[QB][8];
 #pragma unroll
-    for (int qi = 0; qi < QB; ++qi) {
-      int64_t position;
-      const uint4 r = ld_stream(p.q + row_of(qi, position) * D + 8 * sub);
-      unpack8(r, qf[qi]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qf[qi][e] *= p.sc_log2;
-    }
-#pragma unroll
-    for (int qi = 0; qi < QB; ++qi) {
-      m[qi] = -INFINITY;
-      l[qi] = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[qi][e] = 0.0f;
-    }
-    for (int c = 0; c < n_chunks; ++c) {
-      const int st = c % kBulkStages;
-      if (!__all_sync(0xffffffffu, wait(full(st), (c / kBulkStages) & 1, true))) break;
-      const int64_t key0 = k_lo + static_cast<int64_t>(c) * kChunk;
-      const int nk = static_cast<int>(min(static_cast<int64_t>(kChunk), k_hi - key0));
-      const uint16_t* ks = reinterpret_cast<const uint16_t*>(dyn + st * 2u * kChunkBytes);
-      const uint16_t* vs = ks + kChunk * D;
-      // This warp's KPW keys of the stage, UB key rows per lane group at a
-      // time (fewer live registers when QB is large).
-#pragma unroll
-      for (int u0 = 0; u0 < U; u0 += UB) {
-        uint4 kr[UB], vr[UB];
-        int kk[UB];
-#pragma unroll
-        for (int u = 0; u < UB; ++u) {
-          kk[u] = warp * KPW + (u0 + u) * G + grp;
-          if (kk[u] < nk) {
-            kr[u] = *reinterpret_cast<const uint4*>(ks + kk[u] * D + 8 * sub);
-            vr[u] = *reinterpret_cast<const uint4*>(vs + kk[u] * D + 8 * sub);
-          } else {
-            kr[u] = make_uint4(0u, 0u, 0u, 0u);
-            vr[u] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        if (u0 + UB >= U) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(empty(st));  // release orders this warp's reads
-        }
-        float sc[QB][UB];
-#pragma unroll
-        for (int u = 0; u < UB; ++u) {
-          float kf[8];
-          unpack8(kr[u], kf);
-          const int key_rel = static_cast<int>(key0 - k_lo) + kk[u];
-#pragma unroll
-          for (int qi = 0; qi < QB; ++qi) {
-            float dot = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dot = fmaf(qf[qi][e], kf[e], dot);
-#pragma unroll
-            for (int off = 1; off < LPR; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-            sc[qi][u] = (kk[u] < nk && key_rel <= lim_rel[qi]) ? dot : -INFINITY;
-          }
-        }
+      for (int off = LPR; off < 32; off <<= 1) {
 #pragma unroll
         for (int qi = 0; qi < QB; ++qi) {
-          float mx = sc[qi][0];
+          const float m2 = __shfl_xor_sync(0xffffffffu, m[qi], off);
+          const float l2 = __shfl_xor_sync(0xffffffffu, l[qi], off);
+          float o2[8];
 #pragma unroll
-          for (int u = 1; u < UB; ++u) mx = fmaxf(mx, sc[qi][u]);
-          const float m_new = fmaxf(m[qi], mx);
-          if (m_new == -INFINITY) continue;
-          const float alpha = ex2_approx(m[qi] - m_new);
-          l[qi] *= alpha;
+          for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[qi][e], off);
+          merge_state(m[qi], l[qi], o[qi], m2, l2, o2);
+        }
+      }
+      gc += n_chunks;
+      if (grp == 0) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[qi][e] *= alpha;
-          m[qi] = m_new;
+        for (int qi = 0; qi < QB; ++qi) {
 #pragma unroll
-          for (int u = 0; u < UB; ++u) {
-            const float pu = ex2_approx(sc[qi][u] - m_new);
-            l[qi] += pu;
-            float vf[8];
-            unpack8(vr[u], vf);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[qi][e] = fmaf(pu, vf[e], o[qi][e]);
+          for (int e = 0; e < 8; ++e) sm_o[warp][qi][8 * sub + e] = o[qi][e];
+          if (sub == 0) {
+            sm_m[warp][qi] = m[qi];
+            sm_l[warp][qi] = l[qi];
           }
         }
       }
-    }
-    }  // old path
-#pragma unroll
-    for (int off = LPR; off < 32; off <<= 1) {
-#pragma unroll
-      for (int qi = 0; qi < QB; ++qi) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m[qi], off);
-        const float l2 = __shfl_xor_sync(0xffffffffu, l[qi], off);
-        float o2[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[qi][e], off);
-        merge_state(m[qi], l[qi], o[qi], m2, l2, o2);
-      }
-    }
-    if (grp == 0) {
-#pragma unroll
-      for (int qi = 0; qi < QB; ++qi) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sm_o[warp][qi][8 * sub + e] = o[qi][e];
-        if (sub == 0) {
-          sm_m[warp][qi] = m[qi];
-          sm_l[warp][qi] = l[qi];
-        }
-      }
-    }
-  }
-  __syncthreads();
+      consumers_sync(kConsumerThreads);
 
-  for (int idx = threadIdx.x; idx < QB * D; idx += kBulkThreads) {
-    const int qi = idx / D, e = idx % D;
-    if (r0 + qi >= p.R) continue;
-    float M = -INFINITY;
+      for (int idx = threadIdx.x; idx < QB * D; idx += kConsumerThreads) {
+        const int qi = idx / D, e = idx % D;
+        if (r0 + qi >= p.R) continue;
+        float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kBulkWarps; ++w) M = fmaxf(M, sm_m[w][qi]);
-    float L = 0.0f, acc = 0.0f;
-    if (M != -INFINITY) {
+        for (int w = 0; w < kBulkWarps; ++w) M = fmaxf(M, sm_m[w][qi]);
+        float L = 0.0f, acc = 0.0f;
+        if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kBulkWarps; ++w) {
-        const float f = ex2_approx(sm_m[w][qi] - M);
-        L = fmaf(sm_l[w][qi], f, L);
-        acc = fmaf(sm_o[w][qi][e], f, acc);
+          for (int w = 0; w < kBulkWarps; ++w) {
+            const float f = ex2_approx(sm_m[w][qi] - M);
+            L = fmaf(sm_l[w][qi], f, L);
+            acc = fmaf(sm_o[w][qi][e], f, acc);
+          }
+        }
+        const bool empty_row = !(L > 0.0f);
+        int64_t ps;
+        const int64_t qr = row_of(qi, ps);
+        const int64_t slot = ((qr / p.Nq) * p.S + s) * p.Nq + ps;
+        p.o_part[slot * D + e] = empty_row ? 0.0f : acc / L;
+        if (e == 0) p.lse_part[slot] = empty_row ? -INFINITY : (M + log2f(L)) * kLn2;
       }
-    }
-    const bool empty_row = !(L > 0.0f);
-    int64_t ps;
-    const int64_t qr = row_of(qi, ps);
-    const int64_t slot = ((qr / p.Nq) * p.S + s) * p.Nq + ps;
-    p.o_part[slot * D + e] = empty_row ? 0.0f : acc / L;
-    if (e == 0) p.lse_part[slot] = empty_row ? -INFINITY : (M + log2f(L)) * kLn2;
+      // Second meeting: the shared state may be overwritten by the next
+      // item, and the consumers leave together if any of them gave up a wait.
+      if (consumers_sync_or(!ok, kConsumerThreads)) break;
+    }  // items
   }
 }
 
@@ -697,22 +665,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
   float W = 0.0f;
   if (M != -INFINITY) {
-    for (int s = 0; s < S; ++s) {
-      const float w = ex2_approx((lp[static_cast<int64_t>(s) * Nq] - M) * kLog2e);
-      W += w;
-      const float* op = o_part + ((bh * S + s) * Nq + i) * D + lane * E;
-      if constexpr (E == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(op);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
-        acc[2] = fmaf(w, x.z, acc[2]);
-        acc[3] = fmaf(w, x.w, acc[3]);
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(op);
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
+    // Lane j computes the weight of split s0 + j; the splits' partial rows
+    // are then read eight at a time (independent loads in flight) with the
+    // weight broadcast from its lane.
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int n = min(32, S - s0);
+      const float w_lane =
+          lane < n ? ex2_approx((lp[static_cast<int64_t>(s0 + lane) * Nq] - M) * kLog2e) : 0.0f;
+      W += w_lane;
+      const float* op = o_part + ((bh * S + s0) * Nq + i) * D + lane * E;
+      const int64_t stride = Nq * D;  // one split further
+#pragma unroll 8
+      for (int j = 0; j < n; ++j) {
+        const float w = __shfl_sync(0xffffffffu, w_lane, j);
+        if constexpr (E == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(op + j * stride);
+          acc[0] = fmaf(w, x.x, acc[0]);
+          acc[1] = fmaf(w, x.y, acc[1]);
+          acc[2] = fmaf(w, x.z, acc[2]);
+          acc[3] = fmaf(w, x.w, acc[3]);
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(op + j * stride);
+          acc[0] = fmaf(w, x.x, acc[0]);
+          acc[1] = fmaf(w, x.y, acc[1]);
+        }
       }
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   }
   const bool empty = !(W > 0.0f);
   const float inv = empty ? 0.0f : 1.0f / W;
@@ -730,7 +710,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
 template <int D, int DV, int QB, int U, int MINB>
 cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
-  PartialParams p;
+  PartialParams p = {};
   p.q = static_cast<const uint16_t*>(a.q);
   p.k = static_cast<const uint16_t*>(a.k);
   p.v = static_cast<const uint16_t*>(a.v);
@@ -756,7 +736,7 @@ cudaError_t launch_partial(const SplitArgs& a, cudaStream_t stream) {
 
 template <int D, int QB>
 cudaError_t launch_partial_bulk(const SplitArgs& a, cudaStream_t stream) {
-  PartialParams p;
+  PartialParams p = {};
   p.q = static_cast<const uint16_t*>(a.q);
   p.k = static_cast<const uint16_t*>(a.k);
   p.v = static_cast<const uint16_t*>(a.v);
@@ -781,7 +761,15 @@ cudaError_t launch_partial_bulk(const SplitArgs& a, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  const int64_t blocks = (a.BH / p.G) * p.n_qb * a.splits;
+  p.n_items = (a.BH / p.G) * p.n_qb * a.splits;
+  // Persistent: one CTA per SM (the ring takes most of an SM's shared
+  // memory), each walking every gridDim.x-th item.
+  int dev = 0, sms = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int64_t blocks = std::min<int64_t>(p.n_items, std::max(sms, 1));
   splitkv_partial_bulk_kernel<D, QB>
       <<<dim3(static_cast<unsigned>(blocks)), bulk_threads(QB), smem, stream>>>(p);
   return cudaGetLastError();
@@ -798,14 +786,11 @@ cudaError_t launch_splitkv_partial(const SplitArgs& a, cudaStream_t stream) {
     return a.d == 64 ? launch_partial<64, 128, 1, 4, 2>(a, stream)
                      : launch_partial<128, 64, 1, 4, 2>(a, stream);
   const int64_t qb = splitkv_rows_per_cta((a.H / a.Hkv) * a.Nq);
-  if (a.d == 64) {
-    if (qb == 1) return launch_partial<64, 64, 1, 4, 2>(a, stream);
-    if (qb == 4) return launch_partial_bulk<64, 4>(a, stream);
-    return launch_partial_bulk<64, 8>(a, stream);
-  }
-  if (qb == 1) return launch_partial<128, 128, 1, 4, 2>(a, stream);
-  if (qb == 4) return launch_partial_bulk<128, 4>(a, stream);
-  return launch_partial_bulk<128, 8>(a, stream);
+  if (a.d == 64)
+    return qb == 1 ? launch_partial<64, 64, 1, 4, 2>(a, stream)
+                   : launch_partial_bulk<64, 4>(a, stream);
+  return qb == 1 ? launch_partial<128, 128, 1, 4, 2>(a, stream)
+                 : launch_partial_bulk<128, 4>(a, stream);
 }
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, void* o, float* lse,
