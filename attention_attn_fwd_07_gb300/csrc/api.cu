@@ -210,9 +210,13 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   const int64_t BH = p->B * p->H;
   const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
   const int64_t rows = (p->H / Hkv) * p->Nq;  // query rows sharing one K/V head
-  // dv != d: the register-streaming partial kernel, one query row per CTA.
-  const int64_t qb = dv != p->d ? 1 : splitkv_rows_per_cta(rows);
+  // Several rows per K/V head (and dv = d): the tensor-core partial kernel,
+  // one CTA per block of up to 128 rows.  dv != d: the register-streaming
+  // kernel, one query row per CTA.  Otherwise the CUDA-core kernels.
+  const bool tc = dv == p->d && rows >= ATTN_SPLITKV_TC_MIN_ROWS;
+  const int64_t qb = tc ? 128 : (dv != p->d ? 1 : splitkv_rows_per_cta(rows));
   if (p->B * Hkv * ((rows + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
+  if (tc && p->B * p->H * p->Nq > kMaxDim) return ATTN_ERR_UNSUPPORTED;
 
   const size_t part_rows = static_cast<size_t>(BH) * num_splits * static_cast<size_t>(p->Nq);
   SplitArgs a;
@@ -237,7 +241,18 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   a.status = p->dev_status;
   if (a.status == nullptr && default_status_word(&a.status) != cudaSuccess) return ATTN_ERR_CUDA;
   a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
-  if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (tc) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return ATTN_ERR_CUDA;
+    CUtensorMap tq, tk, tv;
+    if (!encode_map(enc, &tq, p->q, BH * p->Nq, 1, p->d) ||
+        !encode_map(enc, &tk, p->k, p->Nk, p->B * Hkv, p->d) ||
+        !encode_map(enc, &tv, p->v, p->Nk, p->B * Hkv, p->d))
+      return ATTN_ERR_CUDA;
+    if (launch_splitkv_partial_tc(a, tq, tk, tv, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  } else if (launch_splitkv_partial(a, stream) != cudaSuccess) {
+    return ATTN_ERR_CUDA;
+  }
   if (launch_combine(a.o_part, a.lse_part, p->o, p->lse, BH, p->Nq, a.dv, num_splits, stream) !=
       cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -82,6 +82,22 @@ ATTN_DECLARE_BWD(64, 128)
 ATTN_DECLARE_BWD(128, 64)
 #undef ATTN_DECLARE_BWD
 
+// Split-KV partial on the tensor cores for rows that share K/V heads
+// (splitkv_tc.cu): tq maps Q as [B*H*Nq rows][d] (z extent 1), tk and tv as
+// the prefill's [B*Hkv][Nk][d] maps.  dv must equal d.
+cudaError_t launch_splitkv_partial_tc(const SplitArgs& a, const CUtensorMap& tq,
+                                      const CUtensorMap& tk, const CUtensorMap& tv,
+                                      cudaStream_t stream);
+
+// Smallest number of query rows per K/V head that the split-KV path serves
+// with the tensor-core partial kernel; fewer go to the CUDA-core kernels,
+// which stream four rows at memory speed (measured, B16 H32 Nk 32768:
+// four rows 0.345 vs 0.376 ms on tensor cores; eight 0.209 vs 0.338 ms;
+// sixteen 0.113 vs 0.337 ms).
+#ifndef ATTN_SPLITKV_TC_MIN_ROWS
+#define ATTN_SPLITKV_TC_MIN_ROWS 5
+#endif
+
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream);
 

@@ -61,6 +61,9 @@ DECODE = Workload("decode B16 H32 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768, 
 # Grouped-query decode: 8 K/V heads shared by groups of 4 query heads.
 DECODE_GQA = Workload("decode GQA B16 H32 Hkv8 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768,
                       128, False, 1005, splits=(8, 16, 32, 64), Hkv=8)
+# Eight query heads per K/V head (the tensor-core partial kernel's case).
+DECODE_GQA8 = Workload("decode GQA B16 H32 Hkv4 Nq1 Nk32768 d128 split-KV", 16, 32, 1, 32768,
+                       128, False, 1006, splits=(4, 8, 16), Hkv=4)
 
 
 def ragged(n: int, causal: bool) -> Workload:

@@ -557,14 +557,16 @@ def main():
                                  "peak": pk["hbm_gbs"], "unit": "GB/s",
                                  "frac": best["GB/s"] / pk["hbm_gbs"],
                                  "peak_source": f"{pk_src} copy bandwidth",
-                                 "traffic": recorded_traffic(
+                                 "traffic": (recorded_traffic(
                                      DECODE_PROFILE_TXT, DECODE_SOURCES,
                                      "traffic_bytes_per_launch" if wd is W.DECODE
-                                     else "gqa_traffic_bytes_per_launch")},
+                                     else "gqa_traffic_bytes_per_launch")
+                                     if wd in (W.DECODE, W.DECODE_GQA) else None)},
                     "l2": f"inputs {decode_bytes(wd) / 1e9:.1f} GB > L2"}
 
         decode = run_decode(W.DECODE)
         decode_gqa = run_decode(W.DECODE_GQA)
+        others.append(run_decode(W.DECODE_GQA8))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

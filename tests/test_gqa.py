@@ -41,6 +41,19 @@ def test_gqa_prefill(d, causal, hkv):
 
 
 @pytest.mark.parametrize("d", [64, 128])
+def test_gqa_splitkv_offsets(d):
+    """Eight rows per K/V head (the tensor-core partial kernel) with offsets
+    that leave whole rows (negative) or whole splits without an admissible key."""
+    w = W.Workload("gqa split offs", 2, 8, 5, 1000, d, True, 450 + d, Hkv=4)
+    q, k, v = W.make_qkv(w)
+    for off in (-3, 0, 400, 995):
+        ref = oracle.attention(q, k, v, causal=True, scale=w.scale, query_offset=off)
+        flags = binding.ATTN_FLAG_ALLOW_NEG_OFFSET if off < 0 else 0
+        o, lse = run_split(*to_dev(q, k, v), True, w.scale, 6, query_offset=off, flags=flags)
+        compare(o, lse, *ref, f"gqa split d={d} offset={off}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("nq", [1, 3, 37])
 @pytest.mark.parametrize("hkv", [1, 2, 8])
 def test_gqa_splitkv(d, nq, hkv):
@@ -56,9 +69,14 @@ def test_gqa_splitkv(d, nq, hkv):
     compare(o, lse, *ref, f"gqa prefill path Hkv={hkv} Nq={nq}")
 
 
-@pytest.mark.parametrize("S", [16, 32])
-def test_gqa_decode_full_size(S):
-    w = W.DECODE_GQA
+# Groups of four rows take the CUDA-core partial kernel, groups of eight the
+# tensor-core one.
+GQA8 = W.DECODE_GQA8
+
+
+@pytest.mark.parametrize("w,S", [(W.DECODE_GQA, 16), (W.DECODE_GQA, 32), (GQA8, 16)],
+                         ids=["g4-S16", "g4-S32", "g8-S16"])
+def test_gqa_decode_full_size(w, S):
     q, k, v = W.make_qkv(w, device=DEV)
     o, lse = run_split(q, k, v, w.causal, w.scale, S)
     G = w.H // w.kv_heads
