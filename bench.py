@@ -64,6 +64,9 @@ def parse_args():
                          "(smaller cases for ncu captures) and print its GB/s")
     ap.add_argument("--decode-profile-gqa", action="store_true",
                     help="with --decode-profile-batch: the grouped-K/V-head decode workload")
+    ap.add_argument("--decode-profile-gqa8", action="store_true",
+                    help="with --decode-profile-batch: the decode with eight query heads per "
+                         "K/V head (tensor-core partial kernel)")
     ap.add_argument("--bwd-profile-batch", type=int, default=0,
                     help="run only the backward of the long causal prefill with this batch "
                          "size (smaller cases for ncu captures) and print its TFLOPS")
@@ -380,7 +383,8 @@ def main():
 
     if args.decode_profile_batch > 0:
         # Decode only, smaller batch: the case the ncu captures run on.
-        base = W.DECODE_GQA if args.decode_profile_gqa else W.DECODE
+        base = (W.DECODE_GQA8 if args.decode_profile_gqa8 else
+                W.DECODE_GQA if args.decode_profile_gqa else W.DECODE)
         wd = W.Workload(base.name.replace("B16", f"B{args.decode_profile_batch}"),
                         args.decode_profile_batch, base.H, 1, base.Nk, base.d,
                         False, base.seed, Hkv=base.Hkv)
