@@ -92,8 +92,8 @@ cudaError_t launch_splitkv_partial_tc(const SplitArgs& a, const CUtensorMap& tq,
 // Smallest number of query rows per K/V head that the split-KV path serves
 // with the tensor-core partial kernel; fewer go to the CUDA-core kernels,
 // which stream four rows at memory speed (measured, B16 H32 Nk 32768:
-// four rows 0.345 vs 0.376 ms on tensor cores; eight 0.209 vs 0.338 ms;
-// sixteen 0.113 vs 0.337 ms).
+// four rows 0.345 ms on CUDA cores, no faster on tensor cores; eight 0.170
+// vs 0.336 ms; sixteen 0.093 vs 0.335 ms).
 #ifndef ATTN_SPLITKV_TC_MIN_ROWS
 #define ATTN_SPLITKV_TC_MIN_ROWS 5
 #endif

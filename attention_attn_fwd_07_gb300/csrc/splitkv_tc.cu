@@ -19,9 +19,11 @@
 //               2^8.  Epilogue: the normalised o (f32) and the natural-log
 //               LSE of the split, o = 0 and lse = -inf for a row with no
 //               admissible key in the split.
-// TMEM: S [0,128), O [128,128+d).  The tensor core is far from busy (a few
-// real rows per MMA); the point is to keep the CUDA cores out of the dot
-// products, so that any number of rows per K/V head streams K and V at
+// TMEM: S [0,128), O [128,128+d), 256 columns, and a 2-stage ring (4 at
+// d = 64) so that two CTAs share an SM: their independent S -> softmax ->
+// P V chains cover each other's latency.  The tensor core is far from busy
+// (a few real rows per MMA); the point is to keep the CUDA cores out of the
+// dot products, so that any number of rows per K/V head streams K and V at
 // memory speed.  Every mbarrier wait is bounded (status word, clean exit).
 #include <algorithm>
 #include <cuda_bf16.h>
@@ -46,7 +48,7 @@ struct TcCfg {
   static constexpr int kAtoms = D / 64;                    // 128-byte swizzle atoms per row
   static constexpr uint32_t kAtomBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = BM * D * 2;       // Q block, K tile, V tile
-  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kStages = D == 128 ? 2 : 4;  // two CTAs per SM
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = kTileBytes;
   static constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
@@ -102,7 +104,7 @@ struct TcWaiter {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
     splitkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcParams p) {
   using C = TcCfg<D>;
