@@ -213,7 +213,9 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   // Several rows per K/V head (and dv = d): the tensor-core partial kernel,
   // one CTA per block of up to 128 rows.  dv != d: the register-streaming
   // kernel, one query row per CTA.  Otherwise the CUDA-core kernels.
-  const bool tc = dv == p->d && rows >= ATTN_SPLITKV_TC_MIN_ROWS;
+  const int64_t tc_min_rows =
+      p->d == 128 ? ATTN_SPLITKV_TC_MIN_ROWS_D128 : ATTN_SPLITKV_TC_MIN_ROWS_D64;
+  const bool tc = dv == p->d && rows >= tc_min_rows;
   const int64_t qb = tc ? 128 : (dv != p->d ? 1 : splitkv_rows_per_cta(rows));
   if (p->B * Hkv * ((rows + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
   if (tc && p->B * p->H * p->Nq > kMaxDim) return ATTN_ERR_UNSUPPORTED;

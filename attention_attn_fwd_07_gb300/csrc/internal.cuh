@@ -90,12 +90,15 @@ cudaError_t launch_splitkv_partial_tc(const SplitArgs& a, const CUtensorMap& tq,
                                       cudaStream_t stream);
 
 // Smallest number of query rows per K/V head that the split-KV path serves
-// with the tensor-core partial kernel; fewer go to the CUDA-core kernels,
-// which stream four rows at memory speed (measured, B16 H32 Nk 32768:
-// four rows 0.345 ms on CUDA cores, no faster on tensor cores; eight 0.170
-// vs 0.336 ms; sixteen 0.093 vs 0.335 ms).
-#ifndef ATTN_SPLITKV_TC_MIN_ROWS
-#define ATTN_SPLITKV_TC_MIN_ROWS 5
+// with the tensor-core partial kernel, per head dim; fewer go to the
+// CUDA-core kernels.  Measured, B16 H32 Nk 32768 (tensor cores vs CUDA
+// cores): d = 128, two rows 0.605 vs 0.636 ms, four 0.320 vs 0.344, eight
+// 0.170 vs 0.336; d = 64, four rows 0.246 vs 0.233.
+#ifndef ATTN_SPLITKV_TC_MIN_ROWS_D128
+#define ATTN_SPLITKV_TC_MIN_ROWS_D128 2
+#endif
+#ifndef ATTN_SPLITKV_TC_MIN_ROWS_D64
+#define ATTN_SPLITKV_TC_MIN_ROWS_D64 5
 #endif
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -6,9 +6,11 @@ refuses further allocation, plug-ins whose host program exposes no
 allocator, and latency-critical loops that cannot afford the device
 synchronisation cudaMalloc/cudaFree may cause.  It keeps the split-KV
 scratch in a fixed 32 MiB array inside the library instead of a caller
-workspace.  Here it must give the same O and LSE as the workspace entry point
-(within the parity tolerances) on two different problems called one after
-the other, and must refuse a problem whose scratch exceeds the array.
+workspace.  Here it must meet the fp64 oracle within the parity tolerances,
+as the workspace entry point does (the two may run different partial kernels
+for the same shape, so they are each compared with the oracle, not
+bitwise), on problems called one after the other, and must refuse a problem
+whose scratch exceeds the array.
 
 This file is named to be collected last.
 """
@@ -17,9 +19,10 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from attention_attn_fwd_07_gb300 import binding, build
 from attention_attn_fwd_07_gb300 import inputs as W
-from tests.parity_util import LSE_TOL, O_TOL
+from tests.parity_util import compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -42,23 +45,26 @@ def _call(f, q, k, v, o, lse, causal, scale, splits):
              torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
+def test_noalloc_parity_on_consecutive_calls():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     build.build()
     f = _entry(binding.load_library())
     cases = [(W.Workload("decode-like", 2, 8, 1, 5000, 128, False, 501), 8),
-             (W.Workload("short causal queries", 3, 2, 37, 777, 64, True, 502), 5)]
+             (W.Workload("short causal queries", 3, 2, 37, 777, 64, True, 502), 5),
+             # several rows per head at d = 128: the pipelined CUDA-core kernel
+             (W.Workload("short causal queries d128", 2, 4, 5, 900, 128, True, 503), 4)]
     for w, splits in cases:
-        q, k, v = (t.to(DEV) for t in W.make_qkv(w))
-        o_ref, lse_ref = binding.attn_fwd_splitkv(q, k, v, w.causal, w.scale, splits)
-        o = torch.full_like(o_ref, float("nan"))
-        lse = torch.full_like(lse_ref, float("nan"))
+        q_h, k_h, v_h = W.make_qkv(w)
+        q, k, v = (t.to(DEV) for t in (q_h, k_h, v_h))
+        ref = oracle.attention(q_h, k_h, v_h, causal=w.causal, scale=w.scale)
+        o_ws, lse_ws = binding.attn_fwd_splitkv(q, k, v, w.causal, w.scale, splits)
+        o = torch.full_like(o_ws, float("nan"))
+        lse = torch.full_like(lse_ws, float("nan"))
         assert _call(f, q, k, v, o, lse, w.causal, w.scale, splits) == binding.ATTN_OK
         torch.cuda.synchronize()
-        assert not torch.isnan(o).any() and not torch.isnan(lse).any()
-        assert (o.float() - o_ref.float()).abs().max().item() <= O_TOL, w.name
-        assert (lse - lse_ref).abs().max().item() <= LSE_TOL, w.name
+        compare(o, lse, *ref, f"{w.name} (no-alloc entry point)")
+        compare(o_ws, lse_ws, *ref, f"{w.name} (workspace entry point)")
 
 
 def test_noalloc_refuses_scratch_beyond_its_array():
