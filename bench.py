@@ -46,7 +46,7 @@ PROFILE_TXT = os.path.join(ROOT, "profiles", "fwd_tcgen05_long_prefill_causal.md
 E2E_CHUNK_HEADS = 8
 KERNEL_SOURCES = ["fwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
 DECODE_PROFILE_TXT = os.path.join(ROOT, "profiles", "splitkv_decode.md")
-DECODE_SOURCES = ["splitkv.cu", "ptx.cuh", "internal.cuh"]
+DECODE_SOURCES = ["splitkv.cu", "splitkv_tc.cu", "ptx.cuh", "internal.cuh"]
 BWD_PROFILE_TXT = os.path.join(ROOT, "profiles", "bwd_tcgen05_long_prefill_causal.md")
 BWD_SOURCES = ["bwd_tcgen05.cu", "ptx.cuh", "internal.cuh"]
 
