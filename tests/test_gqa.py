@@ -88,3 +88,41 @@ def test_gqa_decode_full_size(w, S):
         kh, vh = k[b:b + 1, hk:hk + 1].cpu(), v[b:b + 1, hk:hk + 1].cpu()
         ref = oracle.attention(qh, kh, vh, causal=False, scale=w.scale)
         compare(o[b:b + 1, hs], lse[b:b + 1, hs], *ref, f"gqa decode b={b} hk={hk} S={S}")
+
+
+def _sweep_cases(n):
+    """Seeded shapes across the split-KV dispatch: rows per K/V head from 1 to
+    12 (register-streaming, pipelined and tensor-core partial kernels), both
+    head dims, ragged key counts, 1..17 splits, causal with offsets that
+    leave rows or splits empty, and value dims different from the key dim."""
+    rng = np.random.default_rng(2024)
+    cases = []
+    for i in range(n):
+        d = int(rng.choice([64, 128]))
+        G = int(rng.choice([1, 2, 3, 4, 6, 8]))
+        Hkv = int(rng.choice([1, 2]))
+        Nq = int(rng.choice([1, 1, 2, 3]))
+        Nk = int(rng.integers(1, 2500))
+        S = int(rng.integers(1, 18))
+        causal = bool(rng.integers(0, 2))
+        off = int(rng.choice([Nk - Nq, Nk // 2, 0, -2])) if causal else 0
+        dv = int(rng.choice([0, 0, 0, 64 if d == 128 else 128]))
+        cases.append((i, d, G, Hkv, Nq, Nk, S, causal, off, dv))
+    return cases
+
+
+@pytest.mark.parametrize("i,d,G,Hkv,Nq,Nk,S,causal,off,dv", _sweep_cases(40))
+def test_splitkv_dispatch_sweep(i, d, G, Hkv, Nq, Nk, S, causal, off, dv):
+    w = W.Workload(f"sweep {i}", 1, G * Hkv, Nq, Nk, d, causal, 5000 + i, Hkv=Hkv, dv=dv)
+    q, k, v = W.make_qkv(w)
+    ref = oracle.attention(q, k, v, causal=causal, scale=w.scale, query_offset=off)
+    flags = binding.ATTN_FLAG_ALLOW_NEG_OFFSET if off < 0 else 0
+    qd, kd, vd = to_dev(q, k, v)
+    if dv:
+        o, lse = binding.attn_fwd_splitkv_ex(qd, kd, vd, causal, w.scale, S, query_offset=off,
+                                             flags=flags)
+        torch.cuda.synchronize()
+    else:
+        o, lse = run_split(qd, kd, vd, causal, w.scale, S, query_offset=off, flags=flags)
+    compare(o, lse, *ref, f"sweep {i}: d={d} G={G} Hkv={Hkv} Nq={Nq} Nk={Nk} S={S} "
+                          f"causal={causal} off={off} dv={dv}")
