@@ -219,6 +219,28 @@ def test_worked_example_large_logits(second):
     compare(o, lse, *ref, f"worked example split {second}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_second_half_spikes(d):
+    """Scores that jump in the second half (keys 64-127) of a key tile: the
+    prefill softmax exponentiates the first half against a provisional
+    reference and must redo it when the second half lifts the maximum past
+    the rescale threshold -- on the first tile (no O yet) and on a later
+    tile (with an O rescale)."""
+    g = torch.Generator().manual_seed(81)
+    nk = 256
+    q = torch.zeros((1, 1, 4, d))
+    for r, a in enumerate((1.0, 0.5, 0.25, -1.0)):
+        q[0, 0, r, 0] = a
+    k = 0.1 * torch.randn((1, 1, nk, d), generator=g)
+    k[0, 0, 0, 0], k[0, 0, 100, 0] = 10.0, 30.0    # tile 0: first half 10, second 30
+    k[0, 0, 128, 0], k[0, 0, 200, 0] = 35.0, 60.0  # tile 1: first half 35, second 60
+    v = torch.randn((1, 1, nk, d), generator=g)
+    q, k, v = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    ref = oracle_full(q, k, v, False, 1.0)
+    o, lse = run_fwd(*to_dev(q, k, v), False, 1.0)
+    compare(o, lse, *ref, f"second-half spikes d={d}")
+
+
 def test_combine_alone():
     """attn_combine on partial states the oracle computes per key range."""
     w = W.Workload("combine", 2, 3, 17, 500, 128, False, 31)
