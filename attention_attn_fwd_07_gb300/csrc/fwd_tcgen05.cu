@@ -18,9 +18,9 @@
 // on tcgen05 with TMEM accumulators):
 //   warp 9      TMA producer: Q_A, Q_B once, then K0 V0 K1 V1 ... through an
 //               NS-stage shared-memory ring (full/empty mbarriers).
-//   warp 8      MMA issuer (one thread): S_X = Q_X K^T into TMEM (SS MMA), and
-//               O_X += P_X V (TS MMA, P read from TMEM) for X in {A, B},
-//               (With FP8 Q and K, S comes from kind::f8f6f4 MMAs instead.)
+//   warp 8      MMA issuer: S_X = Q_X K^T into TMEM (SS MMA), and
+//               O_X += P_X V (TS MMA, P read from TMEM) for X in {A, B}
+//               (with FP8 Q and K, S comes from kind::f8f6f4 MMAs instead),
 //               ordered so that the tensor core works on one tile while the
 //               other tile's softmax runs (ping-pong).
 //   warps 0-3   softmax of tile A; warps 4-7 softmax of tile B.  One thread
@@ -29,11 +29,14 @@
 //               S columns with tcgen05.st in two halves of 64 keys, each
 //               announced on its own barrier so that O += P V starts on the
 //               first half while the second is computed; O rescaled in TMEM
-//               only when the
-//               row maximum grew by more than 2^8 (otherwise the stale
-//               reference is kept; o and l share it, so o / l is unchanged).
-//               Epilogue: O / l -> bf16 global, LSE -> f32 global.
+//               only when the row maximum grew by more than 2^8 (otherwise
+//               the stale reference is kept; o and l share it, so o / l is
+//               unchanged).  Epilogue: O / l -> bf16 global, LSE -> f32 global.
 // TMEM (512 columns): S_A [0,128) S_B [128,256) O_A [256,256+d) O_B [256+d, 256+2d).
+// The one-tile configuration (NT = 1, used at d = 64, where CTAs are short)
+// drops tile B: warps 0-3 softmax, warp 4 MMA, warp 5 TMA, TMEM S [0,128)
+// O [128,128+d) in a 256-column allocation and a smaller ring, so that two
+// CTAs share an SM and interleave on its tensor core instead.
 //
 // Every mbarrier wait is bounded (globaltimer budget); on expiry the CTA
 // records a timeout in the status word, all roles leave their loops, pending
@@ -50,14 +53,19 @@ namespace {
 
 constexpr int BM = 128;            // query rows per tile (= TMEM lanes)
 constexpr int BN = 128;            // keys per K/V tile
-constexpr int kThreads = 320;      // 8 softmax warps + MMA warp + TMA warp
-constexpr int kWarpMma = 8;
-constexpr int kWarpLoad = 9;
+// NT query tiles per CTA: 4 NT softmax warps, then the MMA and TMA warps.
+__host__ __device__ constexpr int threads_for(int NT) { return 128 * NT + 64; }
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows by > 2^8
 
-// D: head dim of Q and K; DV: head dim of V and O (the value dim may differ).
-template <int D, int DV, bool FP8>
+// D: head dim of Q and K; DV: head dim of V and O (the value dim may differ);
+// NT: query tiles per CTA.  Two tiles share every K/V tile and ping-pong on
+// the tensor core inside one CTA (one CTA per SM: 512 TMEM columns); one
+// tile takes 128 + DV columns (a 256-column allocation) and a ring small
+// enough that two CTAs share an SM, their pipelines covering each other's
+// start, drain and softmax latency -- the better trade when CTAs are short.
+template <int D, int DV, bool FP8, int NT = 2>
 struct Cfg {
+  static_assert(NT == 1 || NT == 2, "one or two query tiles per CTA");
   static constexpr int kQKElem = FP8 ? 1 : 2;               // bytes per Q/K element
   static constexpr int kQKAtoms = D * kQKElem / 128;        // 128-byte swizzle atoms per Q/K row
   static constexpr int kVAtoms = DV / 64;                   // ... per V row (bf16)
@@ -66,9 +74,10 @@ struct Cfg {
   static constexpr uint32_t kKBytes = BN * D * kQKElem;     // one K tile
   static constexpr uint32_t kVBytes = BN * DV * 2;          // one V tile
   static constexpr uint32_t kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // one ring stage
-  static constexpr int kStages = (kKVBytes >= 32768u) ? 4 : 8;
+  static constexpr int kStages =
+      NT == 2 ? ((kKVBytes >= 32768u) ? 4 : 8) : ((kKVBytes >= 32768u) ? 2 : 5);
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffKV = 2 * kQBytes;
+  static constexpr uint32_t kOffKV = NT * kQBytes;
   static constexpr uint32_t kOffBar = kOffKV + kStages * kKVBytes;
   // barriers: full[S], empty[S], q_full, s_full[2], p_ready[2] (keys 0-63 of
   // P stored), p2_ready[2] (keys 64-127), o_full[2], drain
@@ -83,13 +92,19 @@ struct Cfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + 1 KiB alignment slack
-  static constexpr uint32_t kColS = 0;      // + 128 * tile
-  static constexpr uint32_t kColO = 256;    // + DV * tile
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;        // + 128 * tile
+  static constexpr uint32_t kColO = 128 * NT;  // + DV * tile
+  static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
+  static constexpr int kThreads = threads_for(NT);
+  static constexpr int kWarpMma = 4 * NT;
+  static constexpr int kWarpLoad = 4 * NT + 1;
   static constexpr uint32_t kIdescQK = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, DV, 1);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kSmemBytes > 232448 / 2, "one CTA per SM keeps the 512-column TMEM allocation uncontended");
+  static_assert(NT == 1 || kSmemBytes > 232448 / 2,
+                "one two-tile CTA per SM keeps the 512-column TMEM allocation uncontended");
+  static_assert(NT == 2 || 2 * (kSmemBytes + 1024) <= 232448,
+                "two one-tile CTAs per SM (256 TMEM columns each)");
 };
 
 struct KParams {
@@ -143,12 +158,14 @@ __device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
   return static_cast<int>(min(n_all, last_key / BN + 1));
 }
 
-template <int D, int DV, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int DV, bool FP8, int NT>
+__global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     attn_fwd_tcgen05_kernel(const __grid_constant__ CUtensorMap tq,
                             const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv, const KParams p) {
-  using C = Cfg<D, DV, FP8>;
+  using C = Cfg<D, DV, FP8, NT>;
+  constexpr int kWarpMma = C::kWarpMma;
+  constexpr int kWarpLoad = C::kWarpLoad;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -178,12 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bh = blockIdx.x / p.n_qblk;
     qb = static_cast<int>(blockIdx.x % p.n_qblk);
   }
-  const int64_t q0 = static_cast<int64_t>(qb) * (2 * BM);
+  const int64_t q0 = static_cast<int64_t>(qb) * (NT * BM);
   // K/V head of this query head (grouped K/V heads: H / group per batch).
   const int64_t bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
   int ntile[2];
   ntile[0] = tiles_for(q0, p);
-  ntile[1] = tiles_for(q0 + BM, p);
+  ntile[1] = NT == 2 ? tiles_for(q0 + BM, p) : 0;
   const int n_kv = max(ntile[0], ntile[1]);
 
   if (threadIdx.x == 0) {
@@ -224,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0 && n_kv > 0) {
       uint32_t qbytes = 0;
-      for (int x = 0; x < 2; ++x) qbytes += ntile[x] > 0 ? C::kQBytes : 0u;
+      for (int x = 0; x < NT; ++x) qbytes += ntile[x] > 0 ? C::kQBytes : 0u;
       mbar_arrive_expect_tx(bar(C::kBarQ), qbytes);
-      for (int x = 0; x < 2; ++x) {
+      for (int x = 0; x < NT; ++x) {
         if (ntile[x] == 0) continue;
         for (int a = 0; a < C::kQKAtoms; ++a)
           tma_load_3d(sQ + x * C::kQBytes + a * C::kAtomBytes, &tq, bar(C::kBarQ),
@@ -302,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = wait_w(bar(C::kBarFull + 0), 0);
       if (ok) {
         tc_fence_after();
-        for (int x = 0; x < 2; ++x) {
+        for (int x = 0; x < NT; ++x) {
           if (ntile[x] > 0) {
             qk(x, 0);
             commit(bar(C::kBarS + x));
@@ -317,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool k_ready = false;
         ok = wait_w(bar(C::kBarFull + sV), (tV / C::kStages) & 1);
         if (!ok) break;
-        for (int x = 0; x < 2 && ok; ++x) {
+        for (int x = 0; x < NT && ok; ++x) {
           if (j >= ntile[x]) continue;
           ok = wait_w(bar(C::kBarP + x), j & 1);
           if (!ok) break;
@@ -502,12 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int DV, bool FP8>
+template <int D, int DV, bool FP8, int NT = 2>
 cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                    const CUtensorMap& tv, cudaStream_t stream) {
-  using C = Cfg<D, DV, FP8>;
+  using C = Cfg<D, DV, FP8, NT>;
   static_assert(C::kSmemBytes < (1u << 20), "");
-  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, DV, FP8>,
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, DV, FP8, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
   if (err != cudaSuccess) return err;
@@ -520,7 +537,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.qoff = a.query_offset;
   p.H = a.H;
   p.group = a.group;
-  p.n_qblk = static_cast<int>((a.Nq + 2 * BM - 1) / (2 * BM));
+  p.n_qblk = static_cast<int>((a.Nq + NT * BM - 1) / (NT * BM));
   // Scheduling groups: whole K/V heads whose K and V take about 48 MB of L2.
   const double kv_head_bytes =
       static_cast<double>(a.Nk) * (D * (FP8 ? 1.0 : 2.0) + DV * 2.0);
@@ -532,7 +549,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.flags = a.flags;
   p.timeout_ns = a.timeout_ns;
   const int64_t blocks = a.BH * p.n_qblk;
-  attn_fwd_tcgen05_kernel<D, DV, FP8><<<dim3(static_cast<unsigned>(blocks)), dim3(kThreads),
+  attn_fwd_tcgen05_kernel<D, DV, FP8, NT><<<dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),
                                C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -546,7 +563,7 @@ cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CU
                       : launch<128, 128, true>(a, tq, tk, tv, stream);
   if (a.d == 64) {
     if (a.dv == 128) return launch<64, 128, false>(a, tq, tk, tv, stream);
-    return launch<64, 64, false>(a, tq, tk, tv, stream);
+    return launch<64, 64, false, 1>(a, tq, tk, tv, stream);
   }
   if (a.dv == 64) return launch<128, 64, false>(a, tq, tk, tv, stream);
   return launch<128, 128, false>(a, tq, tk, tv, stream);

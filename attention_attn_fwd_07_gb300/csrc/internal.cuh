@@ -42,8 +42,9 @@ struct SplitArgs {
   uint64_t timeout_ns;  // per-wait limit of the pipelined partial kernel
 };
 
-// Query rows per CTA of the prefill kernel (two 128-row tiles).
-constexpr int kFwdRowsPerCta = 256;
+// Fewest query rows per CTA of the prefill kernel (one 128-row tile; two-tile
+// configurations take 256), for grid-size checks.
+constexpr int kFwdRowsPerCta = 128;
 
 // Query rows one split-KV partial work item serves, out of the rows that
 // share one K/V head (query heads of the group x query positions): one, or
