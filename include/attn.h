@@ -137,9 +137,11 @@ size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
  * cut into num_splits contiguous ranges of L = ceil(Nk/num_splits) keys
  * rounded up to a multiple of 128 (trailing ranges may be empty); each range
  * yields a partial (normalised o, lse) in `workspace`, then attn_combine
- * merges them into O and LSE.  With grouped K/V heads (attn_fwd_splitkv_ex)
- * one CTA serves all query heads of a K/V head, so each K/V byte is read
- * once per group.  1 <= num_splits <= 256.  Two launches on
+ * merges them into O and LSE.  When several query rows share a K/V head
+ * (grouped K/V heads through attn_fwd_splitkv_ex, or Nq > 1) they are served
+ * together -- up to 128 rows per CTA on the tensor cores, or in blocks of
+ * four on the CUDA cores at d = 64 with at most four rows -- so each K/V byte
+ * is read about once per group.  1 <= num_splits <= 256.  Two launches on
  * `stream`; `workspace` (device, 16-byte aligned, caller-owned) must hold
  * attn_splitkv_workspace_bytes(...) bytes (ATTN_ERR_WORKSPACE otherwise).
  */
@@ -149,8 +151,8 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      size_t workspace_bytes, cudaStream_t stream);
 
 /* attn_fwd_splitkv with query_offset, Hkv, dv, flags, dev_status and
- * wait_timeout_us from `p` (the latter two apply to the pipelined partial
- * kernel used when several query rows share a K/V head; ATTN_FLAG_TEST_SKIP_LOAD
+ * wait_timeout_us from `p` (the latter two apply to the partial kernels
+ * used when several query rows share a K/V head; ATTN_FLAG_TEST_SKIP_LOAD
  * applies to the prefill kernel only).  With dv != d every query row gets
  * its own partial CTAs, so a K/V head shared by several rows is read once
  * per row; the workspace holds dv-wide partials. */
