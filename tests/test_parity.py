@@ -221,11 +221,10 @@ def test_worked_example_large_logits(second):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_second_half_spikes(d):
-    """Scores that jump in the second half (keys 64-127) of a key tile: the
-    prefill softmax exponentiates the first half against a provisional
-    reference and must redo it when the second half lifts the maximum past
-    the rescale threshold -- on the first tile (no O yet) and on a later
-    tile (with an O rescale)."""
+    """Scores that jump in the second half (keys 64-127) of a key tile, on
+    the first tile (no O yet) and on a later tile (with an O rescale): the
+    maximum of the whole tile must be known before P's first half, which the
+    P V product consumes early, is exponentiated."""
     g = torch.Generator().manual_seed(81)
     nk = 256
     q = torch.zeros((1, 1, 4, d))
@@ -239,6 +238,36 @@ def test_second_half_spikes(d):
     ref = oracle_full(q, k, v, False, 1.0)
     o, lse = run_fwd(*to_dev(q, k, v), False, 1.0)
     compare(o, lse, *ref, f"second-half spikes d={d}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_row_maximum_per_row(d, causal):
+    """Each row's exponent reference must be that row's own maximum over the
+    whole key tile.  Key j is the unit vector of dimension j mod (d-1) plus a
+    shared last dimension; query row i puts 256 on dimension (37 i) mod (d-1)
+    and a per-row base in {-256, ..., 256} on the last one, so with scale 1
+    row i scores base_i + 256 on one key in each 127 (at a column of the tile
+    that moves from row to row) and base_i elsewhere: 369 log2 units apart.
+    A reference taken over part of the row overflows 2^x on the hot key; one
+    shared across rows (base_i differ by up to 739 log2 units) underflows the
+    whole row to zero.  Either leaves O or LSE far from the oracle."""
+    nq, nk = 256, 384
+    i = torch.arange(nq)
+    j = torch.arange(nk)
+    q = torch.zeros((1, 1, nq, d))
+    q[0, 0, i, (37 * i) % (d - 1)] = 256.0
+    q[0, 0, i, d - 1] = 64.0 * ((13 * i) % 9 - 4).float()
+    k = torch.zeros((1, 1, nk, d))
+    k[0, 0, j, j % (d - 1)] = 1.0
+    k[0, 0, :, d - 1] = 1.0
+    v = torch.randn((1, 1, nk, d), generator=torch.Generator().manual_seed(82))
+    q, k, v = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    ref = oracle_full(q, k, v, causal, 1.0)
+    o, lse = run_fwd(*to_dev(q, k, v), causal, 1.0)
+    compare(o, lse, *ref, f"per-row maximum d={d} causal={causal}")
+    o, lse = run_split(*to_dev(q, k, v), causal, 1.0, 3)
+    compare(o, lse, *ref, f"per-row maximum split d={d} causal={causal}")
 
 
 def test_combine_alone():
