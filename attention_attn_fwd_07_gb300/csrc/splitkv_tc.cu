@@ -268,9 +268,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS;
     const uint32_t tO = tmem + lane_off + C::kColO;
+    // A warp none of whose rows is in the block only keeps pace with the
+    // barriers: its rows of P and O are never read back (each row of P V
+    // depends on that row of P alone), so it skips the softmax and the
+    // epilogue, leaving the issue slots of its SMSP to the live rows.
+    const bool idle = __all_sync(0xffffffffu, !valid);
     float m_run = -INFINITY, m_ref = -INFINITY, l = 0.0f;
     bool ok = true;
-    for (int j = 0; j < n_blk; ++j) {
+    for (int j = 0; idle && j < n_blk; ++j) {
+      ok = __all_sync(0xffffffffu, wait(bar(C::kBarS), j & 1));
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive(bar(C::kBarP));
+        mbar_arrive(bar(C::kBarP2));
+      }
+    }
+    for (int j = 0; !idle && j < n_blk; ++j) {
       ok = __all_sync(0xffffffffu, wait(bar(C::kBarS), j & 1));
       if (!ok) break;
       tc_fence_after();
@@ -346,11 +359,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
       l += sum_lo + sum_hi;
     }
-    if (ok && n_blk > 0) {
+    if (ok && n_blk > 0 && !idle) {
       ok = __all_sync(0xffffffffu, wait(bar(C::kBarO), 0));
       if (ok) tc_fence_after();
     }
-    if (ok) {
+    if (ok && !idle) {
       // Partial slot of (batch*H + query head, split s, position).
       const int64_t bh = b * p.H + hk * p.G + (valid ? r / p.Nq : 0);
       const int64_t slot = (bh * p.S + s) * p.Nq + pos;
