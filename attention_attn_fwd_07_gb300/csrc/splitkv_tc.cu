@@ -261,10 +261,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool valid = row < rows;
     const int64_t r = r0 + row;          // row within the K/V head's group
     const int64_t pos = valid ? r % p.Nq : 0;
-    // Last admissible key (absolute), -1 for rows past the block.
-    int64_t lim = -1;
-    if (valid) lim = p.causal ? min(p.Nk - 1, pos + p.qoff) : p.Nk - 1;
-    lim = min(lim, k_hi - 1);
+    // Last admissible key (absolute).  Rows past the block are left unmasked:
+    // their rows of P and O are never read back, and a warp with nothing to
+    // mask takes the row maximum from the TMEM load.
+    int64_t lim = k_hi - 1;
+    if (valid && p.causal) lim = min(lim, pos + p.qoff);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS;
     const uint32_t tO = tmem + lane_off + C::kColO;
@@ -288,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[128];
-      tmem_ld_x128(tS, sr);
+      // The load returns the row maximum of the unmasked tile.
+      float tmax = tmem_ld_max_x128(tS, sr);
       float sv[128];
 #pragma unroll
       for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(sr[c]);
@@ -299,24 +301,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (__any_sync(0xffffffffu, rel < BN - 1)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) sv[c] = (c > rel) ? -INFINITY : sv[c];
+          // Masking invalidates the load's maximum.
+          float mx[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            mx[g] = fmaxf(sv[16 * g], sv[16 * g + 1]);
+#pragma unroll
+            for (int c = 2; c < 16; c += 2) mx[g] = fmax3f(mx[g], sv[16 * g + c], sv[16 * g + c + 1]);
+          }
+          tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                        fmaxf(mx[6], mx[7]));
         }
       }
-      float mx[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        mx[g] = fmaxf(sv[16 * g], sv[16 * g + 1]);
-#pragma unroll
-        for (int c = 2; c < 16; c += 2) mx[g] = fmax3f(mx[g], sv[16 * g + c], sv[16 * g + c + 1]);
-      }
-      const float tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
-                                fmaxf(mx[6], mx[7]));
       const float m_new = fmaxf(m_run, tmax * p.sc_log2);
       m_run = m_new;
       float alpha = 1.0f;
       bool rescale = false;
       if (m_new > m_ref + kRescaleThreshold) {
         alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
-        rescale = (m_ref != -INFINITY);
+        rescale = valid && (m_ref != -INFINITY);  // rows past the block: no O to keep
         l *= alpha;
         m_ref = m_new;
       }
