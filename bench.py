@@ -185,20 +185,36 @@ def event_time(fn, steps: int, stream) -> float:
     return start.elapsed_time(end) / steps
 
 
-def event_time_flushed(fn, steps: int, stream, scratch: torch.Tensor) -> float:
-    """Average ms per call with L2 flushed before each call: a buffer larger
-    than L2 is rewritten outside the timed events."""
-    total = 0.0
+def event_time_each(fn, steps: int, stream, scratch: torch.Tensor | None = None) -> list:
+    """ms of each of `steps` calls, every call between its own CUDA events on
+    `stream`; with `scratch` (a buffer larger than L2), L2 is flushed by
+    rewriting it before each call, outside the events."""
+    out = []
     for _ in range(steps):
-        scratch.add_(1)
+        if scratch is not None:
+            scratch.add_(1)
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
         fn()
         end.record(stream)
         end.synchronize()
-        total += start.elapsed_time(end)
-    return total / steps
+        out.append(start.elapsed_time(end))
+    return out
+
+
+def launch_stats(times_ms: list) -> dict:
+    """Median, 10th and 90th percentile of per-call times (ms)."""
+    a = np.asarray(times_ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
+def event_time_flushed(fn, steps: int, stream, scratch: torch.Tensor) -> tuple:
+    """Average ms per call with L2 flushed before each call, and the per-call
+    distribution."""
+    t = event_time_each(fn, steps, stream, scratch)
+    return sum(t) / len(t), launch_stats(t)
 
 
 # ------------------------------------------------------------------ CPU oracle legs
@@ -428,6 +444,9 @@ def main():
     clocks = sampler.stop(t0, t1)
     launches += args.steps
     ms = max_over_ranks_(ms)
+    # Per-launch distribution (this rank), taken after the timed region.
+    main_dist = launch_stats(event_time_each(step, 50, stream))
+    launches += 50
     flops = prefill_flops(w)
     value = world * flops / (ms / 1e3) / 1e12
     per_gpu = flops / (ms / 1e3) / 1e12
@@ -486,7 +505,8 @@ def main():
             else:
                 n = args.steps
                 scratch = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
-                m = max_over_ranks_(event_time_flushed(st, n, stream, scratch))
+                m, flushed_dist = event_time_flushed(st, n, stream, scratch)
+                m = max_over_ranks_(m)
                 del scratch
             launches += n
             tf = prefill_flops(wo) / (m / 1e3) / 1e12
@@ -494,6 +514,8 @@ def main():
                            "ms_per_step": m, "frac_of_peak": tf / pk["bf16_tflops"],
                            "l2": "inputs > L2" if wo.Nq >= 8192 else
                                  "L2 flushed (256 MB rewrite) before each timed launch"})
+            if wo.Nq < 8192:
+                others[-1]["launch_ms"] = flushed_dist
             if wo.d == 64:  # the d = 64 backward on the same inputs
                 rb = run_backward(wo, qq, kk, vv, oo, ll, dev, stream, args, pk, pk_src, world,
                                   max_over_ranks_)
@@ -535,6 +557,7 @@ def main():
             od = torch.empty_like(qd)
             ld = torch.empty((wd.B, wd.H, 1), dtype=torch.float32, device=dev)
             results = []
+            calls = {}
             for S in wd.splits:
                 need = binding.attn_splitkv_workspace_bytes(wd.B, wd.H, 1, wd.d, S)
                 ws = torch.empty((need,), dtype=torch.uint8, device=dev)
@@ -543,6 +566,7 @@ def main():
                     binding.attn_fwd_splitkv(qd, kd, vd, False, wd.scale, S, workspace=ws, o=od,
                                              lse=ld, stream=stream)
 
+                calls[S] = sd
                 for _ in range(args.warmup):
                     sd()
                 n = max(10, args.steps // 4)
@@ -551,11 +575,14 @@ def main():
                 gbs = decode_bytes(wd) / (m / 1e3) / 1e9
                 results.append({"splits": S, "ms_per_step": m, "GB/s": gbs,
                                 "workspace_bytes": need})
-            del qd, kd, vd
             best = max(results, key=lambda r: r["GB/s"])
+            # Per-call distribution (partial + combine) at the best split count.
+            best_dist = launch_stats(event_time_each(calls[best["splits"]], 30, stream))
+            launches += 2 * 30
+            del calls, qd, kd, vd
             return {"workload": wd.name, "metric": "HBM GB/s", "unit": "GB/s",
                     "value": world * best["GB/s"], "ms_per_step": best["ms_per_step"],
-                    "splits": best["splits"], "per_split_count": results,
+                    "splits": best["splits"], "per_split_count": results, "launch_ms": best_dist,
                     "algorithmic_bytes_per_step": decode_bytes(wd),
                     "roofline": {"bound": "hbm", "achieved": best["GB/s"],
                                  "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -579,6 +606,7 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "launch_ms": main_dist,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
