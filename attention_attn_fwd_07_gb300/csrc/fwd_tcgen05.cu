@@ -25,7 +25,9 @@
 //               other tile's softmax runs (ping-pong).
 //   warps 0-3   softmax of tile A; warps 4-7 softmax of tile B.  One thread
 //               per query row (TMEM lane = row): tcgen05.ld of the 128-score
-//               row, mask, row max, exp2, row sum, bf16 P written back into the
+//               row (its max-reducing form, which also returns the row max of
+//               an unmasked tile), mask and row max on diagonal and edge tiles,
+//               exp2, row sum, bf16 P written back into the
 //               S columns with tcgen05.st in two halves of 64 keys, each
 //               announced on its own barrier so that O += P V starts on the
 //               first half while the second is computed; O rescaled in TMEM

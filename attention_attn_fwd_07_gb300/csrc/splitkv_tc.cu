@@ -12,8 +12,11 @@
 //               an NS-stage shared-memory ring (full/empty mbarriers);
 //   warp 4      MMA issuer: S = Q K^T (SS MMA into TMEM), O += P V (TS MMA,
 //               P read from TMEM), the next S after P V;
-//   warps 0-3   softmax, one thread per row (TMEM lane = row): rows past the
-//               block are masked out; P goes back into the S columns in two
+//   warps 0-3   softmax, one thread per row (TMEM lane = row): the row
+//               maximum comes with the TMEM load on tiles that need no mask;
+//               rows past the block are never written out, so they are left
+//               unmasked, and a warp with no row in the block only keeps pace
+//               with the barriers; P goes back into the S columns in two
 //               halves of 64 keys, each announced on its own barrier; O is
 //               rescaled in TMEM only when the row maximum grew by more than
 //               2^8.  Epilogue: the normalised o (f32) and the natural-log
