@@ -67,6 +67,9 @@ def parse_args():
     ap.add_argument("--decode-profile-gqa8", action="store_true",
                     help="with --decode-profile-batch: the decode with eight query heads per "
                          "K/V head (tensor-core partial kernel)")
+    ap.add_argument("--prefill-d64-profile", action="store_true",
+                    help="run only the d = 64 causal prefill (its own size is small enough "
+                         "for ncu captures) and print its TFLOPS")
     ap.add_argument("--bwd-profile-batch", type=int, default=0,
                     help="run only the backward of the long causal prefill with this batch "
                          "size (smaller cases for ncu captures) and print its TFLOPS")
@@ -382,6 +385,25 @@ def main():
         return max_over_ranks(dist, x)
 
     launches = 0
+
+    if args.prefill_d64_profile:
+        # The d = 64 prefill alone, L2 flushed before each timed launch as in
+        # the full run.
+        wp = W.PREFILL
+        qp, kp, vp = W.make_qkv(wp, device=dev)
+        op = torch.empty_like(qp)
+        lp = torch.empty((wp.B, wp.H, wp.Nq), dtype=torch.float32, device=dev)
+
+        def sp():
+            binding.attn_fwd(qp, kp, vp, wp.causal, wp.scale, o=op, lse=lp, stream=stream)
+
+        for _ in range(args.warmup):
+            sp()
+        scratch = torch.empty((256 << 20) // 4, dtype=torch.float32, device=dev)
+        m, st = event_time_flushed(sp, args.steps, stream, scratch)
+        print(json.dumps({"workload": wp.name, "ms_per_step": m, "launch_ms": st,
+                          "TFLOPS": prefill_flops(wp) / (m / 1e3) / 1e12}), flush=True)
+        return 0
 
     if args.bwd_profile_batch > 0:
         # Backward only, smaller batch: the case the ncu captures run on.
