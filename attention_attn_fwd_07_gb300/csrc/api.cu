@@ -62,7 +62,10 @@ bool encode_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const v
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Checks shared by both forward entry points.
+}  // namespace
+
+// Checks shared by the forward entry points (attn_fwd_ex, attn_fwd_splitkv_ex
+// and attn_fwd_splitkv_noalloc).
 int validate(const attn_params* p) {
   if (p == nullptr) return ATTN_ERR_INVALID;
   if (!p->q || !p->k || !p->v || !p->o || !p->lse) return ATTN_ERR_INVALID;
@@ -90,7 +93,6 @@ int64_t keys_per_split(int64_t Nk, int splits) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-}  // namespace
 }  // namespace attn
 
 using namespace attn;

@@ -7,7 +7,20 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include "attn.h"
+
 namespace attn {
+
+// Argument checks shared by the forward entry points (api.cu): null
+// pointers, sizes, scale, offsets, head dims, size limits and alignment.
+// Returns ATTN_OK or the attn_status to report; makes no CUDA call.
+int validate(const attn_params* p);
+
+// Keys per split-KV range: ceil(Nk / splits) rounded up to a multiple of 128.
+int64_t keys_per_split(int64_t Nk, int splits);
+
+// x rounded up to a multiple of 256 (workspace sub-buffer alignment).
+size_t align256(size_t x);
 
 // Arguments of one prefill (tcgen05) launch, already validated.
 struct FwdArgs {

@@ -17,9 +17,7 @@
 // call (an empty split writes o = 0, lse = -inf).  Calls that overlap on the
 // GPU (different streams, or different host threads on one device) race on
 // the array and give undefined results; serialise them.
-#include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "attn.h"
 #include "internal.cuh"
@@ -29,28 +27,18 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};  // device address of the array, per device
-
-// Once per device, with that device current: translate the array's host-side
-// name into its device address.  The name itself is only a host stand-in and
-// must never be passed to a kernel.
+// With the caller's device current: translate the array's host-side name
+// into its device address on that device.  The name itself is only a host
+// stand-in and must never be passed to a kernel.  The lookup is repeated on
+// every call (a host-side table lookup, no device work), so an address from
+// a context that was since torn down (cudaDeviceReset) is never reused.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-      return ATTN_ERR_CUDA;
-    g_scratch_ptr[dev] = ptr;
-  }
-  *out = g_scratch_ptr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+    return ATTN_ERR_CUDA;
+  *out = ptr;
   return ATTN_OK;
 }
-
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 }  // namespace
 }  // namespace attn
@@ -61,24 +49,29 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
                                         float* lse, int64_t B, int64_t H, int64_t Nq, int64_t Nk,
                                         int64_t d, int causal, float scale, int num_splits,
                                         cudaStream_t stream) {
-  // The same argument rules as attn_fwd_splitkv.
-  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_INVALID;
-  if (!(scale > 0.0f) || !(scale < INFINITY)) return ATTN_ERR_INVALID;
+  // The argument rules of attn_fwd_splitkv: the same checks, from the same
+  // function.
+  attn_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.d = d;
+  p.causal = causal;
+  p.scale = scale;
+  const int rc0 = validate(&p);
+  if (rc0 != ATTN_OK) return rc0;
   if (num_splits < 1 || num_splits > 256) return ATTN_ERR_INVALID;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-  const int64_t kMaxDim = (int64_t{1} << 31) - 1;
-  if (B > kMaxDim || H > kMaxDim || B * H > kMaxDim || Nq > kMaxDim || Nk > kMaxDim)
-    return ATTN_ERR_UNSUPPORTED;
-  const uintptr_t a16 = 15;
-  if ((reinterpret_cast<uintptr_t>(q) & a16) || (reinterpret_cast<uintptr_t>(k) & a16) ||
-      (reinterpret_cast<uintptr_t>(v) & a16) || (reinterpret_cast<uintptr_t>(o) & a16) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3))
-    return ATTN_ERR_ALIGN;
   // Sizes beyond the fixed array are refused before anything is launched.
   const size_t need = attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
   if (need == 0) return ATTN_ERR_UNSUPPORTED;
   if (need > static_cast<size_t>(ATTN_NOALLOC_SCRATCH_BYTES)) return ATTN_ERR_WORKSPACE;
+  const int64_t kMaxDim = (int64_t{1} << 31) - 1;  // grid size limit
   const int64_t BH = B * H;
   const int64_t qb = splitkv_rows_per_cta(Nq);
   if (BH * ((Nq + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;
@@ -101,8 +94,7 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   a.Nq = Nq;
   a.Nk = Nk;
   a.query_offset = 0;
-  const int64_t per = (Nk + num_splits - 1) / num_splits;
-  a.keys_per_split = (per + 127) / 128 * 128;
+  a.keys_per_split = keys_per_split(Nk, num_splits);
   a.d = static_cast<int>(d);
   a.dv = a.d;
   a.splits = num_splits;
@@ -110,6 +102,8 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   a.scale = scale;
   if (default_status_word(&a.status) != cudaSuccess) return ATTN_ERR_CUDA;
   a.timeout_ns = 1000000000ull;
+  // Always the CUDA-core partial kernels (they need no tensor maps), also
+  // for shapes where attn_fwd_splitkv picks the tensor-core partial kernel.
   if (launch_splitkv_partial(a, stream) != cudaSuccess) return ATTN_ERR_CUDA;
   if (launch_combine(a.o_part, a.lse_part, o, lse, BH, Nq, a.d, num_splits, stream) !=
       cudaSuccess)

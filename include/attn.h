@@ -229,12 +229,18 @@ int attn_bwd(const attn_bwd_params* p, void* workspace, size_t workspace_bytes,
  * the device synchronisation cudaMalloc/cudaFree may cause.  The pages have
  * no counterpart to this entry point; it is a deployment convenience.
  *
- * Same arguments, results and rules as attn_fwd_splitkv (query_offset 0).
+ * Same arguments, argument checks and results as attn_fwd_splitkv
+ * (query_offset 0), with one difference in how the partials are computed:
+ * this entry point always runs the CUDA-core partial kernels, also for
+ * shapes where attn_fwd_splitkv switches to the tensor-core partial kernel
+ * (several query rows per head).  There the two agree within the library's
+ * tolerances but may differ in the last bits, and this one is slower.
  * The scratch lives in a fixed device array of ATTN_NOALLOC_SCRATCH_BYTES
  * inside the library; calls whose attn_splitkv_workspace_bytes(...) exceed it
  * return ATTN_ERR_WORKSPACE before launching anything.  Nothing is allocated.
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * Every call looks up the array's device address on the current device (a
+ * host-side lookup; the first one on a device may load the library's module
+ * there), so make the first call on each device before any stream capture.
  * All calls share the array: calls that overlap on the GPU (other streams or
  * host threads on the same device) race and must be serialised by the
  * caller.  The array keeps the previous call's contents; no call needs it

@@ -11,6 +11,8 @@ Tolerances (stated by the build's target and restated here):
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+
 import numpy as np
 import torch
 
@@ -117,3 +119,27 @@ def compare_grad(g_gpu: torch.Tensor, ref: np.ndarray, what: str = "",
     assert fro_err <= GRAD_TOL * fro_ref + GRAD_ATOL * np.sqrt(max(ref.size, 1)), \
         f"{what}: normwise error {stats}"
     return stats
+
+
+def whole_head_grads(oracle, q, k, v, dout, b, h, scale, chunk=512):
+    """fp64 dQ, dK, dV of one (b, h) slice (K/V head = query head) from the
+    oracle, computed in query-row chunks in parallel: rows [r0, r0 + chunk)
+    with query_offset = r0 are that chunk's own causal problem, its dQ rows
+    are final and its dK, dV are that chunk's contributions, which sum over
+    the chunks (dK_j and dV_j are sums over query rows)."""
+    qs, ds = q[b:b + 1, h:h + 1].cpu(), dout[b:b + 1, h:h + 1].cpu()
+    ks, vs = k[b:b + 1, h:h + 1].cpu(), v[b:b + 1, h:h + 1].cpu()
+    Nq = qs.shape[2]
+    starts = list(range(0, Nq, chunk))
+
+    def one(r0):
+        sl = slice(r0, min(Nq, r0 + chunk))
+        return oracle.attention_bwd(qs[:, :, sl], ks, vs, ds[:, :, sl], causal=True,
+                                    scale=scale, query_offset=r0, threads=1)
+
+    with cf.ThreadPoolExecutor(max_workers=min(len(starts), oracle.default_threads())) as ex:
+        parts = list(ex.map(one, starts))
+    rq = np.concatenate([p[0] for p in parts], axis=2)
+    rk = sum(p[1] for p in parts)
+    rv = sum(p[2] for p in parts)
+    return rq, rk, rv

@@ -66,3 +66,24 @@ def test_launch_stats(bench):
     assert st["p10"] == pytest.approx(np.percentile(t, 10))
     assert st["p90"] == pytest.approx(np.percentile(t, 90))
     assert st["p10"] <= st["median"] <= st["p90"]
+
+
+def test_summary_lists_every_line_last(bench):
+    """The closing summary names the headline, each other workload, both
+    decodes (MHA last, with its split count) and carries each line's own
+    roofline fraction."""
+    line = {"config": {"workload": "main"}, "value": 1600.0, "unit": "TFLOPS",
+            "ms_per_step": 0.68, "roofline": {"frac": 0.86},
+            "other_workloads": [
+                {"workload": "d64", "value": 900.0, "metric": "TFLOPS", "ms_per_step": 0.04,
+                 "roofline": {"frac": 0.48}},
+                {"workload": "fp8", "value": 1700.0, "metric": "TFLOPS", "ms_per_step": 0.65,
+                 "roofline": {"frac": 0.69}, "frac_of_bf16_peak": 0.92}],
+            "decode_gqa": {"workload": "gqa", "value": 6900.0, "unit": "GB/s",
+                           "ms_per_step": 0.31, "roofline": {"frac": 1.02}},
+            "decode": {"workload": "mha", "value": 7100.0, "unit": "GB/s", "ms_per_step": 1.2,
+                       "splits": 16, "roofline": {"frac": 1.05}}}
+    s = bench.summary_of(line)
+    assert [e[0] for e in s] == ["main", "d64", "fp8", "gqa", "mha, S=16"]
+    assert [e[3] for e in s] == [0.86, 0.48, 0.69, 1.02, 1.05]
+    assert s[-1][2] == "GB/s" and s[0][2] == "TFLOPS"

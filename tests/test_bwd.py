@@ -6,8 +6,10 @@ fp64 (its row correction from the definition rowsum(P * dP), not from O).
 Cases span several 128-row tiles with ragged tails, causal and not, grouped
 K/V heads, value head dims different from the key head dim, decode-style
 and negative query offsets (rows with no admissible
-key, keys no row sees), and the long causal prefill at full size (dQ on
-sampled row blocks; dK and dV through identities that hold at any size).
+key, keys no row sees), and the full-size workloads: one whole (b, h) slice
+compared element by element on dQ, dK and dV, dQ on sampled row blocks of
+other slices, and dK and dV of every slice through identities that hold at
+any size.
 """
 import numpy as np
 import pytest
@@ -16,7 +18,7 @@ import torch
 import oracle
 from attention_attn_fwd_07_gb300 import binding, build
 from attention_attn_fwd_07_gb300 import inputs as W
-from tests.parity_util import compare_grad, check_guards, guarded
+from tests.parity_util import check_guards, compare_grad, guarded, whole_head_grads
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -121,6 +123,12 @@ def test_bwd_value_dim_gqa_offsets(d, dv):
                    d=d, dv=dv)
 
 
+def check_whole_head(w, q, k, v, dout, dq, dk, dv, b, h):
+    rq, rk, rv = whole_head_grads(oracle, q, k, v, dout, b, h, w.scale)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        compare_grad(g[b:b + 1, h:h + 1], r, f"{w.name}: whole head b={b} h={h} {name}")
+
+
 def test_bwd_rejects_d96():
     w = W.Workload("d96", 1, 1, 64, 64, 96, False, 7)
     q, k, v = (t.to(DEV) for t in W.make_qkv(w))
@@ -132,12 +140,16 @@ def test_bwd_rejects_d96():
 
 
 def test_bwd_d64_prefill_sampled():
-    """B4 H16 N2048 d64 causal (the d = 64 prefill workload): dQ on sampled row
-    blocks against the oracle; dK and dV through the softmax identities."""
+    """B4 H16 N2048 d64 causal (the d = 64 prefill workload): two whole (b, h)
+    slices (the last one among them) element by element, dQ on sampled row
+    blocks of others, dK and dV of every slice through the softmax
+    identities."""
     w = W.PREFILL
     q, k, v = W.make_qkv(w, device=DEV)
     dout = W.make_dout(w, device=DEV)
     dq, dk, dv = run_bwd(q, k, v, dout, True, w.scale)
+    for b, h in ((w.B - 1, w.H - 1), (1, 5)):
+        check_whole_head(w, q, k, v, dout, dq, dk, dv, b, h)
     rng = np.random.default_rng(2600)
     for _ in range(3):
         b, h = int(rng.integers(w.B)), int(rng.integers(w.H))
@@ -164,16 +176,19 @@ def test_bwd_deterministic():
 
 
 def test_bwd_long_prefill_full_size():
-    """B2 H32 N8192 d128 causal (1% of keys x4): dQ on sampled 128-row blocks
-    against the oracle (rows i of head h need only q_i, dO_i and all of K, V,
-    so the oracle runs on the row block with query_offset = its first row);
-    dK and dV through the softmax identities sum_j dS_ij = 0 and
-    sum_j P_ij = 1, which give, per K/V head, sum_j dK_j = 0 and
-    sum_j dV_j = sum_i dO_i over the head's query rows."""
+    """B2 H32 N8192 d128 causal (1% of keys x4): the last (b, h) slice whole,
+    element by element on dQ, dK and dV (a misplaced or swapped key tile
+    fails here); dQ on sampled 128-row blocks of other slices (rows i of head
+    h need only q_i, dO_i and all of K, V, so the oracle runs on the row block
+    with query_offset = its first row); dK and dV of every slice through the
+    softmax identities sum_j dS_ij = 0 and sum_j P_ij = 1, which give, per
+    K/V head, sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i over the head's
+    query rows."""
     w = W.LONG_PREFILL_CAUSAL
     q, k, v = W.make_qkv(w, device=DEV)
     dout = W.make_dout(w, device=DEV)
     dq, dk, dv = run_bwd(q, k, v, dout, True, w.scale)
+    check_whole_head(w, q, k, v, dout, dq, dk, dv, w.B - 1, w.H - 1)
     rng = np.random.default_rng(2500)
     for _ in range(3):
         b, h = int(rng.integers(w.B)), int(rng.integers(w.H))

@@ -64,3 +64,19 @@ def test_e4m3_decoder_matches_the_format_and_torch():
     finite = ~np.isnan(ref)
     assert np.array_equal(np.isnan(ours), ~finite)
     assert np.array_equal(ours[finite], ref[finite])
+
+
+def test_whole_head_chunking_matches_one_call():
+    """The chunked evaluation the full-size backward tests use
+    (parity_util.whole_head_grads) equals one oracle call on a slice small
+    enough to run whole: a check of the tests' own decomposition."""
+    from attention_attn_fwd_07_gb300 import inputs as W
+    from tests.parity_util import whole_head_grads
+    w = W.Workload("chunk check", 1, 2, 300, 300, 64, True, 2700)
+    q, k, v = W.make_qkv(w)
+    dout = W.make_dout(w)
+    rq, rk, rv = oracle.attention_bwd(q[:, 1:2], k[:, 1:2], v[:, 1:2], dout[:, 1:2],
+                                      causal=True, scale=w.scale)
+    cq, ck, cv = whole_head_grads(oracle, q, k, v, dout, 0, 1, w.scale, chunk=64)
+    for a, c in ((rq, cq), (rk, ck), (rv, cv)):
+        assert np.allclose(a, c, rtol=1e-12, atol=1e-12)

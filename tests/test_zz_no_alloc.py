@@ -12,6 +12,11 @@ for the same shape, so they are each compared with the oracle, not
 bitwise), on problems called one after the other, and must refuse a problem
 whose scratch exceeds the array.
 
+The outputs of the two entry points are also compared with each other
+within the same tolerances.  One case fills the array almost to its end (its
+partial log-sum-exps sit in the last few hundred KiB), and the same shape
+with more splits must be refused.
+
 This file is named to be collected last.
 """
 import ctypes
@@ -22,11 +27,21 @@ import torch
 import oracle
 from attention_attn_fwd_07_gb300 import binding, build
 from attention_attn_fwd_07_gb300 import inputs as W
-from tests.parity_util import compare
+from tests.parity_util import LSE_TOL, O_TOL, compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 SCRATCH_BYTES = 32 << 20  # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h
+
+
+def _agree(o_a, lse_a, o_b, lse_b, what):
+    """The two entry points' outputs within the parity tolerances (O as bf16
+    values, LSE as f32; -inf rows must match exactly)."""
+    la, lb = lse_a.double().cpu(), lse_b.double().cpu()
+    assert torch.equal(torch.isneginf(la), torch.isneginf(lb)), f"{what}: masked rows differ"
+    live = ~torch.isneginf(la)
+    assert (la[live] - lb[live]).abs().max().item() <= LSE_TOL, f"{what}: LSE differs"
+    assert (o_a.double() - o_b.double()).abs().max().item() <= O_TOL, f"{what}: O differs"
 
 
 def _entry(lib):
@@ -65,6 +80,36 @@ def test_noalloc_parity_on_consecutive_calls():
         torch.cuda.synchronize()
         compare(o, lse, *ref, f"{w.name} (no-alloc entry point)")
         compare(o_ws, lse_ws, *ref, f"{w.name} (workspace entry point)")
+        _agree(o, lse, o_ws, lse_ws, w.name)
+
+
+def test_noalloc_fills_the_array_to_its_end():
+    """B16 H32 Nq1 d128 with 120 splits needs 31.7 MB of the 32 MiB array, so
+    the partial log-sum-exps occupy its last 240 KiB; with Nk = 2000 only 16
+    of the 120 key ranges hold keys and the rest are empty (o = 0, lse = -inf
+    partials).  Two calls in a row must both match the oracle, and 128 splits
+    at the same shape must be refused."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    f = _entry(binding.load_library())
+    w = W.Workload("near the end of the array", 16, 32, 1, 2000, 128, False, 504)
+    splits = 120
+    need = binding.attn_splitkv_workspace_bytes(w.B, w.H, 1, w.d, splits)
+    assert SCRATCH_BYTES - (1 << 20) < need <= SCRATCH_BYTES
+    q_h, k_h, v_h = W.make_qkv(w)
+    q, k, v = (t.to(DEV) for t in (q_h, k_h, v_h))
+    ref = oracle.attention(q_h, k_h, v_h, causal=False, scale=w.scale)
+    o_ws, lse_ws = binding.attn_fwd_splitkv(q, k, v, False, w.scale, splits)
+    for call in range(2):
+        o = torch.full_like(o_ws, float("nan"))
+        lse = torch.full_like(lse_ws, float("nan"))
+        assert _call(f, q, k, v, o, lse, False, w.scale, splits) == binding.ATTN_OK
+        torch.cuda.synchronize()
+        compare(o, lse, *ref, f"{w.name}, call {call + 1}")
+        _agree(o, lse, o_ws, lse_ws, f"{w.name}, call {call + 1}")
+    assert binding.attn_splitkv_workspace_bytes(w.B, w.H, 1, w.d, 128) > SCRATCH_BYTES
+    assert _call(f, q, k, v, o, lse, False, w.scale, 128) == binding.ATTN_ERR_WORKSPACE
 
 
 def test_noalloc_refuses_scratch_beyond_its_array():
