@@ -64,6 +64,8 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 }  // namespace
 
+bool head_dim_supported(int64_t d) { return d == 64 || d == 96 || d == 128 || d == 256; }
+
 // Checks shared by the forward entry points (attn_fwd_ex, attn_fwd_splitkv_ex
 // and attn_fwd_splitkv_noalloc).
 int validate(const attn_params* p) {
@@ -74,9 +76,13 @@ int validate(const attn_params* p) {
   if (p->query_offset < -kMaxOffset || p->query_offset > kMaxOffset) return ATTN_ERR_INVALID;
   if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
   if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
-  if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(p->d)) return ATTN_ERR_UNSUPPORTED;
   if (p->dv < 0) return ATTN_ERR_INVALID;
-  if (p->dv != 0 && p->dv != 64 && p->dv != 128) return ATTN_ERR_UNSUPPORTED;
+  // A value dim of its own: 64 or 128 with a key dim of 64 or 128; head
+  // dims 96 and 256 take dv = d.
+  if (p->dv != 0 && p->dv != p->d &&
+      ((p->dv != 64 && p->dv != 128) || (p->d != 64 && p->d != 128)))
+    return ATTN_ERR_UNSUPPORTED;
   if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
       p->Nk > kMaxDim)
     return ATTN_ERR_UNSUPPORTED;
@@ -168,7 +174,7 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
 
 extern "C" size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
                                                int num_splits) {
-  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
+  if (B < 1 || H < 1 || Nq < 1 || !head_dim_supported(d)) return 0;
   if (num_splits < 1 || num_splits > kMaxSplits) return 0;
   if (B > kMaxDim || H > kMaxDim || Nq > kMaxDim || B * H > kMaxDim) return 0;
   const unsigned __int128 rows =
@@ -186,7 +192,7 @@ extern "C" int attn_combine(const float* o_part, const float* lse_part, void* o,
   if (!o_part || !lse_part || !o || !lse) return ATTN_ERR_INVALID;
   if (B < 1 || H < 1 || Nq < 1 || num_splits < 1 || num_splits > kMaxSplits)
     return ATTN_ERR_INVALID;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!head_dim_supported(d)) return ATTN_ERR_UNSUPPORTED;
   if (B > kMaxDim || H > kMaxDim || Nq > kMaxDim || B * H > kMaxDim ||
       (B * H * Nq + 7) / 8 > kMaxDim)
     return ATTN_ERR_UNSUPPORTED;
@@ -215,8 +221,11 @@ extern "C" int attn_fwd_splitkv_ex(const attn_params* p, int num_splits, void* w
   // Several rows per K/V head (and dv = d): the tensor-core partial kernel,
   // one CTA per block of up to 128 rows.  dv != d: the register-streaming
   // kernel, one query row per CTA.  Otherwise the CUDA-core kernels.
-  const int64_t tc_min_rows =
-      p->d == 128 ? ATTN_SPLITKV_TC_MIN_ROWS_D128 : ATTN_SPLITKV_TC_MIN_ROWS_D64;
+  // Head dims 96 and 256 always run on the tensor cores (the CUDA-core
+  // kernels' lane layouts cover 64 and 128 only).
+  const int64_t tc_min_rows = p->d == 128  ? ATTN_SPLITKV_TC_MIN_ROWS_D128
+                              : p->d == 64 ? ATTN_SPLITKV_TC_MIN_ROWS_D64
+                                           : 1;
   const bool tc = dv == p->d && rows >= tc_min_rows;
   const int64_t qb = tc ? 128 : (dv != p->d ? 1 : splitkv_rows_per_cta(rows));
   if (p->B * Hkv * ((rows + qb - 1) / qb) * num_splits > kMaxDim) return ATTN_ERR_UNSUPPORTED;

@@ -69,12 +69,16 @@ template <int D, int DV, bool FP8, int NT = 2>
 struct Cfg {
   static_assert(NT == 1 || NT == 2, "one or two query tiles per CTA");
   static constexpr int kQKElem = FP8 ? 1 : 2;               // bytes per Q/K element
-  static constexpr int kQKAtoms = D * kQKElem / 128;        // 128-byte swizzle atoms per Q/K row
-  static constexpr int kVAtoms = DV / 64;                   // ... per V row (bf16)
+  static constexpr int kQKRowBytes = D * kQKElem;
+  // 128-byte swizzle atoms per Q/K row; a partial last atom (d = 96: 192
+  // bytes per row) is zero-filled past the row by the tensor map's bounds.
+  static constexpr int kQKAtoms = (kQKRowBytes + 127) / 128;
+  static constexpr int kQKSteps = kQKRowBytes / 32;         // MMA K steps (32 bytes each)
+  static constexpr int kVAtoms = (DV + 63) / 64;            // ... per V row (bf16)
   static constexpr uint32_t kAtomBytes = 128u * 128u;       // one [128 rows][128 B] box
-  static constexpr uint32_t kQBytes = BM * D * kQKElem;     // one Q tile
-  static constexpr uint32_t kKBytes = BN * D * kQKElem;     // one K tile
-  static constexpr uint32_t kVBytes = BN * DV * 2;          // one V tile
+  static constexpr uint32_t kQBytes = kQKAtoms * kAtomBytes;  // one Q tile (BM rows)
+  static constexpr uint32_t kKBytes = kQKAtoms * kAtomBytes;  // one K tile (BN rows)
+  static constexpr uint32_t kVBytes = kVAtoms * kAtomBytes;   // one V tile
   static constexpr uint32_t kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // one ring stage
   static constexpr int kStages =
       NT == 2 ? ((kKVBytes >= 32768u) ? 4 : 8) : ((kKVBytes >= 32768u) ? 2 : 5);
@@ -94,18 +98,25 @@ struct Cfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + 1 KiB alignment slack
-  static constexpr uint32_t kColS = 0;        // + 128 * tile
-  static constexpr uint32_t kColO = 128 * NT;  // + DV * tile
-  static constexpr uint32_t kTmemCols = NT == 2 ? 512 : 256;
+  static constexpr uint32_t kColS = 0;          // + 128 * tile
+  static constexpr uint32_t kColO = 128 * NT;   // + kOStride * tile
+  static constexpr uint32_t kOStride = (DV + 63) / 64 * 64;  // O columns per tile, 64-aligned
+  static constexpr uint32_t kTmemCols = (kColO + NT * kOStride) <= 256 ? 256 : 512;
   static constexpr int kThreads = threads_for(NT);
   static constexpr int kWarpMma = 4 * NT;
   static constexpr int kWarpLoad = 4 * NT + 1;
   static constexpr uint32_t kIdescQK = FP8 ? idesc_e4m3_f32(BM, BN) : idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, DV, 1);
+  static_assert(kQKSteps == 4 || kQKSteps == 6 || kQKSteps == 8 || kQKSteps == 16,
+                "Q/K rows of 64, 96, 128 or 256 bf16 (128 e4m3)");
+  static_assert(DV % 32 == 0 && DV <= 256, "value rows of 32-column multiples up to 256");
+  static_assert(kColO + NT * kOStride <= 512, "tensor memory budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(NT == 1 || kSmemBytes > 232448 / 2,
-                "one two-tile CTA per SM keeps the 512-column TMEM allocation uncontended");
-  static_assert(NT == 2 || 2 * (kSmemBytes + 1024) <= 232448,
+  // A CTA that takes all 512 TMEM columns must be alone on its SM (its
+  // shared memory keeps a second one out); 256-column CTAs pair up.
+  static_assert(kTmemCols == 256 || kSmemBytes > 232448 / 2,
+                "a 512-column CTA keeps the SM's tensor memory to itself");
+  static_assert(NT == 2 || kTmemCols == 512 || 2 * (kSmemBytes + 1024) <= 232448,
                 "two one-tile CTAs per SM (256 TMEM columns each)");
 };
 
@@ -300,17 +311,25 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
         const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes, 16, 1024);
         const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, 16, 1024);
         // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
-        if constexpr (FP8)
+        if constexpr (FP8) {
           mma_ss_f8_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
-        else if constexpr (D == 128)
+        } else if constexpr (C::kQKSteps == 16) {
+          // Two runs of eight steps; the second starts two atoms (32 KB =
+          // 2048 descriptor units) further and accumulates.
           mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
-        else
+          mma_ss_run8_w(d_tmem, a + 2048, b + 2048, C::kIdescQK, 1u);
+        } else if constexpr (C::kQKSteps == 8) {
+          mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
+        } else if constexpr (C::kQKSteps == 6) {
+          mma_ss_run6_w(d_tmem, a, b, C::kIdescQK, 0u);
+        } else {
           mma_ss_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
+        }
       };
       // O_X += P_X V over keys 64 h .. 64 h + 63 (four K steps of 16 keys;
       // P's bf16 pairs for those keys sit in columns 32 h .. 32 h + 31).
       auto pv_half = [&](int x, int stage, int h, bool acc) {
-        const uint32_t d_tmem = tmem + C::kColO + DV * x;
+        const uint32_t d_tmem = tmem + C::kColO + C::kOStride * x;
         const uint32_t p_tmem = tmem + C::kColS + 128 * x + 32 * h;
         const uint64_t b =
             sdesc_sw128(sKV + stage * C::kKVBytes + h * 64 * 128, C::kAtomBytes, 1024);
@@ -383,7 +402,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     const int64_t row = row0 + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS + 128 * x;
-    const uint32_t tO = tmem + lane_off + C::kColO + DV * x;
+    const uint32_t tO = tmem + lane_off + C::kColO + C::kOStride * x;
     const int n = ntile[x];
     // Last admissible key of this row and of the tile's first row.
     const int64_t lim = p.causal ? min(p.Nk - 1, row + p.qoff) : p.Nk - 1;
@@ -562,6 +581,12 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
 
 cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                                const CUtensorMap& tv, cudaStream_t stream) {
+  // Head dims 96 and 256 (value dim equal): 96 runs the two-tile layout of
+  // 128 (Q/K rows padded to two atoms by the tensor map's zero fill, six K
+  // steps); 256 takes one query tile per CTA with S and a 256-column O in
+  // all 512 TMEM columns and a two-stage ring of 64 KB tiles.
+  if (a.d == 96) return launch<96, 96, false>(a, tq, tk, tv, stream);
+  if (a.d == 256) return launch<256, 256, false, 1>(a, tq, tk, tv, stream);
   if (a.fp8_qk)
     return a.dv == 64 ? launch<128, 64, true>(a, tq, tk, tv, stream)
                       : launch<128, 128, true>(a, tq, tk, tv, stream);

@@ -16,6 +16,9 @@ namespace attn {
 // Returns ATTN_OK or the attn_status to report; makes no CUDA call.
 int validate(const attn_params* p);
 
+// Head dims the forward entry points take: 64, 96, 128 and 256.
+bool head_dim_supported(int64_t d);
+
 // Keys per split-KV range: ceil(Nk / splits) rounded up to a multiple of 128.
 int64_t keys_per_split(int64_t Nk, int splits);
 

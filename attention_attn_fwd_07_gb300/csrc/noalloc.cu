@@ -66,6 +66,8 @@ extern "C" int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void
   p.scale = scale;
   const int rc0 = validate(&p);
   if (rc0 != ATTN_OK) return rc0;
+  // The CUDA-core partial kernels cover head dims 64 and 128.
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (num_splits < 1 || num_splits > 256) return ATTN_ERR_INVALID;
   // Sizes beyond the fixed array are refused before anything is launched.
   const size_t need = attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits);

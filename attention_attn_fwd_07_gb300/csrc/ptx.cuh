@@ -146,6 +146,16 @@ __device__ __forceinline__ void mma_ss_run8_w(uint32_t d_tmem, uint64_t a_desc, 
                ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                : "memory");
 }
+// Six K steps: four in the first atom, two in the second (bf16 with 96
+// values per row; the rest of the second atom is never read).
+__device__ __forceinline__ void mma_ss_run6_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(ATTN_MMA_RUN_HEAD("f16") ATTN_MMA_SS_STEP("f16", 2) ATTN_MMA_SS_STEP("f16", 4)
+                   ATTN_MMA_SS_STEP("f16", 6) ATTN_MMA_SS_STEP("f16", 1024)
+                       ATTN_MMA_SS_STEP("f16", 1026) "}"
+               ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+               : "memory");
+}
 // Four K steps inside one atom (bf16 with 64 values per row).
 __device__ __forceinline__ void mma_ss_run4_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {

@@ -660,6 +660,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
+  static_assert(E == 2 || E == 3 || E == 4 || E == 8, "head dims 64, 96, 128, 256");
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
@@ -678,12 +679,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 #pragma unroll 8
       for (int j = 0; j < n; ++j) {
         const float w = __shfl_sync(0xffffffffu, w_lane, j);
-        if constexpr (E == 4) {
-          const float4 x = *reinterpret_cast<const float4*>(op + j * stride);
-          acc[0] = fmaf(w, x.x, acc[0]);
-          acc[1] = fmaf(w, x.y, acc[1]);
-          acc[2] = fmaf(w, x.z, acc[2]);
-          acc[3] = fmaf(w, x.w, acc[3]);
+        if constexpr (E == 4 || E == 8) {
+#pragma unroll
+          for (int c = 0; c < E / 4; ++c) {
+            const float4 x = *reinterpret_cast<const float4*>(op + j * stride + 4 * c);
+            acc[4 * c + 0] = fmaf(w, x.x, acc[4 * c + 0]);
+            acc[4 * c + 1] = fmaf(w, x.y, acc[4 * c + 1]);
+            acc[4 * c + 2] = fmaf(w, x.z, acc[4 * c + 2]);
+            acc[4 * c + 3] = fmaf(w, x.w, acc[4 * c + 3]);
+          }
+        } else if constexpr (E == 3) {
+#pragma unroll
+          for (int c = 0; c < 3; ++c) acc[c] = fmaf(w, op[j * stride + c], acc[c]);
         } else {
           const float2 x = *reinterpret_cast<const float2*>(op + j * stride);
           acc[0] = fmaf(w, x.x, acc[0]);
@@ -697,11 +704,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const bool empty = !(W > 0.0f);
   const float inv = empty ? 0.0f : 1.0f / W;
   uint16_t* dst = o + row * D + lane * E;
-  if constexpr (E == 4) {
+  if constexpr (E == 8) {
+    uint4 pk;
+    pk.x = empty ? 0u : pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    pk.y = empty ? 0u : pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    pk.z = empty ? 0u : pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    pk.w = empty ? 0u : pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(dst) = pk;
+  } else if constexpr (E == 4) {
     uint2 pk;
     pk.x = empty ? 0u : pack_bf16x2(acc[0] * inv, acc[1] * inv);
     pk.y = empty ? 0u : pack_bf16x2(acc[2] * inv, acc[3] * inv);
     *reinterpret_cast<uint2*>(dst) = pk;
+  } else if constexpr (E == 3) {
+    // Three values per lane (d = 96): 6-byte rows slices, 2-byte stores.
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      const uint32_t b = empty ? 0u : pack_bf16x2(acc[c] * inv, 0.0f);
+      dst[c] = static_cast<uint16_t>(b & 0xFFFFu);
+    }
   } else {
     *reinterpret_cast<uint32_t*>(dst) = empty ? 0u : pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
@@ -797,12 +818,13 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, void* o, 
                            int64_t BH, int64_t Nq, int d, int splits, cudaStream_t stream) {
   const int64_t rows = BH * Nq;
   const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-  if (d == 64)
-    combine_kernel<64><<<blocks, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o),
-                                                    lse, rows, Nq, splits);
-  else
-    combine_kernel<128><<<blocks, 256, 0, stream>>>(o_part, lse_part, static_cast<uint16_t*>(o),
-                                                     lse, rows, Nq, splits);
+  uint16_t* out = static_cast<uint16_t*>(o);
+  switch (d) {
+    case 64: combine_kernel<64><<<blocks, 256, 0, stream>>>(o_part, lse_part, out, lse, rows, Nq, splits); break;
+    case 96: combine_kernel<96><<<blocks, 256, 0, stream>>>(o_part, lse_part, out, lse, rows, Nq, splits); break;
+    case 256: combine_kernel<256><<<blocks, 256, 0, stream>>>(o_part, lse_part, out, lse, rows, Nq, splits); break;
+    default: combine_kernel<128><<<blocks, 256, 0, stream>>>(o_part, lse_part, out, lse, rows, Nq, splits); break;
+  }
   return cudaGetLastError();
 }
 

@@ -24,7 +24,8 @@
 //               admissible key in the split.
 // TMEM: S [0,128), O [128,128+d), 256 columns, and a 2-stage ring (4 at
 // d = 64) so that two CTAs share an SM: their independent S -> softmax ->
-// P V chains cover each other's latency.  The tensor core is far from busy
+// P V chains cover each other's latency (d = 256: 512 columns and 192 KB of
+// shared memory, one CTA per SM).  The tensor core is far from busy
 // (a few real rows per MMA); the point is to keep the CUDA cores out of the
 // dot products, so that any number of rows per K/V head streams K and V at
 // memory speed.  Every mbarrier wait is bounded (status word, clean exit).
@@ -48,10 +49,15 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
 struct TcCfg {
-  static constexpr int kAtoms = D / 64;                    // 128-byte swizzle atoms per row
+  // 128-byte swizzle atoms per row; d = 96 leaves half of its second atom to
+  // the tensor map's zero fill.
+  static constexpr int kAtoms = (D + 63) / 64;
+  static constexpr int kQKSteps = D / 16;                  // MMA K steps of 16 bf16
   static constexpr uint32_t kAtomBytes = 128u * 128u;
-  static constexpr uint32_t kTileBytes = BM * D * 2;       // Q block, K tile, V tile
-  static constexpr int kStages = D == 128 ? 2 : 4;  // two CTAs per SM
+  static constexpr uint32_t kTileBytes = kAtoms * kAtomBytes;  // Q block, K tile, V tile
+  // Two CTAs per SM (256 TMEM columns each) up to d = 128; d = 256 needs
+  // 384 columns and 192 KB of shared memory, one CTA per SM.
+  static constexpr int kStages = D == 64 ? 4 : 2;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = kTileBytes;
   static constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
@@ -68,10 +74,15 @@ struct TcCfg {
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  static constexpr uint32_t kColS = 0, kColO = 128, kTmemCols = 256;
+  static constexpr uint32_t kColS = 0, kColO = 128;
+  static constexpr uint32_t kTmemCols = 128 + D <= 256 ? 256 : 512;
   static constexpr uint32_t kIdescQK = idesc_bf16_f32(BM, BN, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 1);
+  static_assert(D == 64 || D == 96 || D == 128 || D == 256, "head dims 64, 96, 128, 256");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kTmemCols == 256 || kSmemBytes > 232448 / 2,
+                "a 512-column CTA keeps the SM's tensor memory to itself");
+  static_assert(kTmemCols == 512 || 2 * (kSmemBytes + 1024) <= 232448, "two CTAs per SM");
 };
 
 struct TcParams {
@@ -214,10 +225,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       auto qk = [&](int stage) {
         const uint64_t a = sdesc_sw128(sQ, 16, 1024);
         const uint64_t bd = sdesc_sw128(sKV + stage * C::kTileBytes, 16, 1024);
-        if constexpr (D == 128)
+        if constexpr (C::kQKSteps == 16) {
           mma_ss_run8_w(tmem + C::kColS, a, bd, C::kIdescQK, 0u);
-        else
+          mma_ss_run8_w(tmem + C::kColS, a + 2048, bd + 2048, C::kIdescQK, 1u);  // atoms 2, 3
+        } else if constexpr (C::kQKSteps == 8) {
+          mma_ss_run8_w(tmem + C::kColS, a, bd, C::kIdescQK, 0u);
+        } else if constexpr (C::kQKSteps == 6) {
+          mma_ss_run6_w(tmem + C::kColS, a, bd, C::kIdescQK, 0u);
+        } else {
           mma_ss_run4_w(tmem + C::kColS, a, bd, C::kIdescQK, 0u);
+        }
         mma_commit_w(bar(C::kBarS));
       };
       // O += P V over keys 64 h .. 64 h + 63 (P's bf16 pairs in columns 32 h ..).
@@ -441,7 +458,12 @@ cudaError_t launch_tc(const SplitArgs& a, const CUtensorMap& tq, const CUtensorM
 cudaError_t launch_splitkv_partial_tc(const SplitArgs& a, const CUtensorMap& tq,
                                       const CUtensorMap& tk, const CUtensorMap& tv,
                                       cudaStream_t stream) {
-  return a.d == 64 ? launch_tc<64>(a, tq, tk, tv, stream) : launch_tc<128>(a, tq, tk, tv, stream);
+  switch (a.d) {
+    case 64: return launch_tc<64>(a, tq, tk, tv, stream);
+    case 96: return launch_tc<96>(a, tq, tk, tv, stream);
+    case 256: return launch_tc<256>(a, tq, tk, tv, stream);
+    default: return launch_tc<128>(a, tq, tk, tv, stream);
+  }
 }
 
 }  // namespace attn

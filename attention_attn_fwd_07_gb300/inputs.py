@@ -66,6 +66,17 @@ DECODE_GQA8 = Workload("decode GQA B16 H32 Hkv4 Nq1 Nk32768 d128 split-KV", 16, 
                        128, False, 1006, splits=(4, 8, 16), Hkv=4)
 
 
+# Head dims beyond 64 and 128 (several head dimensions, GPU Engineering
+# section 22.5's lab): long causal prefills with the long prefill's bytes
+# per (b, h) scaled by d, and a decode at d = 256.
+LONG_PREFILL_D96 = Workload("long prefill B2 H32 N8192 d96 causal", 2, 32, 8192, 8192, 96, True,
+                            1008)
+LONG_PREFILL_D256 = Workload("long prefill B2 H16 N8192 d256 causal", 2, 16, 8192, 8192, 256,
+                             True, 1009)
+DECODE_D256 = Workload("decode B8 H16 Nq1 Nk32768 d256 split-KV", 8, 16, 1, 32768, 256, False,
+                       1010, splits=(8, 16, 32))
+
+
 def ragged(n: int, causal: bool) -> Workload:
     """Ragged-length edge case: B=3, H=4, d=64, Nq=Nk=n (seed 1001 + n)."""
     tag = "causal" if causal else "non-causal"

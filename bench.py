@@ -529,8 +529,9 @@ def main():
     decode_gqa = None
     if not args.quick:
         # ---- the other prefill workloads
-        for wo in (W.LONG_PREFILL_NONCAUSAL, W.PREFILL):
-            if wo.Nq == w.Nq and wo.d == w.d:
+        for wo in (W.LONG_PREFILL_NONCAUSAL, W.PREFILL, W.LONG_PREFILL_D96,
+                   W.LONG_PREFILL_D256):
+            if wo.Nq == w.Nq and wo.d == w.d and wo.H == w.H:
                 qq, kk, vv, oo, ll = q, k, v, o, lse
             else:
                 qq, kk, vv = (t.to(dev) for t in W.make_qkv(wo))
@@ -663,6 +664,7 @@ def main():
         decode = run_decode(W.DECODE)
         decode_gqa = run_decode(W.DECODE_GQA)
         others.append(run_decode(W.DECODE_GQA8))
+        others.append(run_decode(W.DECODE_D256))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

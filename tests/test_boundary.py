@@ -63,8 +63,10 @@ def call_fwd(lib, q=A16, k=A16, v=A16, o=A16, lse=A16, B=1, H=1, Nq=8, Nk=8, d=6
     (dict(scale=float("inf")), binding.ATTN_ERR_INVALID),
     (dict(scale=0.0), binding.ATTN_ERR_INVALID),
     (dict(scale=-0.5), binding.ATTN_ERR_INVALID),
-    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED),
-    (dict(d=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=32), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=80), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=192), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=512), binding.ATTN_ERR_UNSUPPORTED),
     (dict(Nq=1 << 31), binding.ATTN_ERR_UNSUPPORTED),
     (dict(B=1 << 20, H=1 << 12), binding.ATTN_ERR_UNSUPPORTED),
     (dict(q=MIS), binding.ATTN_ERR_ALIGN),
@@ -101,6 +103,8 @@ def test_grouped_heads_must_divide(lib, H, Hkv):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(qk_dtype=1, q_descale=1.0, k_descale=1.0, d=64), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(qk_dtype=1, q_descale=1.0, k_descale=1.0, d=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(qk_dtype=1, q_descale=1.0, k_descale=1.0, d=256), binding.ATTN_ERR_UNSUPPORTED),
     (dict(qk_dtype=1, q_descale=0.0, k_descale=1.0, d=128), binding.ATTN_ERR_INVALID),
     (dict(qk_dtype=1, q_descale=1.0, k_descale=float("nan"), d=128), binding.ATTN_ERR_INVALID),
     (dict(qk_dtype=2, q_descale=1.0, k_descale=1.0, d=128), binding.ATTN_ERR_INVALID),
@@ -119,8 +123,10 @@ def test_workspace_bytes(lib):
     assert f(16, 32, 1, 128, 64) == math.ceil(rows * 128 * 4 / 256) * 256 + rows * 4
     rows = 3 * 4 * 3 * 1003
     assert f(3, 4, 1003, 64, 3) == math.ceil(rows * 64 * 4 / 256) * 256 + rows * 4
-    for bad in [(0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, 0), (1, 1, 1, 64, 257),
-                (1, 1, 0, 64, 1)]:
+    for d in (96, 256):  # every head dim the forward takes has a workspace size
+        assert f(2, 3, 5, d, 7) == math.ceil(2 * 3 * 7 * 5 * d * 4 / 256) * 256 + 2 * 3 * 7 * 5 * 4
+    for bad in [(0, 1, 1, 64, 1), (1, 1, 1, 80, 1), (1, 1, 1, 32, 1), (1, 1, 1, 64, 0),
+                (1, 1, 1, 64, 257), (1, 1, 0, 64, 1)]:
         assert f(*bad) == 0
 
 
@@ -138,11 +144,32 @@ def test_splitkv_rejects(lib):
     assert sk(*bad, 4, A16, need, None) == binding.ATTN_ERR_UNSUPPORTED
 
 
+def test_noalloc_rejects(lib):
+    """The allocation-free split-KV entry point shares the workspace entry
+    point's checks, refuses the head dims its CUDA-core kernels do not cover
+    and problems whose scratch exceeds its fixed array -- all before any CUDA
+    call."""
+    f = lib.attn_fwd_splitkv_noalloc
+    f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 5 + [ctypes.c_int, ctypes.c_float,
+                                                                 ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    args = [A16, A16, A16, A16, A16, 1, 1, 8, 8]
+    assert f(*args, 64, 0, 0.125, 0, None) == binding.ATTN_ERR_INVALID
+    assert f(*args, 64, 0, float("nan"), 4, None) == binding.ATTN_ERR_INVALID
+    assert f(MIS, *args[1:], 64, 0, 0.125, 4, None) == binding.ATTN_ERR_ALIGN
+    for d in (96, 256):
+        assert f(*args, d, 0, 0.125, 4, None) == binding.ATTN_ERR_UNSUPPORTED
+    assert f(*args, 80, 0, 0.125, 4, None) == binding.ATTN_ERR_UNSUPPORTED
+    big = [A16, A16, A16, A16, A16, 16, 32, 1, 4096]
+    assert f(*big, 128, 0, 0.125, 128, None) == binding.ATTN_ERR_WORKSPACE
+
+
 def test_combine_rejects(lib):
     c = lib.attn_combine
     assert c(0, A16, A16, A16, 1, 1, 1, 64, 4, None) == binding.ATTN_ERR_INVALID
     assert c(A16, A16, A16, A16, 1, 1, 1, 64, 0, None) == binding.ATTN_ERR_INVALID
     assert c(A16, A16, A16, A16, 1, 1, 1, 32, 4, None) == binding.ATTN_ERR_UNSUPPORTED
+    assert c(A16, A16, A16, A16, 1, 1, 1, 80, 4, None) == binding.ATTN_ERR_UNSUPPORTED
     assert c(MIS, A16, A16, A16, 1, 1, 1, 64, 4, None) == binding.ATTN_ERR_ALIGN
 
 
@@ -208,6 +235,9 @@ def test_bwd_workspace_bytes(lib):
     (dict(dv=-1), binding.ATTN_ERR_INVALID),
     (dict(dv=96), binding.ATTN_ERR_UNSUPPORTED),
     (dict(dv=256), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96, dv=64), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256, dv=128), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=128, dv=96), binding.ATTN_ERR_UNSUPPORTED),
     (dict(d=64, dv=128, qk_dtype=1, q_descale=1.0, k_descale=1.0), binding.ATTN_ERR_UNSUPPORTED),
 ])
 def test_value_dim_rejects(lib, kw, code):

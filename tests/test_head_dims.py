@@ -1,0 +1,189 @@
+"""GPU parity of head dims 96 and 256 against the fp64 oracle.
+
+GPU Engineering's lab (section 22.5) asks for several head dimensions; the
+forward entry points take d in {64, 96, 128, 256}.  Head dim 96 runs the
+two-tile prefill layout with Q/K rows of one and a half swizzle atoms (the
+tensor map zero-fills the rest, six MMA K steps) and a 96-column P V; head
+dim 256 runs one query tile per CTA with a 256-column O.  Split-KV at these
+dims always uses the tensor-core partial kernel.  Cases: the ragged lengths
+(1, 31, 32, 33, 1003) causal and not, multi-tile tails, grouped K/V heads,
+query offsets (decode-style subproblems and fully masked rows), split-KV
+with several split counts, the combine, full-size prefills (whole heads,
+each element also within the bf16-P bound) and the refusals that remain.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_attn_fwd_07_gb300 import binding, build
+from attention_attn_fwd_07_gb300 import inputs as W
+from tests.parity_util import compare
+from tests.test_parity import _sampled, oracle_full, run_fwd, run_split, to_dev
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+DIMS = (96, 256)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    build.build()
+    binding.load_library()
+    yield
+    assert binding.attn_get_device_status() == 0, "a kernel reported a wait timeout"
+
+
+def _wl(name, B, H, Nq, Nk, d, causal, seed, Hkv=0):
+    return W.Workload(f"{name} d{d}", B, H, Nq, Nk, d, causal, seed, Hkv=Hkv)
+
+
+@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", W.RAGGED_LENGTHS)
+def test_ragged_fwd(d, n, causal):
+    w = _wl(f"ragged N{n}", 3, 4, n, n, d, causal, 3000 + n + d)
+    q, k, v = W.make_qkv(w)
+    o, lse = run_fwd(*to_dev(q, k, v), causal, w.scale)
+    compare(o, lse, *oracle_full(q, k, v, causal, w.scale), w.name)
+
+
+@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_tile_ragged_tail_and_groups(d, causal):
+    """Several query blocks and key tiles with a ragged tail; then the same
+    shape with two query heads per K/V head."""
+    w = _wl("multi-tile", 2, 4, 700, 700, d, causal, 3100 + d)
+    q, k, v = W.make_qkv(w)
+    o, lse = run_fwd(*to_dev(q, k, v), causal, w.scale)
+    compare(o, lse, *oracle_full(q, k, v, causal, w.scale), w.name)
+    wg = _wl("multi-tile GQA", 2, 4, 700, 700, d, causal, 3200 + d, Hkv=2)
+    q, k, v = W.make_qkv(wg)
+    o, lse = run_fwd(*to_dev(q, k, v), causal, wg.scale)
+    compare(o, lse, *oracle_full(q, k, v, causal, wg.scale), wg.name)
+
+
+@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("Nq,Nk,off", [(300, 1000, 700), (1, 1000, 999), (129, 520, 3)])
+def test_query_offset(d, Nq, Nk, off):
+    w = _wl("offset", 1, 2, Nq, Nk, d, True, 3300 + Nq + d)
+    q, k, v = W.make_qkv(w)
+    ref = oracle_full(q, k, v, True, w.scale, off)
+    o, lse = run_fwd(*to_dev(q, k, v), True, w.scale, query_offset=off)
+    compare(o, lse, *ref, f"{w.name} fwd Nq={Nq} Nk={Nk} off={off}")
+    for S in (1, 5):
+        o, lse = run_split(*to_dev(q, k, v), True, w.scale, S, query_offset=off)
+        compare(o, lse, *ref, f"{w.name} split S={S} off={off}")
+
+
+@pytest.mark.parametrize("d", DIMS)
+def test_fully_masked_rows(d):
+    w = _wl("masked", 2, 2, 333, 333, d, True, 3400 + d)
+    q, k, v = W.make_qkv(w)
+    off = -130
+    flags = binding.ATTN_FLAG_ALLOW_NEG_OFFSET
+    ref = oracle_full(q, k, v, True, w.scale, off)
+    o, lse = run_fwd(*to_dev(q, k, v), True, w.scale, query_offset=off, flags=flags)
+    st = compare(o, lse, *ref, f"{w.name} fwd")
+    assert st["masked_rows"] == 2 * 2 * 130
+    for S in (1, 3, 16):
+        o, lse = run_split(*to_dev(q, k, v), True, w.scale, S, query_offset=off, flags=flags)
+        compare(o, lse, *ref, f"{w.name} split S={S}")
+
+
+@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("S", W.RAGGED_SPLITS)
+@pytest.mark.parametrize("n", [1, 33, 1003])
+def test_ragged_splitkv(d, n, S):
+    w = _wl(f"ragged split N{n}", 3, 4, n, n, d, True, 3500 + n + d)
+    q, k, v = W.make_qkv(w)
+    o, lse = run_split(*to_dev(q, k, v), True, w.scale, S)
+    compare(o, lse, *oracle_full(q, k, v, True, w.scale), f"{w.name} S={S}")
+
+
+@pytest.mark.parametrize("d", DIMS)
+@pytest.mark.parametrize("Hkv", [8, 2, 1])
+def test_decode_splitkv(d, Hkv):
+    """One query row per head (Hkv = H: one row per K/V head), and grouped
+    heads (four and eight rows per K/V head), non-causal decode."""
+    w = _wl(f"decode Hkv{Hkv}", 2, 8, 1, 3000, d, False, 3600 + Hkv + d, Hkv=Hkv)
+    q, k, v = W.make_qkv(w)
+    ref = oracle_full(q, k, v, False, w.scale)
+    for S in (4, 16):
+        o, lse = run_split(*to_dev(q, k, v), False, w.scale, S)
+        compare(o, lse, *ref, f"{w.name} S={S}")
+
+
+@pytest.mark.parametrize("d", DIMS)
+def test_combine_alone(d):
+    """attn_combine fed the oracle's own per-range partials (one range
+    empty) gives the oracle's full result."""
+    B, H, Nq, Nk, S, L = 2, 3, 5, 700, 4, 256
+    w = _wl("combine", B, H, Nq, Nk, d, False, 3700 + d)
+    q, k, v = W.make_qkv(w)
+    o_part = np.zeros((B, H, S, Nq, d))
+    lse_part = np.full((B, H, S, Nq), -np.inf)
+    for s in range(S):
+        lo, hi = s * L, min((s + 1) * L, Nk)
+        if lo >= hi:
+            continue
+        o_s, l_s = oracle.attention(q, k, v, causal=False, scale=w.scale, key_range=(lo, hi))
+        o_part[:, :, s], lse_part[:, :, s] = o_s, l_s
+    o, lse = binding.attn_combine(torch.tensor(o_part, dtype=torch.float32, device=DEV),
+                                  torch.tensor(lse_part, dtype=torch.float32, device=DEV), S)
+    torch.cuda.synchronize()
+    compare(o, lse, *oracle_full(q, k, v, False, w.scale), w.name)
+
+
+@pytest.mark.parametrize("wl", [W.LONG_PREFILL_D96, W.LONG_PREFILL_D256], ids=["d96", "d256"])
+def test_long_prefill_full_size(wl):
+    """The last (b, h) slice whole, each element also within the bf16-P
+    bound, plus edge and random rows of other slices."""
+    q, k, v = W.make_qkv(wl)
+    o, lse = run_fwd(*to_dev(q, k, v), wl.causal, wl.scale)
+    BH = wl.B * wl.H
+    rows = np.arange((BH - 1) * wl.Nq, BH * wl.Nq, dtype=np.int64)
+    _sampled(wl, o, lse, q, k, v, rows, bound=True)
+    rng = np.random.default_rng(wl.d)
+    heads = sorted(set(rng.choice(BH - 1, size=4, replace=False).tolist()) | {0})
+    edge = [0, 1, 127, 128, 255, 256, wl.Nq // 2, wl.Nq - 1]
+    rows = np.array([h * wl.Nq + i for h in heads
+                     for i in sorted(set(edge) | set(rng.integers(0, wl.Nq, 12).tolist()))],
+                    dtype=np.int64)
+    _sampled(wl, o, lse, q, k, v, rows)
+
+
+def test_decode_d256_full_size():
+    """The d = 256 decode bench workload (B8 H16 Nk32768), sampled heads."""
+    w = W.DECODE_D256
+    q, k, v = W.make_qkv(w, device=DEV)
+    heads = sorted(set(np.random.default_rng(5).choice(w.B * w.H, 10, replace=False).tolist())
+                   | {0, w.B * w.H - 1})
+    idx = torch.as_tensor(heads, device=DEV)
+    qh, kh, vh = (t.reshape(w.B * w.H, -1, w.d)[idx].unsqueeze(0).cpu() for t in (q, k, v))
+    o_ref, lse_ref = oracle.attention(qh, kh, vh, causal=False, scale=w.scale)
+    for S in w.splits:
+        o, lse = run_split(q, k, v, False, w.scale, S)
+        compare(o.reshape(w.B * w.H, 1, w.d)[idx].unsqueeze(0),
+                lse.reshape(w.B * w.H, 1)[idx].unsqueeze(0), o_ref, lse_ref,
+                f"{w.name} S={S}")
+
+
+def test_remaining_refusals():
+    """Head dims outside {64, 96, 128, 256}, value dims of their own at 96
+    and 256, FP8 at 96/256 and the backward at 96/256 stay unsupported."""
+    for d in (32, 80, 192):
+        w = W.Workload("bad", 1, 1, 64, 64, d, False, 7)
+        q, k, v = (t.to(DEV) for t in W.make_qkv(w))
+        with pytest.raises(binding.AttnError) as e:
+            binding.attn_fwd(q, k, v, False, w.scale)
+        assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
+    for d in DIMS:
+        w = W.Workload("bwd", 1, 1, 64, 64, d, False, 7)
+        q, k, v = (t.to(DEV) for t in W.make_qkv(w))
+        o, lse = binding.attn_fwd(q, k, v, False, w.scale)
+        with pytest.raises(binding.AttnError) as e:
+            binding.attn_bwd(q, k, v, o, lse, torch.zeros_like(q), False, w.scale)
+        assert e.value.status == binding.ATTN_ERR_UNSUPPORTED

@@ -298,13 +298,20 @@ def test_deterministic():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _sampled(w, o, lse, q, k, v, rows, query_offset=0):
+def _sampled(w, o, lse, q, k, v, rows, query_offset=0, bound=False):
+    """Compare the given flattened rows; with ``bound``, also against the
+    per-element bound of the bf16 P staging (the oracle run once more with
+    |V|)."""
     o_ref, lse_ref = oracle.attention(q, k, v, causal=w.causal, scale=w.scale,
                                       query_offset=query_offset, rows=rows)
-    d = q.shape[-1]
-    o_s = o.reshape(-1, d)[torch.as_tensor(rows, device=o.device)]
+    absv = None
+    if bound:
+        absv, _ = oracle.attention(q, k, v.abs(), causal=w.causal, scale=w.scale,
+                                   query_offset=query_offset, rows=rows)
+    dv = v.shape[-1]
+    o_s = o.reshape(-1, dv)[torch.as_tensor(rows, device=o.device)]
     l_s = lse.reshape(-1)[torch.as_tensor(rows, device=lse.device)]
-    return compare(o_s, l_s, o_ref, lse_ref, w.name)
+    return compare(o_s, l_s, o_ref, lse_ref, w.name, absv_ref=absv)
 
 
 def test_prefill_full_size():
@@ -320,14 +327,15 @@ def test_prefill_full_size():
                          ids=["causal", "noncausal"])
 def test_long_prefill_full_size(wl):
     """Two whole (b, h) slices (the last one and one drawn from a seed), every
-    row, plus edge and random rows of six more slices."""
+    row, each element also within the bf16-P bound; plus edge and random rows
+    of six more slices."""
     q, k, v = W.make_qkv(wl)
     o, lse = run_fwd(*to_dev(q, k, v), wl.causal, wl.scale)
     BH = wl.B * wl.H
     whole = sorted({BH - 1, int(np.random.default_rng(31).integers(BH - 1))})
     rows = np.concatenate([np.arange(h * wl.Nq, (h + 1) * wl.Nq, dtype=np.int64)
                            for h in whole])
-    _sampled(wl, o, lse, q, k, v, rows)
+    _sampled(wl, o, lse, q, k, v, rows, bound=True)
     _sampled(wl, o, lse, q, k, v, sample_rows(wl.B, wl.H, wl.Nq, n_heads=6, n_rand=16))
 
 
