@@ -44,3 +44,13 @@ def test_masked_rows_must_be_plus_zero_and_minus_inf():
     with pytest.raises(AssertionError):
         compare(torch.tensor([[-0.0, 0.0]], dtype=torch.bfloat16), torch.tensor([-np.inf]),
                 o_ref, lse_ref)
+
+
+def test_bound_takes_the_ulp_of_the_rounded_output():
+    # An exact value just below 2 whose kernel value (within P_ROUND * 1.0
+    # of it) rounds up to the bf16 grid above 2, where the spacing doubles:
+    # the rounding may move it by half an ulp of [2, 4), 2^-8, not of [1, 2).
+    o_ref = np.array([[1.9990]])
+    st = compare(_bf16([[2.0078125]]), torch.tensor([1.0]), o_ref, np.array([1.0]), "crossing",
+                 absv_ref=np.array([[1.0]]))
+    assert st["o_max_over_bound"] <= 0.0

@@ -21,13 +21,14 @@ This file is named to be collected last.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
 import oracle
 from attention_attn_fwd_07_gb300 import binding, build
 from attention_attn_fwd_07_gb300 import inputs as W
-from tests.parity_util import LSE_TOL, O_TOL, compare
+from tests.parity_util import LSE_TOL, O_TOL, compare, half_ulp_bf16
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -35,13 +36,17 @@ SCRATCH_BYTES = 32 << 20  # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h
 
 
 def _agree(o_a, lse_a, o_b, lse_b, what):
-    """The two entry points' outputs within the parity tolerances (O as bf16
-    values, LSE as f32; -inf rows must match exactly)."""
+    """The two entry points' outputs within the parity tolerances: LSE within
+    1e-3 (-inf rows exactly alike); O within 1e-2 beyond the two outputs' own
+    bf16 roundings (half an ulp each), the rule the oracle comparison applies
+    to one output."""
     la, lb = lse_a.double().cpu(), lse_b.double().cpu()
     assert torch.equal(torch.isneginf(la), torch.isneginf(lb)), f"{what}: masked rows differ"
     live = ~torch.isneginf(la)
     assert (la[live] - lb[live]).abs().max().item() <= LSE_TOL, f"{what}: LSE differs"
-    assert (o_a.double() - o_b.double()).abs().max().item() <= O_TOL, f"{what}: O differs"
+    a, b = o_a.double().cpu().numpy(), o_b.double().cpu().numpy()
+    excess = np.abs(a - b) - half_ulp_bf16(a) - half_ulp_bf16(b)
+    assert excess.max() <= O_TOL, f"{what}: O differs by {excess.max()} beyond rounding"
 
 
 def _entry(lib):
@@ -84,19 +89,19 @@ def test_noalloc_parity_on_consecutive_calls():
 
 
 def test_noalloc_fills_the_array_to_its_end():
-    """B16 H32 Nq1 d128 with 120 splits needs 31.7 MB of the 32 MiB array, so
-    the partial log-sum-exps occupy its last 240 KiB; with Nk = 2000 only 16
-    of the 120 key ranges hold keys and the rest are empty (o = 0, lse = -inf
-    partials).  Two calls in a row must both match the oracle, and 128 splits
-    at the same shape must be refused."""
+    """B16 H32 Nq1 d128 with 127 splits needs all but 2 KiB of the 32 MiB
+    array, so the partial log-sum-exps occupy its last 254 KiB; with
+    Nk = 2000 only 16 of the 127 key ranges hold keys and the rest are empty
+    (o = 0, lse = -inf partials).  Two calls in a row must both match the
+    oracle, and 128 splits at the same shape must be refused."""
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     build.build()
     f = _entry(binding.load_library())
     w = W.Workload("near the end of the array", 16, 32, 1, 2000, 128, False, 504)
-    splits = 120
+    splits = 127
     need = binding.attn_splitkv_workspace_bytes(w.B, w.H, 1, w.d, splits)
-    assert SCRATCH_BYTES - (1 << 20) < need <= SCRATCH_BYTES
+    assert SCRATCH_BYTES - 4096 < need <= SCRATCH_BYTES
     q_h, k_h, v_h = W.make_qkv(w)
     q, k, v = (t.to(DEV) for t in (q_h, k_h, v_h))
     ref = oracle.attention(q_h, k_h, v_h, causal=False, scale=w.scale)
