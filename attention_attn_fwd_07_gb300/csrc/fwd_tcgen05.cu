@@ -65,9 +65,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows b
 // tile takes 128 + DV columns (a 256-column allocation) and a ring small
 // enough that two CTAs share an SM, their pipelines covering each other's
 // start, drain and softmax latency -- the better trade when CTAs are short.
-template <int D, int DV, bool FP8, int NT = 2>
+// SB: score buffers per query tile (one-tile CTAs only).  With two, the
+// next tile's S = Q K^T runs while the softmax works on the current one,
+// and P V of a tile runs while the softmax works on the next.
+template <int D, int DV, bool FP8, int NT = 2, int SB = 1>
 struct Cfg {
   static_assert(NT == 1 || NT == 2, "one or two query tiles per CTA");
+  static_assert(SB == 1 || (SB == 2 && NT == 1), "two score buffers for one-tile CTAs");
+  static constexpr int kSBufs = NT * SB;                    // S slots of 128 columns
   static constexpr int kQKElem = FP8 ? 1 : 2;               // bytes per Q/K element
   static constexpr int kQKRowBytes = D * kQKElem;
   // 128-byte swizzle atoms per Q/K row; a partial last atom (d = 96: 192
@@ -81,12 +86,15 @@ struct Cfg {
   static constexpr uint32_t kVBytes = kVAtoms * kAtomBytes;   // one V tile
   static constexpr uint32_t kKVBytes = kKBytes > kVBytes ? kKBytes : kVBytes;  // one ring stage
   static constexpr int kStages =
-      NT == 2 ? ((kKVBytes >= 32768u) ? 4 : 8) : ((kKVBytes >= 32768u) ? 2 : 5);
+      NT == 2 ? ((kKVBytes >= 32768u) ? 4 : 8)
+              : ((kKVBytes >= 32768u) ? 2 : (SB == 2 ? 8 : 5));
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = NT * kQBytes;
   static constexpr uint32_t kOffBar = kOffKV + kStages * kKVBytes;
   // barriers: full[S], empty[S], q_full, s_full[2], p_ready[2] (keys 0-63 of
-  // P stored), p2_ready[2] (keys 64-127), o_full[2], drain
+  // P stored), p2_ready[2] (keys 64-127), o_full[2], drain, o_step (P V of
+  // one tile done; two score buffers only).  s_full / p_ready / p2_ready are
+  // per query tile with two tiles, per score buffer with two buffers.
   static constexpr int kBarFull = 0;
   static constexpr int kBarEmpty = kStages;
   static constexpr int kBarQ = 2 * kStages;
@@ -95,11 +103,12 @@ struct Cfg {
   static constexpr int kBarP2 = kBarP + 2;
   static constexpr int kBarO = kBarP2 + 2;
   static constexpr int kBarDrain = kBarO + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarOStep = kBarDrain + 1;
+  static constexpr int kNumBars = kBarOStep + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + 1 KiB alignment slack
-  static constexpr uint32_t kColS = 0;          // + 128 * tile
-  static constexpr uint32_t kColO = 128 * NT;   // + kOStride * tile
+  static constexpr uint32_t kColS = 0;              // + 128 * (tile or score buffer)
+  static constexpr uint32_t kColO = 128 * kSBufs;   // + kOStride * tile
   static constexpr uint32_t kOStride = (DV + 63) / 64 * 64;  // O columns per tile, 64-aligned
   static constexpr uint32_t kTmemCols = (kColO + NT * kOStride) <= 256 ? 256 : 512;
   static constexpr int kThreads = threads_for(NT);
@@ -159,6 +168,22 @@ struct Waiter {
   }
 };
 
+// Ring order of the K and V tiles with two score buffers: the order the MMA
+// warp consumes them (S(0), S(1), P(0) V, S(2), P(1) V, S(3), ...), i.e.
+// K0 K1 V0 K2 V1 K3 V2 ... K(n-1) V(n-2) V(n-1), so that every load waits
+// only for the release of the tile two positions before it.  These give the
+// ring position of K(j) and V(j) for n tiles, and what position t holds.
+__device__ __forceinline__ int kpos2(int j) { return j <= 1 ? j : 2 * j - 1; }
+__device__ __forceinline__ int vpos2(int j, int n) { return j <= n - 2 ? 2 + 2 * j : 2 * n - 1; }
+__device__ __forceinline__ void item2(int t, int n, bool& is_v, int& j) {
+  if (n == 1) { is_v = t == 1; j = 0; return; }
+  if (t <= 1) { is_v = false; j = t; return; }
+  if (t >= 2 * n - 2) { is_v = true; j = t - n; return; }
+  const int m = (t - 2) >> 1;
+  is_v = ((t - 2) & 1) == 0;
+  j = is_v ? m : m + 2;
+}
+
 // Number of K/V tiles query tile `row0` (128 rows) must visit; 0 if the tile
 // is past Nq or (negative offsets only) no row of it sees any key.
 __device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
@@ -171,12 +196,12 @@ __device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
   return static_cast<int>(min(n_all, last_key / BN + 1));
 }
 
-template <int D, int DV, bool FP8, int NT>
+template <int D, int DV, bool FP8, int NT, int SB>
 __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     attn_fwd_tcgen05_kernel(const __grid_constant__ CUtensorMap tq,
                             const __grid_constant__ CUtensorMap tk,
                             const __grid_constant__ CUtensorMap tv, const KParams p) {
-  using C = Cfg<D, DV, FP8, NT>;
+  using C = Cfg<D, DV, FP8, NT, SB>;
   constexpr int kWarpMma = C::kWarpMma;
   constexpr int kWarpLoad = C::kWarpLoad;
   extern __shared__ uint8_t smem_raw[];
@@ -229,6 +254,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
       mbar_init(bar(C::kBarO + x), 1);
     }
     mbar_init(bar(C::kBarDrain), 1);
+    mbar_init(bar(C::kBarOStep), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -263,7 +289,8 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
                       a * (128 / C::kQKElem), static_cast<int>(q0 + x * BM),
                       static_cast<int>(bh));
       }
-      // Ring position t: K(t/2) for even t, V(t/2) for odd t.
+      // Ring position t: K(t/2) for even t, V(t/2) for odd t (one score
+      // buffer per tile); the consumption order of item2() with two.
       int last_t[C::kStages];
       for (int s = 0; s < C::kStages; ++s) last_t[s] = -1;
       int skipped = -1;
@@ -277,9 +304,11 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
           skipped = t;
           continue;
         }
-        const bool is_v = (t & 1) != 0;
+        bool is_v = (t & 1) != 0;
+        int tile = t >> 1;
+        if constexpr (SB == 2) item2(t, n_kv, is_v, tile);
         mbar_arrive_expect_tx(bar(C::kBarFull + s), is_v ? C::kVBytes : C::kKBytes);
-        const int key0 = (t >> 1) * BN;
+        const int key0 = tile * BN;
         const int atoms = is_v ? C::kVAtoms : C::kQKAtoms;
         const int per_atom = is_v ? 64 : 128 / C::kQKElem;  // elements per 128-byte row
         for (int a = 0; a < atoms; ++a)
@@ -306,8 +335,10 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     };
     auto commit = [&](uint32_t b) { mma_commit_w(b); };
     if (n_kv > 0) {
-      auto qk = [&](int x, int stage) {
-        const uint32_t d_tmem = tmem + C::kColS + 128 * x;
+      // S = Q_x K^T into score slot `slot` (the tile's own with two tiles,
+      // the alternating buffer with two score buffers).
+      auto qk = [&](int x, int stage, int slot) {
+        const uint32_t d_tmem = tmem + C::kColS + 128 * slot;
         const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes, 16, 1024);
         const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, 16, 1024);
         // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
@@ -328,9 +359,9 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
       };
       // O_X += P_X V over keys 64 h .. 64 h + 63 (four K steps of 16 keys;
       // P's bf16 pairs for those keys sit in columns 32 h .. 32 h + 31).
-      auto pv_half = [&](int x, int stage, int h, bool acc) {
+      auto pv_half = [&](int x, int stage, int h, bool acc, int slot) {
         const uint32_t d_tmem = tmem + C::kColO + C::kOStride * x;
-        const uint32_t p_tmem = tmem + C::kColS + 128 * x + 32 * h;
+        const uint32_t p_tmem = tmem + C::kColS + 128 * slot + 32 * h;
         const uint64_t b =
             sdesc_sw128(sKV + stage * C::kKVBytes + h * 64 * 128, C::kAtomBytes, 1024);
         static_assert(BN == 128, "two halves of four K steps of 16 keys");
@@ -338,11 +369,63 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
       };
       bool ok = wait_w(bar(C::kBarQ), 0);
       if (ok) ok = wait_w(bar(C::kBarFull + 0), 0);
+      if constexpr (SB == 2) {
+        // One tile, two score buffers.  Issue order: S(0), S(1), then for
+        // each j: P(j) V (two halves, as P arrives), S(j+2) into P(j)'s
+        // buffer (in order after the P V that reads it).  A commit after
+        // every P V tells the softmax when O may be rescaled.
+        const int n = ntile[0];
+        auto stage_of = [&](int t) { return t % C::kStages; };
+        auto phase_of = [&](int t) { return static_cast<uint32_t>((t / C::kStages) & 1); };
+        if (ok) {
+          tc_fence_after();
+          qk(0, 0, 0);
+          commit(bar(C::kBarS + 0));
+          commit(bar(C::kBarEmpty + 0));
+        }
+        if (ok && n > 1) {
+          const int tK = kpos2(1);
+          ok = wait_w(bar(C::kBarFull + stage_of(tK)), phase_of(tK));
+          if (ok) {
+            tc_fence_after();
+            qk(0, stage_of(tK), 1);
+            commit(bar(C::kBarS + 1));
+            commit(bar(C::kBarEmpty + stage_of(tK)));
+          }
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          const int b = j & 1;
+          const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
+          const int tV = vpos2(j, n);
+          ok = wait_w(bar(C::kBarFull + stage_of(tV)), phase_of(tV));
+          if (!ok) break;
+          ok = wait_w(bar(C::kBarP + b), ph);
+          if (!ok) break;
+          tc_fence_after();
+          pv_half(0, stage_of(tV), 0, j > 0, b);
+          ok = wait_w(bar(C::kBarP2 + b), ph);
+          if (!ok) break;
+          tc_fence_after();
+          pv_half(0, stage_of(tV), 1, true, b);
+          commit(bar(C::kBarOStep));
+          if (j == n - 1) commit(bar(C::kBarO + 0));
+          commit(bar(C::kBarEmpty + stage_of(tV)));
+          if (j + 2 < n) {
+            const int tK = kpos2(j + 2);
+            ok = wait_w(bar(C::kBarFull + stage_of(tK)), phase_of(tK));
+            if (!ok) break;
+            tc_fence_after();
+            qk(0, stage_of(tK), b);
+            commit(bar(C::kBarS + b));
+            commit(bar(C::kBarEmpty + stage_of(tK)));
+          }
+        }
+      } else {
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < NT; ++x) {
           if (ntile[x] > 0) {
-            qk(x, 0);
+            qk(x, 0, x);
             commit(bar(C::kBarS + x));
           }
         }
@@ -360,11 +443,11 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
           ok = wait_w(bar(C::kBarP + x), j & 1);
           if (!ok) break;
           tc_fence_after();
-          pv_half(x, sV, 0, j > 0);
+          pv_half(x, sV, 0, j > 0, x);
           ok = wait_w(bar(C::kBarP2 + x), j & 1);
           if (!ok) break;
           tc_fence_after();
-          pv_half(x, sV, 1, true);
+          pv_half(x, sV, 1, true, x);
           if (j == ntile[x] - 1) commit(bar(C::kBarO + x));
           if (j + 1 < ntile[x]) {
             if (!k_ready) {
@@ -373,7 +456,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
               tc_fence_after();
               k_ready = true;
             }
-            qk(x, sK);
+            qk(x, sK, x);
             commit(bar(C::kBarS + x));
           }
         }
@@ -387,6 +470,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
           commit(bar(C::kBarEmpty + sK));
         }
       }
+      }  // one score buffer per tile
       // All issued MMAs must complete before TMEM is released (bounded wait
       // that ignores the abort flag).
       commit(bar(C::kBarDrain));
@@ -401,7 +485,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     const int64_t row0 = q0 + x * BM;
     const int64_t row = row0 + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::kColS + 128 * x;
+    const uint32_t tS0 = tmem + lane_off + C::kColS + 128 * x;  // (first) score buffer
     const uint32_t tO = tmem + lane_off + C::kColO + C::kOStride * x;
     const int n = ntile[x];
     // Last admissible key of this row and of the tile's first row.
@@ -413,8 +497,13 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     float l = 0.0f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
+      // Score slot and barrier phase of this tile: the tile's own slot with
+      // one buffer, alternating buffers (each used every other tile) with two.
+      const int slot = SB == 2 ? (j & 1) : x;
+      const uint32_t ph = SB == 2 ? static_cast<uint32_t>((j >> 1) & 1) : static_cast<uint32_t>(j & 1);
+      const uint32_t tS = tS0 + 128 * (SB == 2 ? (j & 1) : 0);
       // tcgen05.ld/st below are warp-collective: the warp leaves together.
-      ok = __all_sync(0xffffffffu, wait(bar(C::kBarS + x), j & 1));
+      ok = __all_sync(0xffffffffu, wait(bar(C::kBarS + slot), ph));
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[128];
@@ -450,6 +539,15 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
         rescale = (m_ref != -INFINITY);
         l *= alpha;
         m_ref = m_new;
+      }
+      if constexpr (SB == 2) {
+        // With two score buffers P V of the previous tile may still be
+        // running: an O rescale waits for it first (rare: the threshold).
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+          ok = __all_sync(0xffffffffu, wait(bar(C::kBarOStep), (j - 1) & 1));
+          if (!ok) break;
+          tc_fence_after();
+        }
       }
       const float neg_ref = (m_ref == -INFINITY) ? 0.0f : -m_ref;
       // p = 2^(s * scale * log2 e - m_ref), two lanes per instruction; the
@@ -490,7 +588,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar((h == 0 ? C::kBarP : C::kBarP2) + x));
+        if (lane == 0) mbar_arrive(bar((h == 0 ? C::kBarP : C::kBarP2) + slot));
       }
       float sum_lo, sum_hi;
       f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
@@ -542,12 +640,12 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
   }
 }
 
-template <int D, int DV, bool FP8, int NT = 2>
+template <int D, int DV, bool FP8, int NT = 2, int SB = 1>
 cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                    const CUtensorMap& tv, cudaStream_t stream) {
-  using C = Cfg<D, DV, FP8, NT>;
+  using C = Cfg<D, DV, FP8, NT, SB>;
   static_assert(C::kSmemBytes < (1u << 20), "");
-  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, DV, FP8, NT>,
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_tcgen05_kernel<D, DV, FP8, NT, SB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(C::kSmemBytes));
   if (err != cudaSuccess) return err;
@@ -572,7 +670,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.flags = a.flags;
   p.timeout_ns = a.timeout_ns;
   const int64_t blocks = a.BH * p.n_qblk;
-  attn_fwd_tcgen05_kernel<D, DV, FP8, NT><<<dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),
+  attn_fwd_tcgen05_kernel<D, DV, FP8, NT, SB><<<dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),
                                C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
@@ -586,7 +684,7 @@ cudaError_t launch_fwd_tcgen05(const FwdArgs& a, const CUtensorMap& tq, const CU
   // steps); 256 takes one query tile per CTA with S and a 256-column O in
   // all 512 TMEM columns and a two-stage ring of 64 KB tiles.
   if (a.d == 96) return launch<96, 96, false>(a, tq, tk, tv, stream);
-  if (a.d == 256) return launch<256, 256, false, 1>(a, tq, tk, tv, stream);
+  if (a.d == 256) return launch<256, 256, false, 1, 2>(a, tq, tk, tv, stream);
   if (a.fp8_qk)
     return a.dv == 64 ? launch<128, 64, true>(a, tq, tk, tv, stream)
                       : launch<128, 128, true>(a, tq, tk, tv, stream);

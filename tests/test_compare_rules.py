@@ -13,18 +13,19 @@ def _bf16(x):
 def test_bound_accepts_weight_rounding_and_rejects_more():
     # O_ref = 0.5 with sum_j w_j |v_j| = 5 (dominant weights on large |v| of
     # opposite signs): the weight rounding allows 1/2 ulp + P_ROUND * 5 =
-    # 0.0123, beyond 1e-2 raw.  GPU values below sit on the bf16 grid
+    # 0.0227, beyond 1e-2 raw.  GPU values below sit on the bf16 grid
     # (spacing 2^-8 in [0.5, 1)).
     o_ref = np.array([[0.5]])
     lse_ref = np.array([3.0])
     st = compare(_bf16([[0.5 + 3 * 2.0 ** -8]]), torch.tensor([3.0]), o_ref, lse_ref, "within",
                  absv_ref=np.array([[5.0]]))
     assert st["o_max_over_bound"] <= 0.0 and st["o_max_abs"] > 1e-2
-    # With sum_j w_j |v_j| = 1 the bound is 1/2 ulp + P_ROUND = 0.0040: an
-    # error of 2 grid steps (0.0078) passes the 1e-2 rules but not the bound.
+    # With sum_j w_j |v_j| = 0.5 the bound is 1/2 ulp + P_ROUND / 2 = 0.0040:
+    # an error of 2 grid steps (0.0078) passes the 1e-2 rules but not the
+    # bound.
     with pytest.raises(AssertionError):
         compare(_bf16([[0.5 + 2 * 2.0 ** -8]]), torch.tensor([3.0]), o_ref, lse_ref, "beyond",
-                absv_ref=np.array([[1.0]]))
+                absv_ref=np.array([[0.5]]))
 
 
 def test_without_bound_raw_rule_applies_below_two():
@@ -47,10 +48,10 @@ def test_masked_rows_must_be_plus_zero_and_minus_inf():
 
 
 def test_bound_takes_the_ulp_of_the_rounded_output():
-    # An exact value just below 2 whose kernel value (within P_ROUND * 1.0
+    # An exact value just below 2 whose kernel value (within P_ROUND * 0.5
     # of it) rounds up to the bf16 grid above 2, where the spacing doubles:
     # the rounding may move it by half an ulp of [2, 4), 2^-8, not of [1, 2).
     o_ref = np.array([[1.9990]])
     st = compare(_bf16([[2.0078125]]), torch.tensor([1.0]), o_ref, np.array([1.0]), "crossing",
-                 absv_ref=np.array([[1.0]]))
+                 absv_ref=np.array([[0.5]]))
     assert st["o_max_over_bound"] <= 0.0
