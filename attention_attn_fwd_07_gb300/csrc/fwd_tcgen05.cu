@@ -93,7 +93,8 @@ struct Cfg {
   static constexpr uint32_t kOffBar = kOffKV + kStages * kKVBytes;
   // barriers: full[S], empty[S], q_full, s_full[2], p_ready[2] (keys 0-63 of
   // P stored), p2_ready[2] (keys 64-127), o_full[2], drain, o_step (P V of
-  // one tile done; two score buffers only).  s_full / p_ready / p2_ready are
+  // one tile done; two score buffers only), q_free (the work item's last
+  // Q K^T done: the next item's Q may load).  s_full / p_ready / p2_ready are
   // per query tile with two tiles, per score buffer with two buffers.
   static constexpr int kBarFull = 0;
   static constexpr int kBarEmpty = kStages;
@@ -104,7 +105,8 @@ struct Cfg {
   static constexpr int kBarO = kBarP2 + 2;
   static constexpr int kBarDrain = kBarO + 2;
   static constexpr int kBarOStep = kBarDrain + 1;
-  static constexpr int kNumBars = kBarOStep + 1;
+  static constexpr int kBarQFree = kBarOStep + 1;  // an item's last Q K^T completed
+  static constexpr int kNumBars = kBarQFree + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag
   static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + 1 KiB alignment slack
   static constexpr uint32_t kColS = 0;              // + 128 * (tile or score buffer)
@@ -136,7 +138,7 @@ struct KParams {
   int64_t Nq, Nk, qoff;
   int64_t H, group;  // query heads per batch; query heads per K/V head
   int64_t n_bh;       // batch x query heads
-  int64_t heads_per_group;  // (b, h) slices per causal scheduling group
+  int64_t chunk;      // items per causal scheduling chunk (whole rounds of the grid)
   int n_qblk;
   int causal;
   float sc_log2;  // scale * log2(e)
@@ -196,6 +198,64 @@ __device__ __forceinline__ int tiles_for(int64_t row0, const KParams& p) {
   return static_cast<int>(min(n_all, last_key / BN + 1));
 }
 
+// One work item: 128 * NT query rows of one (b, h).  Items are numbered in
+// the launch's scheduling order.  Causal problems take consecutive chunks of
+// the (b, h)-major item list, each chunk sized to whole rounds of the grid
+// and to K/V that fit in L2 together, and order every chunk heaviest first
+// (last query block first, then by head): dealt out in the alternating
+// rounds of item_of(), a chunk's heavy and light items pair up on each CTA,
+// and K/V are read from DRAM about once.
+struct Item {
+  int64_t bh, bkv, q0;
+  int ntile[2];
+  int n_kv;
+};
+
+template <int NT>
+__device__ __forceinline__ Item decode_item(int64_t idx, const KParams& p) {
+  Item it;
+  int64_t qb;
+  const int64_t nq = p.n_qblk;
+  if (p.causal) {
+    const int64_t n_items = p.n_bh * nq;
+    const int64_t a = (idx / p.chunk) * p.chunk;        // chunk [a, e) of the (b, h)-major list
+    const int64_t e = min(a + p.chunk, n_items);
+    const int64_t h_first = a / nq, h_last = (e - 1) / nq;
+    const int64_t a0 = a % nq, e0 = (e - 1) % nq;       // first block of h_first, last of h_last
+    // Rank r inside the chunk: query blocks from the last down, the chunk's
+    // heads holding that block in (b, h) order.
+    int64_t r = idx - a;
+    for (qb = nq - 1;; --qb) {
+      const int64_t lo = qb >= a0 ? h_first : h_first + 1;
+      const int64_t hi = qb <= e0 ? h_last : h_last - 1;
+      const int64_t cnt = hi >= lo ? hi - lo + 1 : 0;
+      if (r < cnt || qb == 0) {
+        it.bh = lo + r;
+        break;
+      }
+      r -= cnt;
+    }
+  } else {
+    it.bh = idx / nq;
+    qb = idx % nq;
+  }
+  it.q0 = qb * (NT * BM);
+  // K/V head of this query head (grouped K/V heads: H / group per batch).
+  it.bkv = (it.bh / p.H) * (p.H / p.group) + (it.bh % p.H) / p.group;
+  it.ntile[0] = tiles_for(it.q0, p);
+  it.ntile[1] = NT == 2 ? tiles_for(it.q0 + BM, p) : 0;
+  it.n_kv = max(it.ntile[0], it.ntile[1]);
+  return it;
+}
+
+// The k-th work item of CTA c out of G: rounds of G items, alternately in
+// and against CTA order (so a CTA that drew a heavy item in one round draws
+// a light one in the next); -1 once the rounds pass the last item.
+__device__ __forceinline__ int64_t item_of(int64_t k, int64_t c, int64_t G, int64_t n_items) {
+  const int64_t idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+  return idx < n_items ? idx : -1;
+}
+
 template <int D, int DV, bool FP8, int NT, int SB>
 __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
     attn_fwd_tcgen05_kernel(const __grid_constant__ CUtensorMap tq,
@@ -215,31 +275,11 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // CTA -> (bh, query block).  Causal grids run in groups of consecutive
-  // (b, h) slices whose K and V fit in L2 together; inside a group the CTAs
-  // go longest-first (last query block first, then by head), so the CTAs
-  // dispatched last are short and K/V are read from DRAM about once.
-  int64_t bh;
-  int qb;
-  if (p.causal) {
-    const int64_t per_group = p.heads_per_group * p.n_qblk;
-    const int64_t h0 = (blockIdx.x / per_group) * p.heads_per_group;
-    const int64_t r = blockIdx.x % per_group;
-    const int64_t gh = min(p.heads_per_group, p.n_bh - h0);  // the last group may be smaller
-    bh = h0 + r % gh;
-    qb = p.n_qblk - 1 - static_cast<int>(r / gh);
-  } else {
-    bh = blockIdx.x / p.n_qblk;
-    qb = static_cast<int>(blockIdx.x % p.n_qblk);
-  }
-  const int64_t q0 = static_cast<int64_t>(qb) * (NT * BM);
-  // K/V head of this query head (grouped K/V heads: H / group per batch).
-  const int64_t bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
-  int ntile[2];
-  ntile[0] = tiles_for(q0, p);
-  ntile[1] = NT == 2 ? tiles_for(q0 + BM, p) : 0;
-  const int n_kv = max(ntile[0], ntile[1]);
+  // This CTA walks work items item_of(0), item_of(1), ... (one item per CTA
+  // when the grid has one CTA per item).  Every role walks the same list and
+  // counts barrier phases across items.
+  const int64_t n_items = p.n_bh * p.n_qblk;
+  const int64_t G = gridDim.x, cta = blockIdx.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -247,6 +287,7 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
       mbar_init(bar(C::kBarEmpty + s), 1);
     }
     mbar_init(bar(C::kBarQ), 1);
+    mbar_init(bar(C::kBarQFree), 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(C::kBarS + x), 1);
       mbar_init(bar(C::kBarP + x), 4);  // one arrival per softmax warp
@@ -278,53 +319,68 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
 
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_kv > 0) {
-      uint32_t qbytes = 0;
-      for (int x = 0; x < NT; ++x) qbytes += ntile[x] > 0 ? C::kQBytes : 0u;
-      mbar_arrive_expect_tx(bar(C::kBarQ), qbytes);
-      for (int x = 0; x < NT; ++x) {
-        if (ntile[x] == 0) continue;
-        for (int a = 0; a < C::kQKAtoms; ++a)
-          tma_load_3d(sQ + x * C::kQBytes + a * C::kAtomBytes, &tq, bar(C::kBarQ),
-                      a * (128 / C::kQKElem), static_cast<int>(q0 + x * BM),
-                      static_cast<int>(bh));
-      }
-      // Ring position t: K(t/2) for even t, V(t/2) for odd t (one score
-      // buffer per tile); the consumption order of item2() with two.
-      int last_t[C::kStages];
-      for (int s = 0; s < C::kStages; ++s) last_t[s] = -1;
-      int skipped = -1;
+    if (lane == 0) {
+      // Ring position T runs on across items: within an item, position t is
+      // K(t/2) for even t, V(t/2) for odd t (one score buffer per tile), or
+      // the consumption order of item2() (two).
+      int64_t last_T[C::kStages];
+      for (int s = 0; s < C::kStages; ++s) last_T[s] = -1;
+      int64_t T = 0, skipped = -1;
+      int q_loads = 0;
       bool ok = true;
-      for (int t = 0; t < 2 * n_kv && ok; ++t) {
-        const int s = t % C::kStages;
-        if (t >= C::kStages) ok = wait(bar(C::kBarEmpty + s), ((t / C::kStages) - 1) & 1);
+      for (int64_t k = 0; ok; ++k) {
+        const int64_t idx = item_of(k, cta, G, n_items);
+        if (idx < 0) break;
+        const Item it = decode_item<NT>(idx, p);
+        if (it.n_kv == 0) continue;
+        // The Q tiles are overwritten once the previous item's last Q K^T
+        // has completed.
+        if (q_loads > 0) ok = wait(bar(C::kBarQFree), (q_loads - 1) & 1);
         if (!ok) break;
-        last_t[s] = t;
-        if ((p.flags & ATTN_FLAG_TEST_SKIP_LOAD) && t == 1) {  // fault injection
-          skipped = t;
-          continue;
+        uint32_t qbytes = 0;
+        for (int x = 0; x < NT; ++x) qbytes += it.ntile[x] > 0 ? C::kQBytes : 0u;
+        mbar_arrive_expect_tx(bar(C::kBarQ), qbytes);
+        for (int x = 0; x < NT; ++x) {
+          if (it.ntile[x] == 0) continue;
+          for (int a = 0; a < C::kQKAtoms; ++a)
+            tma_load_3d(sQ + x * C::kQBytes + a * C::kAtomBytes, &tq, bar(C::kBarQ),
+                        a * (128 / C::kQKElem), static_cast<int>(it.q0 + x * BM),
+                        static_cast<int>(it.bh));
         }
-        bool is_v = (t & 1) != 0;
-        int tile = t >> 1;
-        if constexpr (SB == 2) item2(t, n_kv, is_v, tile);
-        mbar_arrive_expect_tx(bar(C::kBarFull + s), is_v ? C::kVBytes : C::kKBytes);
-        const int key0 = tile * BN;
-        const int atoms = is_v ? C::kVAtoms : C::kQKAtoms;
-        const int per_atom = is_v ? 64 : 128 / C::kQKElem;  // elements per 128-byte row
-        for (int a = 0; a < atoms; ++a)
-          tma_load_3d(sKV + s * C::kKVBytes + a * C::kAtomBytes, is_v ? &tv : &tk,
-                      bar(C::kBarFull + s), a * per_atom, key0, static_cast<int>(bkv));
+        ++q_loads;
+        for (int t = 0; t < 2 * it.n_kv && ok; ++t) {
+          const int64_t TT = T + t;
+          const int s = static_cast<int>(TT % C::kStages);
+          if (TT >= C::kStages) ok = wait(bar(C::kBarEmpty + s), ((TT / C::kStages) - 1) & 1);
+          if (!ok) break;
+          last_T[s] = TT;
+          if ((p.flags & ATTN_FLAG_TEST_SKIP_LOAD) && TT == 1) {  // fault injection
+            skipped = TT;
+            continue;
+          }
+          bool is_v = (t & 1) != 0;
+          int tile = t >> 1;
+          if constexpr (SB == 2) item2(t, it.n_kv, is_v, tile);
+          mbar_arrive_expect_tx(bar(C::kBarFull + s), is_v ? C::kVBytes : C::kKBytes);
+          const int key0 = tile * BN;
+          const int atoms = is_v ? C::kVAtoms : C::kQKAtoms;
+          const int per_atom = is_v ? 64 : 128 / C::kQKElem;  // elements per 128-byte row
+          for (int a = 0; a < atoms; ++a)
+            tma_load_3d(sKV + s * C::kKVBytes + a * C::kAtomBytes, is_v ? &tv : &tk,
+                        bar(C::kBarFull + s), a * per_atom, key0, static_cast<int>(it.bkv));
+        }
+        T += 2 * it.n_kv;
       }
       // Every issued load must land before the CTA can exit.  Only this
-      // thread arrives on the full barriers, so the phase of the last load
-      // into a stage stays complete once it lands.  These waits ignore the
+      // thread arrives on the full and Q barriers, so the phase of the last
+      // load into each stays complete once it lands.  These waits ignore the
       // abort flag (they cover copies in flight) but are still bounded.
       volatile int no_abort = 0;
       const Waiter own{&no_abort, p.status, p.timeout_ns};
-      own(bar(C::kBarQ), 0);
+      if (q_loads > 0) own(bar(C::kBarQ), (q_loads - 1) & 1);
       for (int s = 0; s < C::kStages; ++s)
-        if (last_t[s] >= 0 && last_t[s] != skipped)
-          own(bar(C::kBarFull + s), (last_t[s] / C::kStages) & 1);
+        if (last_T[s] >= 0 && last_T[s] != skipped)
+          own(bar(C::kBarFull + s), (last_T[s] / C::kStages) & 1);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -334,69 +390,80 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
       return __all_sync(0xffffffffu, wait(b, parity));
     };
     auto commit = [&](uint32_t b) { mma_commit_w(b); };
-    if (n_kv > 0) {
-      // S = Q_x K^T into score slot `slot` (the tile's own with two tiles,
-      // the alternating buffer with two score buffers).
-      auto qk = [&](int x, int stage, int slot) {
-        const uint32_t d_tmem = tmem + C::kColS + 128 * slot;
-        const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes, 16, 1024);
-        const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, 16, 1024);
-        // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
-        if constexpr (FP8) {
-          mma_ss_f8_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
-        } else if constexpr (C::kQKSteps == 16) {
-          // Two runs of eight steps; the second starts two atoms (32 KB =
-          // 2048 descriptor units) further and accumulates.
-          mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
-          mma_ss_run8_w(d_tmem, a + 2048, b + 2048, C::kIdescQK, 1u);
-        } else if constexpr (C::kQKSteps == 8) {
-          mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
-        } else if constexpr (C::kQKSteps == 6) {
-          mma_ss_run6_w(d_tmem, a, b, C::kIdescQK, 0u);
-        } else {
-          mma_ss_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
-        }
-      };
-      // O_X += P_X V over keys 64 h .. 64 h + 63 (four K steps of 16 keys;
-      // P's bf16 pairs for those keys sit in columns 32 h .. 32 h + 31).
-      auto pv_half = [&](int x, int stage, int h, bool acc, int slot) {
-        const uint32_t d_tmem = tmem + C::kColO + C::kOStride * x;
-        const uint32_t p_tmem = tmem + C::kColS + 128 * slot + 32 * h;
-        const uint64_t b =
-            sdesc_sw128(sKV + stage * C::kKVBytes + h * 64 * 128, C::kAtomBytes, 1024);
-        static_assert(BN == 128, "two halves of four K steps of 16 keys");
-        mma_ts_run4_w(d_tmem, p_tmem, b, C::kIdescPV, acc ? 1u : 0u);
-      };
-      bool ok = wait_w(bar(C::kBarQ), 0);
-      if (ok) ok = wait_w(bar(C::kBarFull + 0), 0);
+    auto stage_of = [&](int64_t t) { return static_cast<int>(t % C::kStages); };
+    auto phase_of = [&](int64_t t) { return static_cast<uint32_t>((t / C::kStages) & 1); };
+    // S = Q_x K^T into score slot `slot` (the tile's own with two tiles,
+    // the alternating buffer with two score buffers).
+    auto qk = [&](int x, int stage, int slot) {
+      const uint32_t d_tmem = tmem + C::kColS + 128 * slot;
+      const uint64_t a = sdesc_sw128(sQ + x * C::kQBytes, 16, 1024);
+      const uint64_t b = sdesc_sw128(sKV + stage * C::kKVBytes, 16, 1024);
+      // One MMA consumes 32 bytes of each Q/K row (16 bf16 or 32 e4m3).
+      if constexpr (FP8) {
+        mma_ss_f8_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
+      } else if constexpr (C::kQKSteps == 16) {
+        // Two runs of eight steps; the second starts two atoms (32 KB =
+        // 2048 descriptor units) further and accumulates.
+        mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
+        mma_ss_run8_w(d_tmem, a + 2048, b + 2048, C::kIdescQK, 1u);
+      } else if constexpr (C::kQKSteps == 8) {
+        mma_ss_run8_w(d_tmem, a, b, C::kIdescQK, 0u);
+      } else if constexpr (C::kQKSteps == 6) {
+        mma_ss_run6_w(d_tmem, a, b, C::kIdescQK, 0u);
+      } else {
+        mma_ss_run4_w(d_tmem, a, b, C::kIdescQK, 0u);
+      }
+    };
+    // O_X += P_X V over keys 64 h .. 64 h + 63 (four K steps of 16 keys;
+    // P's bf16 pairs for those keys sit in columns 32 h .. 32 h + 31).  The
+    // first half of an item's first tile overwrites O: the softmax warps read
+    // the previous item's O before they announced this item's first P.
+    auto pv_half = [&](int x, int stage, int h, bool acc, int slot) {
+      const uint32_t d_tmem = tmem + C::kColO + C::kOStride * x;
+      const uint32_t p_tmem = tmem + C::kColS + 128 * slot + 32 * h;
+      const uint64_t b =
+          sdesc_sw128(sKV + stage * C::kKVBytes + h * 64 * 128, C::kAtomBytes, 1024);
+      static_assert(BN == 128, "two halves of four K steps of 16 keys");
+      mma_ts_run4_w(d_tmem, p_tmem, b, C::kIdescPV, acc ? 1u : 0u);
+    };
+    int64_t T = 0;     // ring position of the item's first tile
+    int q_uses = 0;    // items with work so far (Q barrier phases)
+    int64_t sc[2] = {0, 0};  // score tiles handled so far, per query tile
+    bool ok = true;
+    for (int64_t k = 0; ok; ++k) {
+      const int64_t idx = item_of(k, cta, G, n_items);
+      if (idx < 0) break;
+      const Item it = decode_item<NT>(idx, p);
+      if (it.n_kv == 0) continue;
+      ok = wait_w(bar(C::kBarQ), q_uses & 1);
+      if (ok) ok = wait_w(bar(C::kBarFull + stage_of(T)), phase_of(T));
+      if (!ok) break;
       if constexpr (SB == 2) {
         // One tile, two score buffers.  Issue order: S(0), S(1), then for
         // each j: P(j) V (two halves, as P arrives), S(j+2) into P(j)'s
         // buffer (in order after the P V that reads it).  A commit after
         // every P V tells the softmax when O may be rescaled.
-        const int n = ntile[0];
-        auto stage_of = [&](int t) { return t % C::kStages; };
-        auto phase_of = [&](int t) { return static_cast<uint32_t>((t / C::kStages) & 1); };
-        if (ok) {
-          tc_fence_after();
-          qk(0, 0, 0);
-          commit(bar(C::kBarS + 0));
-          commit(bar(C::kBarEmpty + 0));
-        }
-        if (ok && n > 1) {
-          const int tK = kpos2(1);
+        const int n = it.ntile[0];
+        const int64_t g0 = sc[0];  // score tiles before this item
+        tc_fence_after();
+        qk(0, stage_of(T), static_cast<int>(g0 & 1));
+        commit(bar(C::kBarS + static_cast<int>(g0 & 1)));
+        commit(bar(C::kBarEmpty + stage_of(T)));
+        if (n > 1) {
+          const int64_t tK = T + kpos2(1);
           ok = wait_w(bar(C::kBarFull + stage_of(tK)), phase_of(tK));
-          if (ok) {
-            tc_fence_after();
-            qk(0, stage_of(tK), 1);
-            commit(bar(C::kBarS + 1));
-            commit(bar(C::kBarEmpty + stage_of(tK)));
-          }
+          if (!ok) break;
+          tc_fence_after();
+          qk(0, stage_of(tK), static_cast<int>((g0 + 1) & 1));
+          commit(bar(C::kBarS + static_cast<int>((g0 + 1) & 1)));
+          commit(bar(C::kBarEmpty + stage_of(tK)));
         }
+        if (n <= 2) commit(bar(C::kBarQFree));  // the item's last Q K^T is issued
         for (int j = 0; j < n && ok; ++j) {
-          const int b = j & 1;
-          const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-          const int tV = vpos2(j, n);
+          const int64_t g = g0 + j;
+          const int b = static_cast<int>(g & 1);
+          const uint32_t ph = static_cast<uint32_t>((g >> 1) & 1);
+          const int64_t tV = T + vpos2(j, n);
           ok = wait_w(bar(C::kBarFull + stage_of(tV)), phase_of(tV));
           if (!ok) break;
           ok = wait_w(bar(C::kBarP + b), ph);
@@ -411,199 +478,214 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
           if (j == n - 1) commit(bar(C::kBarO + 0));
           commit(bar(C::kBarEmpty + stage_of(tV)));
           if (j + 2 < n) {
-            const int tK = kpos2(j + 2);
+            const int64_t tK = T + kpos2(j + 2);
             ok = wait_w(bar(C::kBarFull + stage_of(tK)), phase_of(tK));
             if (!ok) break;
             tc_fence_after();
             qk(0, stage_of(tK), b);
             commit(bar(C::kBarS + b));
             commit(bar(C::kBarEmpty + stage_of(tK)));
+            if (j + 3 == n) commit(bar(C::kBarQFree));
           }
         }
       } else {
-      if (ok) {
         tc_fence_after();
         for (int x = 0; x < NT; ++x) {
-          if (ntile[x] > 0) {
-            qk(x, 0, x);
+          if (it.ntile[x] > 0) {
+            qk(x, stage_of(T), x);
             commit(bar(C::kBarS + x));
           }
         }
-        commit(bar(C::kBarEmpty + 0));
-      }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int tV = 2 * j + 1, sV = tV % C::kStages;
-        const int tK = 2 * j + 2, sK = tK % C::kStages;
-        const bool next = j + 1 < n_kv;
-        bool k_ready = false;
-        ok = wait_w(bar(C::kBarFull + sV), (tV / C::kStages) & 1);
-        if (!ok) break;
-        for (int x = 0; x < NT && ok; ++x) {
-          if (j >= ntile[x]) continue;
-          ok = wait_w(bar(C::kBarP + x), j & 1);
+        if (it.n_kv == 1) commit(bar(C::kBarQFree));  // the item's only Q K^T
+        commit(bar(C::kBarEmpty + stage_of(T)));
+        for (int j = 0; j < it.n_kv && ok; ++j) {
+          const int64_t tV = T + 2 * j + 1, tK = T + 2 * j + 2;
+          const int sV = stage_of(tV), sK = stage_of(tK);
+          const bool next = j + 1 < it.n_kv;
+          bool k_ready = false;
+          ok = wait_w(bar(C::kBarFull + sV), phase_of(tV));
           if (!ok) break;
-          tc_fence_after();
-          pv_half(x, sV, 0, j > 0, x);
-          ok = wait_w(bar(C::kBarP2 + x), j & 1);
-          if (!ok) break;
-          tc_fence_after();
-          pv_half(x, sV, 1, true, x);
-          if (j == ntile[x] - 1) commit(bar(C::kBarO + x));
-          if (j + 1 < ntile[x]) {
-            if (!k_ready) {
-              ok = wait_w(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
-            }
-            qk(x, sK, x);
-            commit(bar(C::kBarS + x));
-          }
-        }
-        if (!ok) break;
-        commit(bar(C::kBarEmpty + sV));
-        if (next) {
-          if (!k_ready) {  // K(j+1) is used by no tile: still consume it in order
-            ok = wait_w(bar(C::kBarFull + sK), (tK / C::kStages) & 1);
+          for (int x = 0; x < NT && ok; ++x) {
+            if (j >= it.ntile[x]) continue;
+            const uint32_t ph = static_cast<uint32_t>((sc[x] + j) & 1);
+            ok = wait_w(bar(C::kBarP + x), ph);
             if (!ok) break;
+            tc_fence_after();
+            pv_half(x, sV, 0, j > 0, x);
+            ok = wait_w(bar(C::kBarP2 + x), ph);
+            if (!ok) break;
+            tc_fence_after();
+            pv_half(x, sV, 1, true, x);
+            if (j == it.ntile[x] - 1) commit(bar(C::kBarO + x));
+            if (j + 1 < it.ntile[x]) {
+              if (!k_ready) {
+                ok = wait_w(bar(C::kBarFull + sK), phase_of(tK));
+                if (!ok) break;
+                tc_fence_after();
+                k_ready = true;
+              }
+              qk(x, sK, x);
+              commit(bar(C::kBarS + x));
+            }
           }
-          commit(bar(C::kBarEmpty + sK));
+          if (!ok) break;
+          if (j + 2 == it.n_kv) commit(bar(C::kBarQFree));  // the item's last Q K^T
+          commit(bar(C::kBarEmpty + sV));
+          if (next) {
+            if (!k_ready) {  // K(j+1) is used by no tile: still consume it in order
+              ok = wait_w(bar(C::kBarFull + sK), phase_of(tK));
+              if (!ok) break;
+            }
+            commit(bar(C::kBarEmpty + sK));
+          }
         }
       }
-      }  // one score buffer per tile
-      // All issued MMAs must complete before TMEM is released (bounded wait
-      // that ignores the abort flag).
-      commit(bar(C::kBarDrain));
-      volatile int no_abort = 0;
-      const Waiter own{&no_abort, p.status, p.timeout_ns};
-      own(bar(C::kBarDrain), 0);
+      T += 2 * it.n_kv;
+      for (int x = 0; x < NT; ++x) sc[x] += it.ntile[x];
+      ++q_uses;
     }
+    // All issued MMAs must complete before TMEM is released (bounded wait
+    // that ignores the abort flag).
+    commit(bar(C::kBarDrain));
+    volatile int no_abort = 0;
+    const Waiter own{&no_abort, p.status, p.timeout_ns};
+    own(bar(C::kBarDrain), 0);
   } else {
     // ------------------------------------------------------------ softmax
     const int x = warp >> 2;  // query tile
     const int row_in_tile = ((warp & 3) << 5) + lane;
-    const int64_t row0 = q0 + x * BM;
-    const int64_t row = row0 + row_in_tile;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS0 = tmem + lane_off + C::kColS + 128 * x;  // (first) score buffer
     const uint32_t tO = tmem + lane_off + C::kColO + C::kOStride * x;
-    const int n = ntile[x];
-    // Last admissible key of this row and of the tile's first row.
-    const int64_t lim = p.causal ? min(p.Nk - 1, row + p.qoff) : p.Nk - 1;
-    const int64_t lim_tile = p.causal ? min(p.Nk - 1, row0 + p.qoff) : p.Nk - 1;
-
-    float m_run = -INFINITY;  // running maximum of scaled scores (log2 units)
-    float m_ref = -INFINITY;  // exponent reference shared by o and l
-    float l = 0.0f;
+    int64_t sc = 0;  // score tiles of this query tile handled so far
+    int o_uses = 0;  // items in which this query tile had keys (O barrier phases)
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      // Score slot and barrier phase of this tile: the tile's own slot with
-      // one buffer, alternating buffers (each used every other tile) with two.
-      const int slot = SB == 2 ? (j & 1) : x;
-      const uint32_t ph = SB == 2 ? static_cast<uint32_t>((j >> 1) & 1) : static_cast<uint32_t>(j & 1);
-      const uint32_t tS = tS0 + 128 * (SB == 2 ? (j & 1) : 0);
-      // tcgen05.ld/st below are warp-collective: the warp leaves together.
-      ok = __all_sync(0xffffffffu, wait(bar(C::kBarS + slot), ph));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[128];
-      // The load returns the row maximum of the unmasked tile.
-      float tmax = tmem_ld_max_x128(tS, sr);
-      float s[128];
+    for (int64_t k = 0; ok; ++k) {
+      const int64_t idx = item_of(k, cta, G, n_items);
+      if (idx < 0) break;
+      const Item it = decode_item<NT>(idx, p);
+      const int64_t row0 = it.q0 + x * BM;
+      const int64_t row = row0 + row_in_tile;
+      const int n = it.ntile[x];
+      // Last admissible key of this row and of the tile's first row.
+      const int64_t lim = p.causal ? min(p.Nk - 1, row + p.qoff) : p.Nk - 1;
+      const int64_t lim_tile = p.causal ? min(p.Nk - 1, row0 + p.qoff) : p.Nk - 1;
+
+      float m_run = -INFINITY;  // running maximum of scaled scores (log2 units)
+      float m_ref = -INFINITY;  // exponent reference shared by o and l
+      float l = 0.0f;
+      for (int j = 0; j < n; ++j) {
+        // Score slot and barrier phase of this tile: the tile's own slot with
+        // one buffer, alternating buffers (each used every other tile) with
+        // two.
+        const int64_t g = sc + j;
+        const int slot = SB == 2 ? static_cast<int>(g & 1) : x;
+        const uint32_t ph = static_cast<uint32_t>(SB == 2 ? ((g >> 1) & 1) : (g & 1));
+        const uint32_t tS = tS0 + 128 * (SB == 2 ? static_cast<uint32_t>(g & 1) : 0u);
+        // tcgen05.ld/st below are warp-collective: the warp leaves together.
+        ok = __all_sync(0xffffffffu, wait(bar(C::kBarS + slot), ph));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
+        // The load returns the row maximum of the unmasked tile.
+        float tmax = tmem_ld_max_x128(tS, sr);
+        float s[128];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
-      const int64_t k0 = static_cast<int64_t>(j) * BN;
-      if (k0 + BN - 1 > lim_tile) {  // edge or diagonal tile (uniform per tile)
-        const int64_t rel64 = lim - k0;
-        const int rel = static_cast<int>(rel64 < -1 ? -1 : (rel64 > BN ? BN : rel64));
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        const int64_t k0 = static_cast<int64_t>(j) * BN;
+        if (k0 + BN - 1 > lim_tile) {  // edge or diagonal tile (uniform per tile)
+          const int64_t rel64 = lim - k0;
+          const int rel = static_cast<int>(rel64 < -1 ? -1 : (rel64 > BN ? BN : rel64));
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = (c > rel) ? -INFINITY : s[c];
-        // Masking invalidates the load's maximum: eight independent
-        // 16-element chains of 3-input maxima over the masked row.
-        float mx[8];
+          for (int c = 0; c < 128; ++c) s[c] = (c > rel) ? -INFINITY : s[c];
+          // Masking invalidates the load's maximum: eight independent
+          // 16-element chains of 3-input maxima over the masked row.
+          float mx[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          mx[g] = fmaxf(s[16 * g], s[16 * g + 1]);
+          for (int gg = 0; gg < 8; ++gg) {
+            mx[gg] = fmaxf(s[16 * gg], s[16 * gg + 1]);
 #pragma unroll
-          for (int c = 2; c < 16; c += 2) mx[g] = fmax3f(mx[g], s[16 * g + c], s[16 * g + c + 1]);
+            for (int c = 2; c < 16; c += 2)
+              mx[gg] = fmax3f(mx[gg], s[16 * gg + c], s[16 * gg + c + 1]);
+          }
+          tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                        fmaxf(mx[6], mx[7]));
         }
-        tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
-                      fmaxf(mx[6], mx[7]));
-      }
-      const float m_new = fmaxf(m_run, tmax * p.sc_log2);
-      m_run = m_new;
-      float alpha = 1.0f;
-      bool rescale = false;
-      if (m_new > m_ref + kRescaleThreshold) {
-        alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
-        rescale = (m_ref != -INFINITY);
-        l *= alpha;
-        m_ref = m_new;
-      }
-      if constexpr (SB == 2) {
-        // With two score buffers P V of the previous tile may still be
-        // running: an O rescale waits for it first (rare: the threshold).
-        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-          ok = __all_sync(0xffffffffu, wait(bar(C::kBarOStep), (j - 1) & 1));
-          if (!ok) break;
-          tc_fence_after();
+        const float m_new = fmaxf(m_run, tmax * p.sc_log2);
+        m_run = m_new;
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (m_new > m_ref + kRescaleThreshold) {
+          alpha = ex2_approx(m_ref - m_new);  // 0 when m_ref = -inf
+          rescale = (m_ref != -INFINITY);
+          l *= alpha;
+          m_ref = m_new;
         }
-      }
-      const float neg_ref = (m_ref == -INFINITY) ? 0.0f : -m_ref;
-      // p = 2^(s * scale * log2 e - m_ref), two lanes per instruction; the
-      // row sum uses four independent packed accumulators.  P goes back to
-      // tensor memory in two halves (keys 0-63, then 64-127), each announced
-      // on its own barrier, so the first half of P V starts while the second
-      // half is exponentiated.  The rare O rescale lands before the first
-      // announcement.
-      const uint64_t scale2 = f2_pack(p.sc_log2, p.sc_log2);
-      const uint64_t bias2 = f2_pack(neg_ref, neg_ref);
-      uint64_t acc2[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc2[i] = 0ull;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int cc = 32 * h + c;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(s[2 * cc], s[2 * cc + 1]), scale2, bias2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_x32(tS + 32 * h, pk);
-        if (h == 0 && __any_sync(0xffffffffu, rescale) && j > 0) {
-#pragma unroll 1
-          for (int cc = 0; cc < DV / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld_x32(tO + cc * 32, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st_x32(tO + cc * 32, o);
+        if constexpr (SB == 2) {
+          // With two score buffers P V of the previous tile may still be
+          // running: an O rescale waits for it first (rare: the threshold).
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+            ok = __all_sync(0xffffffffu, wait(bar(C::kBarOStep), static_cast<uint32_t>((g - 1) & 1)));
+            if (!ok) break;
+            tc_fence_after();
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar((h == 0 ? C::kBarP : C::kBarP2) + slot));
+        const float neg_ref = (m_ref == -INFINITY) ? 0.0f : -m_ref;
+        // p = 2^(s * scale * log2 e - m_ref), two lanes per instruction; the
+        // row sum uses four independent packed accumulators.  P goes back to
+        // tensor memory in two halves (keys 0-63, then 64-127), each announced
+        // on its own barrier, so the first half of P V starts while the second
+        // half is exponentiated.  The rare O rescale lands before the first
+        // announcement.
+        const uint64_t scale2 = f2_pack(p.sc_log2, p.sc_log2);
+        const uint64_t bias2 = f2_pack(neg_ref, neg_ref);
+        uint64_t acc2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc2[i] = 0ull;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int cc = 32 * h + c;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(s[2 * cc], s[2 * cc + 1]), scale2, bias2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_x32(tS + 32 * h, pk);
+          if (h == 0 && __any_sync(0xffffffffu, rescale) && j > 0) {
+#pragma unroll 1
+            for (int cc = 0; cc < DV / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld_x32(tO + cc * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st_x32(tO + cc * 32, o);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar((h == 0 ? C::kBarP : C::kBarP2) + slot));
+        }
+        float sum_lo, sum_hi;
+        f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
+        l += sum_lo + sum_hi;
       }
-      float sum_lo, sum_hi;
-      f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
-      l += sum_lo + sum_hi;
-    }
-    if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, wait(bar(C::kBarO + x), 0));
-      if (ok) tc_fence_after();
-    }
-    if (ok) {
+      if (!ok) break;
+      if (n > 0) {
+        ok = __all_sync(0xffffffffu, wait(bar(C::kBarO + x), static_cast<uint32_t>(o_uses & 1)));
+        if (!ok) break;
+        tc_fence_after();
+      }
       const bool valid = row < p.Nq;
       const bool empty = (n == 0) || !(l > 0.0f);
+      uint4* dst = reinterpret_cast<uint4*>(p.o + (it.bh * p.Nq + row) * DV);
       if (n > 0) {
         const float inv = empty ? 0.0f : 1.0f / l;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * DV);
 #pragma unroll 1
         for (int cc = 0; cc < DV / 32; ++cc) {
           uint32_t o[32];
@@ -622,12 +704,13 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
           }
         }
       } else if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (bh * p.Nq + row) * DV);
         for (int i = 0; i < DV / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       }
       if (valid)
-        p.lse[bh * p.Nq + row] =
+        p.lse[it.bh * p.Nq + row] =
             empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
+      sc += n;
+      o_uses += n > 0 ? 1 : 0;
     }
   }
 
@@ -659,17 +742,33 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap& tq, const CUtensorMap& t
   p.H = a.H;
   p.group = a.group;
   p.n_qblk = static_cast<int>((a.Nq + NT * BM - 1) / (NT * BM));
-  // Scheduling groups: whole K/V heads whose K and V take about 48 MB of L2.
-  const double kv_head_bytes =
-      static_cast<double>(a.Nk) * (D * (FP8 ? 1.0 : 2.0) + DV * 2.0);
-  const int64_t kv_fit = std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / kv_head_bytes));
   p.n_bh = a.BH;
-  p.heads_per_group = std::min<int64_t>(a.BH, kv_fit * a.group);
   p.causal = a.causal;
   p.sc_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634074);
   p.flags = a.flags;
   p.timeout_ns = a.timeout_ns;
-  const int64_t blocks = a.BH * p.n_qblk;
+  // Persistent grid: as many CTAs as fit on the GPU at once (one per SM for
+  // 512 TMEM columns, two for 256), each walking its share of the work
+  // items, so that CTA start-up, the first Q load and the last item's
+  // epilogue are paid once per CTA instead of once per item.
+  int dev = 0, sms = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const int64_t per_sm = C::kTmemCols == 512 ? 1 : 2;
+  const int64_t n_items = a.BH * p.n_qblk;
+  const int64_t resident = std::min<int64_t>(n_items, std::max(sms, 1) * per_sm);
+  // Causal scheduling chunks: pairs of rounds of the grid (a heavy and a
+  // light item per CTA), as many pairs as keep the chunk's K and V within
+  // about 48 MB of L2 (query heads sharing a K/V head count once).
+  const double kv_head_bytes =
+      static_cast<double>(a.Nk) * (D * (FP8 ? 1.0 : 2.0) + DV * 2.0);
+  const double pair_kv_bytes =
+      static_cast<double>(2 * resident) / p.n_qblk / static_cast<double>(a.group) * kv_head_bytes;
+  const int64_t pairs = std::max<int64_t>(1, static_cast<int64_t>(48.0e6 / pair_kv_bytes));
+  p.chunk = std::min<int64_t>(n_items, 2 * resident * pairs);
+  const int64_t blocks = resident;
   attn_fwd_tcgen05_kernel<D, DV, FP8, NT, SB><<<dim3(static_cast<unsigned>(blocks)), dim3(C::kThreads),
                                C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -70,6 +70,9 @@ def parse_args():
     ap.add_argument("--prefill-d64-profile", action="store_true",
                     help="run only the d = 64 causal prefill (its own size is small enough "
                          "for ncu captures) and print its TFLOPS")
+    ap.add_argument("--seqlen-sweep", action="store_true",
+                    help="latency and peak device memory of the forward and the backward as "
+                         "the sequence length grows (B2 H32 d128 causal, N = 1k .. 32k)")
     ap.add_argument("--bwd-profile-batch", type=int, default=0,
                     help="run only the backward of the long causal prefill with this batch "
                          "size (smaller cases for ncu captures) and print its TFLOPS")
@@ -350,6 +353,56 @@ def summary_of(line: dict) -> list:
     return [o for o in out if o is not None]
 
 
+def run_seqlen_sweep(args, dev, stream, pk) -> list:
+    """Forward and backward latency and peak device memory as N grows, at
+    the long prefill's head shape (B2 H32 d128, causal).  Peak memory is
+    torch's allocator high-water mark over the call (inputs, outputs and the
+    backward's workspace: the library allocates nothing); the unfused score
+    matrix a non-fused forward would hold (fp32 [B, H, N, N]) is listed
+    beside it."""
+    from attention_attn_fwd_07_gb300 import binding
+    rows = []
+    for N in (1024, 2048, 4096, 8192, 16384, 32768):
+        w = W.Workload(f"B2 H32 N{N} d128 causal", 2, 32, N, N, 128, True, 1011)
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        q, k, v = W.make_qkv(w, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, N), dtype=torch.float32, device=dev)
+
+        def f():
+            binding.attn_fwd(q, k, v, True, w.scale, o=o, lse=lse, stream=stream)
+
+        for _ in range(args.warmup):
+            f()
+        fwd_ms = launch_stats(event_time_each(f, 10, stream))["median"]
+        fwd_peak = torch.cuda.max_memory_allocated(dev) - base
+        dout = W.make_dout(w, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty((binding.attn_bwd_workspace_bytes(w.B, w.H, N),), dtype=torch.uint8,
+                         device=dev)
+
+        def b():
+            binding.attn_bwd(q, k, v, o, lse, dout, True, w.scale, workspace=ws, dq=dq, dk=dk,
+                             dv=dv, stream=stream)
+
+        for _ in range(args.warmup):
+            b()
+        bwd_ms = launch_stats(event_time_each(b, 10, stream))["median"]
+        bwd_peak = torch.cuda.max_memory_allocated(dev) - base
+        fl = prefill_flops(w)
+        rows.append({"N": N, "fwd_ms": fwd_ms, "fwd_tflops": fl / (fwd_ms / 1e3) / 1e12,
+                     "fwd_peak_bytes": int(fwd_peak), "bwd_ms": bwd_ms,
+                     "bwd_tflops": 2.5 * fl / (bwd_ms / 1e3) / 1e12,
+                     "bwd_peak_bytes": int(bwd_peak),
+                     "unfused_scores_bytes": int(w.B * w.H * N * N * 4),
+                     "fwd_frac": fl / (fwd_ms / 1e3) / 1e12 / pk["bf16_tflops"]})
+        print(json.dumps(rows[-1]), flush=True)
+        del q, k, v, o, lse, dout, dq, dk, dv, ws
+    return rows
+
+
 def run_backward(w, q, k, v, o, lse, dev, stream, args, pk, pk_src, world, max_over_ranks):
     """Time attn_bwd (three launches) on the workload's forward outputs."""
     from attention_attn_fwd_07_gb300 import binding
@@ -424,6 +477,10 @@ def main():
         m, st = event_time_flushed(sp, args.steps, stream, scratch)
         print(json.dumps({"workload": wp.name, "ms_per_step": m, "launch_ms": st,
                           "TFLOPS": prefill_flops(wp) / (m / 1e3) / 1e12}), flush=True)
+        return 0
+
+    if args.seqlen_sweep:
+        run_seqlen_sweep(args, dev, stream, pk)
         return 0
 
     if args.bwd_profile_batch > 0:
