@@ -67,9 +67,10 @@ def parse_args():
     ap.add_argument("--decode-profile-gqa8", action="store_true",
                     help="with --decode-profile-batch: the decode with eight query heads per "
                          "K/V head (tensor-core partial kernel)")
-    ap.add_argument("--prefill-d64-profile", action="store_true",
-                    help="run only the d = 64 causal prefill (its own size is small enough "
-                         "for ncu captures) and print its TFLOPS")
+    ap.add_argument("--prefill-profile", choices=["d64", "d96", "d256"], default=None,
+                    help="run only this causal prefill workload (B4 H16 N2048 d64, or the "
+                         "long prefill's bytes at d96 / d256; each small enough for ncu "
+                         "captures) and print its TFLOPS")
     ap.add_argument("--seqlen-sweep", action="store_true",
                     help="latency and peak device memory of the forward and the backward as "
                          "the sequence length grows (B2 H32 d128 causal, N = 1k .. 32k)")
@@ -460,10 +461,11 @@ def main():
 
     launches = 0
 
-    if args.prefill_d64_profile:
-        # The d = 64 prefill alone, L2 flushed before each timed launch as in
-        # the full run.
-        wp = W.PREFILL
+    if args.prefill_profile:
+        # One prefill workload alone, L2 flushed before each timed launch as
+        # in the full run.
+        wp = {"d64": W.PREFILL, "d96": W.LONG_PREFILL_D96,
+              "d256": W.LONG_PREFILL_D256}[args.prefill_profile]
         qp, kp, vp = W.make_qkv(wp, device=dev)
         op = torch.empty_like(qp)
         lp = torch.empty((wp.B, wp.H, wp.Nq), dtype=torch.float32, device=dev)
