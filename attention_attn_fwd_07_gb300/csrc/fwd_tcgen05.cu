@@ -1033,15 +1033,7 @@ __global__ void __launch_bounds__(threads_for(1), 2)
           l *= alpha;
           m_ref = m_new;
         }
-        if constexpr (PS) {
-          // P V of the previous tile must have read P's columns before they
-          // are rewritten (and O before it is rescaled).
-          if (j > 0) {
-            ok = __all_sync(0xffffffffu, wait(bar(C::kBarOStep), static_cast<uint32_t>((g - 1) & 1)));
-            if (!ok) break;
-            tc_fence_after();
-          }
-        } else if constexpr (SB == 2) {
+        if constexpr (SB == 2) {
           // With two score buffers P V of the previous tile may still be
           // running: an O rescale waits for it first (rare: the threshold).
           if (j > 0 && __any_sync(0xffffffffu, rescale)) {
@@ -1075,6 +1067,17 @@ __global__ void __launch_bounds__(threads_for(1), 2)
             acc2[c & 3] = f2_add(acc2[c & 3], f2_pack(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
           }
+          if constexpr (PS) {
+            // P V of the previous tile must have read P's columns before
+            // they are rewritten (and O before it is rescaled); the wait
+            // comes after the first half's exponentials, which hide it.
+            if (h == 0 && j > 0) {
+              ok = __all_sync(0xffffffffu,
+                              wait(bar(C::kBarOStep), static_cast<uint32_t>((g - 1) & 1)));
+              if (!ok) break;
+              tc_fence_after();
+            }
+          }
           tmem_st_x32((PS ? tP : tS) + 32 * h, pk);
           if (h == 0 && __any_sync(0xffffffffu, rescale) && j > 0) {
 #pragma unroll 1
@@ -1091,6 +1094,7 @@ __global__ void __launch_bounds__(threads_for(1), 2)
           __syncwarp();
           if (lane == 0) mbar_arrive(bar((h == 0 ? C::kBarP : C::kBarP2) + slot));
         }
+        if (!ok) break;
         float sum_lo, sum_hi;
         f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), sum_lo, sum_hi);
         l += sum_lo + sum_hi;
