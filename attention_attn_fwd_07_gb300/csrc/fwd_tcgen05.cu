@@ -232,15 +232,20 @@ __device__ __forceinline__ Item decode_item(int64_t idx, const KParams& p) {
   Item it;
   int64_t qb;
   const int64_t nq = p.n_qblk;
+  // Item indices and counts are below 2^31 (checked on the host): 32-bit
+  // divisions (64-bit ones are slow software routines).
+  const uint32_t nq32 = static_cast<uint32_t>(nq);
+  const uint32_t idx32 = static_cast<uint32_t>(idx);
   if (p.causal) {
-    const int64_t n_items = p.n_bh * nq;
-    const int64_t a = (idx / p.chunk) * p.chunk;        // chunk [a, e) of the (b, h)-major list
-    const int64_t e = min(a + p.chunk, n_items);
-    const int64_t h_first = a / nq, h_last = (e - 1) / nq;
-    const int64_t a0 = a % nq, e0 = (e - 1) % nq;       // first block of h_first, last of h_last
+    const uint32_t chunk = static_cast<uint32_t>(p.chunk);
+    const uint32_t n_items = static_cast<uint32_t>(p.n_bh) * nq32;
+    const uint32_t a = (idx32 / chunk) * chunk;        // chunk [a, e) of the (b, h)-major list
+    const uint32_t e = min(a + chunk, n_items);
+    const int64_t h_first = a / nq32, h_last = (e - 1) / nq32;
+    const int64_t a0 = a % nq32, e0 = (e - 1) % nq32;  // first block of h_first, last of h_last
     // Rank r inside the chunk: query blocks from the last down, the chunk's
     // heads holding that block in (b, h) order.
-    int64_t r = idx - a;
+    int64_t r = idx32 - a;
     for (qb = nq - 1;; --qb) {
       const int64_t lo = qb >= a0 ? h_first : h_first + 1;
       const int64_t hi = qb <= e0 ? h_last : h_last - 1;
@@ -252,12 +257,14 @@ __device__ __forceinline__ Item decode_item(int64_t idx, const KParams& p) {
       r -= cnt;
     }
   } else {
-    it.bh = idx / nq;
-    qb = idx % nq;
+    it.bh = idx32 / nq32;
+    qb = idx32 % nq32;
   }
   it.q0 = qb * (NT * BM);
   // K/V head of this query head (grouped K/V heads: H / group per batch).
-  it.bkv = (it.bh / p.H) * (p.H / p.group) + (it.bh % p.H) / p.group;
+  const uint32_t bh32 = static_cast<uint32_t>(it.bh);
+  const uint32_t H32 = static_cast<uint32_t>(p.H), G32 = static_cast<uint32_t>(p.group);
+  it.bkv = (bh32 / H32) * (H32 / G32) + (bh32 % H32) / G32;
   it.ntile[0] = tiles_for(it.q0, p);
   it.ntile[1] = NT == 2 ? tiles_for(it.q0 + BM, p) : 0;
   it.n_kv = max(it.ntile[0], it.ntile[1]);
@@ -298,22 +305,35 @@ __global__ void __launch_bounds__(threads_for(NT), 3 - NT)
   // (b, h) slices whose K and V fit in L2 together; inside a group the CTAs
   // go longest-first (last query block first, then by head), so the CTAs
   // dispatched last are short and K/V are read from DRAM about once.
+  // Item indices, head counts and block counts are below 2^31 (checked on
+  // the host), so the divisions run in 32 bits: 64-bit ones are software
+  // routines that held every CTA's start back by ~1800 cycles.
   int64_t bh;
   int qb;
-  if (p.causal) {
-    const int64_t per_group = p.heads_per_group * p.n_qblk;
-    const int64_t h0 = (blockIdx.x / per_group) * p.heads_per_group;
-    const int64_t r = blockIdx.x % per_group;
-    const int64_t gh = min(p.heads_per_group, p.n_bh - h0);  // the last group may be smaller
-    bh = h0 + r % gh;
-    qb = p.n_qblk - 1 - static_cast<int>(r / gh);
-  } else {
-    bh = blockIdx.x / p.n_qblk;
-    qb = static_cast<int>(blockIdx.x % p.n_qblk);
+  {
+    const uint32_t idx = blockIdx.x;
+    const uint32_t nq = static_cast<uint32_t>(p.n_qblk);
+    uint32_t h32, q32;
+    if (p.causal) {
+      const uint32_t hpg = static_cast<uint32_t>(p.heads_per_group);
+      const uint32_t per_group = hpg * nq;
+      const uint32_t h0 = (idx / per_group) * hpg;
+      const uint32_t r = idx % per_group;
+      const uint32_t gh = min(hpg, static_cast<uint32_t>(p.n_bh) - h0);  // the last group may be smaller
+      h32 = h0 + r % gh;
+      q32 = nq - 1 - r / gh;
+    } else {
+      h32 = idx / nq;
+      q32 = idx % nq;
+    }
+    bh = h32;
+    qb = static_cast<int>(q32);
   }
   const int64_t q0 = static_cast<int64_t>(qb) * (NT * BM);
   // K/V head of this query head (grouped K/V heads: H / group per batch).
-  const int64_t bkv = (bh / p.H) * (p.H / p.group) + (bh % p.H) / p.group;
+  const uint32_t H32 = static_cast<uint32_t>(p.H), G32 = static_cast<uint32_t>(p.group);
+  const int64_t bkv = (static_cast<uint32_t>(bh) / H32) * (H32 / G32) +
+                      (static_cast<uint32_t>(bh) % H32) / G32;
   int ntile[2];
   ntile[0] = tiles_for(q0, p);
   ntile[1] = NT == 2 ? tiles_for(q0 + BM, p) : 0;
