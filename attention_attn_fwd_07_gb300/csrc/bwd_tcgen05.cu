@@ -306,9 +306,9 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 // have advanced.
 template <typename LoadA, typename LoadB>
 __device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, const BwdParams& p,
-                                           int64_t n_items, LoadA load_a, LoadB load_b) {
-  int64_t last_a = -1, last_b = -1;
-  for (int64_t n = 0; n < n_items; ++n) {
+                                           int n_items, LoadA load_a, LoadB load_b) {
+  int last_a = -1, last_b = -1;
+  for (int n = 0; n < n_items; ++n) {
     const int sa = static_cast<int>(n % kStagesA), sb = static_cast<int>(n % kStagesB);
     if (n >= kStagesA &&
         !wait(c.bar(kBarEmptyA + sa), static_cast<uint32_t>(((n / kStagesA) - 1) & 1)))
@@ -326,10 +326,10 @@ __device__ __forceinline__ void run_loader(const Ctx& c, const Waiter& wait, con
   volatile int no_abort = 0;
   const Waiter own{&no_abort, p.status, p.timeout_ns};
   own(c.bar(kBarRes), 0);
-  for (int64_t n = last_a - kStagesA + 1; n <= last_a; ++n)
-    if (n >= 0) own(c.bar(kBarFullA + static_cast<int>(n % kStagesA)), (n / kStagesA) & 1);
-  for (int64_t n = last_b - kStagesB + 1; n <= last_b; ++n)
-    if (n >= 0) own(c.bar(kBarFullB + static_cast<int>(n % kStagesB)), (n / kStagesB) & 1);
+  for (int n = last_a - kStagesA + 1; n <= last_a; ++n)
+    if (n >= 0) own(c.bar(kBarFullA + n % kStagesA), static_cast<uint32_t>((n / kStagesA) & 1));
+  for (int n = last_b - kStagesB + 1; n <= last_b; ++n)
+    if (n >= 0) own(c.bar(kBarFullB + n % kStagesB), static_cast<uint32_t>((n / kStagesB) & 1));
 }
 
 // ======================================================================= dK, dV
@@ -350,17 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // streamed Q and dO fit in L2 together; inside a group key tiles go in
   // ascending order (under a causal mask the first key tiles see the most
   // query tiles), so the CTAs dispatched last are the shortest.
+  // Item and head indices are below 2^31 (checked on the host): the
+  // divisions run in 32 bits (64-bit ones are slow software routines).
   const int64_t n_kt = (p.Nk + T - 1) / T;
   int64_t bkv, k0;
   {
-    const int64_t per_group = p.kv_per_group * n_kt;
-    const int64_t u0 = (blockIdx.x / per_group) * p.kv_per_group;
-    const int64_t r = blockIdx.x % per_group;
-    const int64_t gu = min(p.kv_per_group, p.B * p.Hkv - u0);
+    const uint32_t kvg = static_cast<uint32_t>(p.kv_per_group);
+    const uint32_t per_group = kvg * static_cast<uint32_t>(n_kt);
+    const uint32_t u0 = (blockIdx.x / per_group) * kvg;
+    const uint32_t r = blockIdx.x % per_group;
+    const uint32_t gu = min(kvg, static_cast<uint32_t>(p.B * p.Hkv) - u0);
     bkv = u0 + r % gu;
-    k0 = (r / gu) * T;
+    k0 = static_cast<int64_t>(r / gu) * T;
   }
-  const int64_t b = bkv / p.Hkv, hk = bkv % p.Hkv, G = p.H / p.Hkv;
+  const uint32_t Hkv32 = static_cast<uint32_t>(p.Hkv);
+  const int64_t b = static_cast<uint32_t>(bkv) / Hkv32, hk = static_cast<uint32_t>(bkv) % Hkv32;
+  const int64_t G = static_cast<uint32_t>(p.H) / Hkv32;
   const int64_t n_qt = (p.Nq + T - 1) / T;
   // First query tile whose rows can see a key of this tile (causal).
   int64_t qt_first = 0;
@@ -369,20 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     qt_first = need <= 0 ? 0 : (need + T - 1) / T;
   }
   const int64_t per_head = qt_first < n_qt ? n_qt - qt_first : 0;
-  const int64_t n_items = G * per_head;
-  auto item_rows = [&](int64_t n, int64_t& bh, int64_t& q0) {
-    const int64_t g = n / per_head;
+  const int n_items = static_cast<int>(G * per_head);  // < 2^31 (host check)
+  const uint32_t per_head32 = per_head > 0 ? static_cast<uint32_t>(per_head) : 1u;
+  auto item_rows = [&](int n, int64_t& bh, int64_t& q0) {
+    const uint32_t g = static_cast<uint32_t>(n) / per_head32;
     bh = b * p.H + hk * G + g;
-    q0 = (qt_first + n % per_head) * T;
+    q0 = (qt_first + static_cast<uint32_t>(n) % per_head32) * T;
   };
 
   const uint32_t sK = c.sbase + kOffRes, sV = c.sbase + kOffRes2;
-  auto sQ = [&](int64_t n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kQKTileBytes; };
-  auto sdO = [&](int64_t n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kVTileBytes; };
-  auto slot_a = [](int64_t n) { return static_cast<int>(n % kStagesA); };
-  auto slot_b = [](int64_t n) { return static_cast<int>(n % kStagesB); };
-  auto par_a = [](int64_t n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
-  auto par_b = [](int64_t n) { return static_cast<uint32_t>((n / kStagesB) & 1); };
+  auto sQ = [&](int n) { return c.sbase + kOffRingA + static_cast<uint32_t>(n % kStagesA) * kQKTileBytes; };
+  auto sdO = [&](int n) { return c.sbase + kOffRingB + static_cast<uint32_t>(n % kStagesB) * kVTileBytes; };
+  auto slot_a = [](int n) { return n % kStagesA; };
+  auto slot_b = [](int n) { return n % kStagesB; };
+  auto par_a = [](int n) { return static_cast<uint32_t>((n / kStagesA) & 1); };
+  auto par_b = [](int n) { return static_cast<uint32_t>((n / kStagesB) & 1); };
   const uint32_t tS = c.tmem + 0, tdP = c.tmem + 128, tdV = c.tmem + kColDV,
                  tdK = c.tmem + kColDK;
 
@@ -393,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_tile<DV>(sV, &tv, c.bar(kBarRes), static_cast<int>(k0), bkv);
       run_loader(
           c, wait, p, n_items,
-          [&](int64_t n, uint32_t bar) {
+          [&](int n, uint32_t bar) {
             int64_t bh, q0;
             item_rows(n, bh, q0);
             load_tile<D>(sQ(n), &tq, bar, static_cast<int>(q0), bh);
           },
-          [&](int64_t n, uint32_t bar) {
+          [&](int n, uint32_t bar) {
             int64_t bh, q0;
             item_rows(n, bh, q0);
             load_tile<DV>(sdO(n), &tdo, bar, static_cast<int>(q0), bh);
@@ -415,11 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, wait(b, parity));
     };
     if (n_items > 0) {
-      auto issue_s = [&](int64_t n) {  // S^T = K Q^T
+      auto issue_s = [&](int n) {  // S^T = K Q^T
         mma_ss_tiles_w<D>(tS, sK, sQ(n));
         mma_commit_w(c.bar(kBarS));
       };
-      auto issue_dp = [&](int64_t n) {  // dP^T = V dO^T
+      auto issue_dp = [&](int n) {  // dP^T = V dO^T
         mma_ss_tiles_w<DV>(tdP, sV, sdO(n));
         mma_commit_w(c.bar(kBarDP));
       };
@@ -433,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_dp(0);
         }
       }
-      for (int64_t n = 0; n < n_items && ok; ++n) {
+      for (int n = 0; n < n_items && ok; ++n) {
         ok = wait_w(c.bar(kBarP), n & 1);
         if (!ok) break;
         tc_fence_after();
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
     const bool row_live = j < p.Nk;
     bool ok = true;
-    for (int64_t n = 0; n < n_items; ++n) {
+    for (int n = 0; n < n_items; ++n) {
       int64_t bh, q0;
       item_rows(n, bh, q0);
       float* nl2 = stat_buf + (n & 1) * 2 * T;
@@ -609,18 +615,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   // CTA -> (b, h, query tile).  Groups of consecutive query heads whose K
   // and V fit in L2 together; inside a group query tiles go last first
   // (under a causal mask the last query tiles see the most key tiles).
+  // Item and head indices are below 2^31 (checked on the host): 32-bit
+  // divisions.
   const int64_t n_qt = (p.Nq + T - 1) / T;
   int64_t bh, q0;
   {
-    const int64_t per_group = p.q_per_group * n_qt;
-    const int64_t u0 = (blockIdx.x / per_group) * p.q_per_group;
-    const int64_t r = blockIdx.x % per_group;
-    const int64_t gu = min(p.q_per_group, p.B * p.H - u0);
+    const uint32_t qg = static_cast<uint32_t>(p.q_per_group);
+    const uint32_t per_group = qg * static_cast<uint32_t>(n_qt);
+    const uint32_t u0 = (blockIdx.x / per_group) * qg;
+    const uint32_t r = blockIdx.x % per_group;
+    const uint32_t gu = min(qg, static_cast<uint32_t>(p.B * p.H) - u0);
     bh = u0 + r % gu;
-    q0 = (n_qt - 1 - r / gu) * T;
+    q0 = (n_qt - 1 - static_cast<int64_t>(r / gu)) * T;
   }
-  const int64_t b = bh / p.H, h = bh % p.H;
-  const int64_t bkv = b * p.Hkv + h / (p.H / p.Hkv);
+  const uint32_t H32 = static_cast<uint32_t>(p.H), Hkv32 = static_cast<uint32_t>(p.Hkv);
+  const int64_t b = static_cast<uint32_t>(bh) / H32, h = static_cast<uint32_t>(bh) % H32;
+  const int64_t bkv = b * p.Hkv + static_cast<uint32_t>(h) / (H32 / Hkv32);
   int n_kt = static_cast<int>((p.Nk + T - 1) / T);
   if (p.causal) {
     const int64_t last_key = min(q0 + T - 1, p.Nq - 1) + p.qoff;
@@ -643,12 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_tile<DV>(sdO, &tdo, c.bar(kBarRes), static_cast<int>(q0), bh);
       run_loader(
           c, wait, p, n_kt,
-          [&](int64_t n, uint32_t bar) {
-            load_tile<D>(sK(static_cast<int>(n)), &tk, bar, static_cast<int>(n) * T, bkv);
-          },
-          [&](int64_t n, uint32_t bar) {
-            load_tile<DV>(sV(static_cast<int>(n)), &tv, bar, static_cast<int>(n) * T, bkv);
-          });
+          [&](int n, uint32_t bar) { load_tile<D>(sK(n), &tk, bar, n * T, bkv); },
+          [&](int n, uint32_t bar) { load_tile<DV>(sV(n), &tv, bar, n * T, bkv); });
     }
   } else if (warp == kWarpMma) {
     // Issue order per tile n: ... S(n+1) (once tile n's S is read), dQ(n),

@@ -25,7 +25,11 @@
  *    float32 [B][H][Nq].  All tensor pointers are DEVICE pointers owned by the
  *    caller; the library keeps no pointer after a call returns.
  *  - Q, K, V, O and workspaces must be 16-byte aligned; LSE 4-byte aligned.
- *  - d must be 64 or 128 (ATTN_ERR_UNSUPPORTED otherwise).
+ *  - Head dims: d in {64, 96, 128, 256} for the forward entry points (the
+ *    lab of "GPU Engineering" section 22.5 asks for several head
+ *    dimensions); 96 and 256 take dv = d; the backward and
+ *    attn_fwd_splitkv_noalloc take 64 and 128 (ATTN_ERR_UNSUPPORTED
+ *    otherwise).
  *  - B, H, Nq, Nk >= 1 (ATTN_ERR_INVALID otherwise); scale must be finite
  *    and > 0.  Inputs must be finite (a documented precondition, not checked:
  *    a check would cost a full pass over the data).
@@ -53,7 +57,7 @@ extern "C" {
 typedef enum attn_status {
   ATTN_OK = 0,
   ATTN_ERR_INVALID = -1,        /* null pointer, size < 1, bad scale, ...   */
-  ATTN_ERR_UNSUPPORTED = -2,    /* head dim other than 64/128, size limits  */
+  ATTN_ERR_UNSUPPORTED = -2,    /* head dim not supported, size limits      */
   ATTN_ERR_ALIGN = -3,          /* pointer misaligned                       */
   ATTN_ERR_WORKSPACE = -4,      /* split-KV workspace missing or too small  */
   ATTN_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed        */
@@ -103,9 +107,9 @@ typedef struct attn_params {
   int64_t dv;             /* head dim of V and O; 0 = d.  dv may differ from d
                              in attn_fwd_ex (d and dv in {64, 128}; FP8: d =
                              128, dv in {64, 128}) and attn_fwd_splitkv_ex
-                             (bf16, d and dv in {64, 128}); every other entry
-                             point needs dv = d (ATTN_ERR_UNSUPPORTED
-                             otherwise).                                    */
+                             (bf16, d and dv in {64, 128}); head dims 96 and
+                             256, and every other entry point, need dv = d
+                             (ATTN_ERR_UNSUPPORTED otherwise).              */
 } attn_params;
 
 /* attn_params.qk_dtype */
@@ -113,7 +117,8 @@ enum { ATTN_QK_BF16 = 0, ATTN_QK_E4M3 = 1 };
 
 /*
  * Prefill / general forward: O and LSE for all rows, query_offset = 0.
- * tcgen05 (TMEM accumulators) + TMA kernel; any Nq, Nk >= 1.
+ * tcgen05 (TMEM accumulators) + TMA kernels; any Nq, Nk >= 1; d in
+ * {64, 96, 128, 256}.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
              int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
@@ -141,7 +146,8 @@ size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,
  * (grouped K/V heads through attn_fwd_splitkv_ex, or Nq > 1) they are served
  * together -- up to 128 rows per CTA on the tensor cores, or in blocks of
  * four on the CUDA cores at d = 64 with at most four rows -- so each K/V byte
- * is read about once per group.  1 <= num_splits <= 256.  Two launches on
+ * is read about once per group; head dims 96 and 256 always run on the
+ * tensor cores, one row per K/V head included.  1 <= num_splits <= 256.  Two launches on
  * `stream`; `workspace` (device, 16-byte aligned, caller-owned) must hold
  * attn_splitkv_workspace_bytes(...) bytes (ATTN_ERR_WORKSPACE otherwise).
  */
