@@ -33,7 +33,8 @@ ATTN_QK_E4M3 = 1
 
 EXPORTED = ("attn_fwd", "attn_fwd_ex", "attn_fwd_splitkv", "attn_fwd_splitkv_ex",
             "attn_combine", "attn_splitkv_workspace_bytes", "attn_get_device_status",
-            "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes")
+            "attn_status_string", "attn_bwd", "attn_bwd_workspace_bytes",
+            "attn_fwd_from_host")
 
 
 class AttnError(RuntimeError):
@@ -99,6 +100,9 @@ def load_library(path: str | None = None):
         lib.attn_bwd.restype = c_int
         lib.attn_bwd_workspace_bytes.argtypes = [i64, i64, i64]
         lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.attn_fwd_from_host.argtypes = [ctypes.POINTER(attn_params), vp, vp, vp, vp, vp,
+                                           c_int, vp, vp, vp]
+        lib.attn_fwd_from_host.restype = c_int
         lib.attn_status_string.argtypes = [c_int]
         lib.attn_status_string.restype = ctypes.c_char_p
         if path is None:
@@ -309,50 +313,26 @@ def _streams_for(device):
 
 def fwd_from_host(q_host, k_host, v_host, causal: bool, scale: float, q_dev, k_dev, v_dev,
                   o_dev, lse_dev, o_host, lse_host, stream=None, chunk_heads: int = 8):
-    """End-to-end call with pinned host buffers: host -> device copies of Q, K,
-    V, attn_fwd, device -> host copies of O and LSE.
-
-    The work is split into chunks of ``chunk_heads`` query heads of one batch
-    entry (whole K/V heads; every (b, h) slice is independent), and the chunks
-    are pipelined over three streams: uploads on a side stream, attn_fwd on
-    ``stream`` once its chunk has landed, downloads on another side stream once
-    its chunk is computed.  The host link is the bottleneck, so the compute and
-    most of the downloads hide behind the uploads.  ``stream`` waits for the
-    last download before this returns (the host buffers are valid once
-    ``stream`` is synchronised)."""
-    s = torch.cuda.current_stream() if stream is None else stream
+    """End-to-end call with pinned host buffers (the C entry point
+    attn_fwd_from_host): host -> device copies of Q, K, V, the forward,
+    device -> host copies of O and LSE, pipelined in chunks of
+    ``chunk_heads`` query heads of one batch entry over an upload stream,
+    ``stream`` and a download stream (two side streams per device, created
+    once here).  ``stream`` waits for the last download before this returns
+    (the host buffers are valid once ``stream`` is synchronised)."""
+    for t, name in ((q_host, "q_host"), (k_host, "k_host"), (v_host, "v_host"),
+                    (o_host, "o_host"), (lse_host, "lse_host")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if (q_host.shape != q_dev.shape or k_host.shape != k_dev.shape or v_host.shape != v_dev.shape
+            or o_host.shape != o_dev.shape or lse_host.shape != lse_dev.shape):
+        raise ValueError("host and device tensors must have the same shapes")
     up, down = _streams_for(q_dev.device)
-    B, H = q_dev.shape[0], q_dev.shape[1]
-    Hkv = k_dev.shape[1]
-    G = H // Hkv
-    hc = max(G, (min(chunk_heads, H) // G) * G)  # whole groups of query heads
-    start = torch.cuda.Event()
-    start.record(s)
-    up.wait_event(start)
-    down.wait_event(start)
-    for b in range(B):
-        for h0 in range(0, H, hc):
-            h1 = min(H, h0 + hc)
-            g0, g1 = h0 // G, (h1 + G - 1) // G
-            loaded = torch.cuda.Event()
-            with torch.cuda.stream(up):
-                q_dev[b, h0:h1].copy_(q_host[b, h0:h1], non_blocking=True)
-                k_dev[b, g0:g1].copy_(k_host[b, g0:g1], non_blocking=True)
-                v_dev[b, g0:g1].copy_(v_host[b, g0:g1], non_blocking=True)
-                loaded.record(up)
-            s.wait_event(loaded)
-            attn_fwd(q_dev[b:b + 1, h0:h1], k_dev[b:b + 1, g0:g1], v_dev[b:b + 1, g0:g1],
-                     causal, scale, o=o_dev[b:b + 1, h0:h1], lse=lse_dev[b:b + 1, h0:h1],
-                     stream=s)
-            computed = torch.cuda.Event()
-            computed.record(s)
-            down.wait_event(computed)
-            with torch.cuda.stream(down):
-                o_host[b, h0:h1].copy_(o_dev[b, h0:h1], non_blocking=True)
-                lse_host[b, h0:h1].copy_(lse_dev[b, h0:h1], non_blocking=True)
-    done = torch.cuda.Event()
-    done.record(down)
-    s.wait_event(done)
+    p = make_params(q_dev, k_dev, v_dev, o_dev, lse_dev, causal, scale)
+    rc = load_library().attn_fwd_from_host(
+        ctypes.byref(p), _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(o_host), _ptr(lse_host),
+        int(chunk_heads), _stream(stream), up.cuda_stream, down.cuda_stream)
+    _check(rc, "attn_fwd_from_host")
     return o_host, lse_host
 
 

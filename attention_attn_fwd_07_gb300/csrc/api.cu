@@ -5,6 +5,7 @@
 // reported identically with or without a GPU.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -170,6 +171,103 @@ extern "C" int attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   p.causal = causal;
   p.scale = scale;
   return attn_fwd_ex(&p, stream);
+}
+
+namespace {
+
+// One event per use, created without timing; destroying a recorded event
+// before it completes is allowed (its resources are released afterwards).
+cudaError_t record_new_event(cudaEvent_t* ev, cudaStream_t s) {
+  cudaError_t e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecord(*ev, s);
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_from_host(const attn_params* p, const void* q_host, const void* k_host,
+                                  const void* v_host, void* o_host, float* lse_host,
+                                  int chunk_heads, cudaStream_t stream,
+                                  cudaStream_t upload_stream, cudaStream_t download_stream) {
+  int rc = validate(p);
+  if (rc != ATTN_OK) return rc;
+  if (!q_host || !k_host || !v_host || !o_host || !lse_host || chunk_heads < 1)
+    return ATTN_ERR_INVALID;
+  if (p->qk_dtype != ATTN_QK_BF16) return ATTN_ERR_UNSUPPORTED;
+  const int64_t Hkv = p->Hkv > 0 ? p->Hkv : p->H;
+  const int64_t G = p->H / Hkv;  // query heads per K/V head
+  const int64_t dv = p->dv > 0 ? p->dv : p->d;
+  // Chunks of whole K/V head groups of one batch entry: contiguous in every
+  // tensor, and independent of each other.
+  const int64_t hc = std::max<int64_t>(G, (std::min<int64_t>(chunk_heads, p->H) / G) * G);
+  const size_t e2 = 2;  // bf16
+  const size_t q_head = static_cast<size_t>(p->Nq) * p->d * e2;
+  const size_t k_head = static_cast<size_t>(p->Nk) * p->d * e2;
+  const size_t v_head = static_cast<size_t>(p->Nk) * dv * e2;
+  const size_t o_head = static_cast<size_t>(p->Nq) * dv * e2;
+  const size_t l_head = static_cast<size_t>(p->Nq) * sizeof(float);
+  auto at = [](const void* base, size_t off) {
+    return static_cast<const char*>(base) + off;
+  };
+  auto at_w = [](void* base, size_t off) { return static_cast<char*>(base) + off; };
+
+  // The side streams start after the work already queued on `stream` (the
+  // device buffers may still be in use there).
+  cudaEvent_t ev = nullptr;
+  if (record_new_event(&ev, stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  bool fail = cudaStreamWaitEvent(upload_stream, ev, 0) != cudaSuccess ||
+              cudaStreamWaitEvent(download_stream, ev, 0) != cudaSuccess;
+  cudaEventDestroy(ev);
+  for (int64_t b = 0; b < p->B && !fail; ++b) {
+    for (int64_t h0 = 0; h0 < p->H && !fail; h0 += hc) {
+      const int64_t h1 = std::min(p->H, h0 + hc);
+      const int64_t g0 = h0 / G, g1 = (h1 + G - 1) / G;
+      const size_t qo = static_cast<size_t>(b * p->H + h0) * q_head;
+      const size_t ko = static_cast<size_t>(b * Hkv + g0) * k_head;
+      const size_t vo = static_cast<size_t>(b * Hkv + g0) * v_head;
+      const size_t oo = static_cast<size_t>(b * p->H + h0) * o_head;
+      const size_t lo = static_cast<size_t>(b * p->H + h0) * l_head;
+      const size_t nh = static_cast<size_t>(h1 - h0), nkv = static_cast<size_t>(g1 - g0);
+      // Upload the chunk, then compute it on `stream` once it has landed.
+      fail = cudaMemcpyAsync(at_w(const_cast<void*>(p->q), qo), at(q_host, qo), nh * q_head,
+                             cudaMemcpyHostToDevice, upload_stream) != cudaSuccess ||
+             cudaMemcpyAsync(at_w(const_cast<void*>(p->k), ko), at(k_host, ko), nkv * k_head,
+                             cudaMemcpyHostToDevice, upload_stream) != cudaSuccess ||
+             cudaMemcpyAsync(at_w(const_cast<void*>(p->v), vo), at(v_host, vo), nkv * v_head,
+                             cudaMemcpyHostToDevice, upload_stream) != cudaSuccess;
+      if (fail) break;
+      fail = record_new_event(&ev, upload_stream) != cudaSuccess ||
+             cudaStreamWaitEvent(stream, ev, 0) != cudaSuccess;
+      cudaEventDestroy(ev);
+      if (fail) break;
+      attn_params c = *p;
+      c.q = at(p->q, qo);
+      c.k = at(p->k, ko);
+      c.v = at(p->v, vo);
+      c.o = at_w(p->o, oo);
+      c.lse = reinterpret_cast<float*>(at_w(p->lse, lo));
+      c.B = 1;
+      c.H = h1 - h0;
+      c.Hkv = p->Hkv > 0 ? g1 - g0 : 0;
+      rc = attn_fwd_ex(&c, stream);
+      if (rc != ATTN_OK) return rc;
+      // Download the chunk's O and LSE once it is computed.
+      fail = record_new_event(&ev, stream) != cudaSuccess ||
+             cudaStreamWaitEvent(download_stream, ev, 0) != cudaSuccess;
+      cudaEventDestroy(ev);
+      if (fail) break;
+      fail = cudaMemcpyAsync(at_w(o_host, oo), at(p->o, oo), nh * o_head,
+                             cudaMemcpyDeviceToHost, download_stream) != cudaSuccess ||
+             cudaMemcpyAsync(at_w(lse_host, lo), at(p->lse, lo), nh * l_head,
+                             cudaMemcpyDeviceToHost, download_stream) != cudaSuccess;
+    }
+  }
+  // `stream` waits for the last download: the host buffers are complete
+  // once `stream` is.
+  if (record_new_event(&ev, download_stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  const bool joined = cudaStreamWaitEvent(stream, ev, 0) == cudaSuccess;
+  cudaEventDestroy(ev);
+  return fail || !joined ? ATTN_ERR_CUDA : ATTN_OK;
 }
 
 extern "C" size_t attn_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t d,

@@ -577,10 +577,11 @@ def main():
     d2h = o_p.numel() * o_p.element_size() + lse_p.numel() * lse_p.element_size()
     e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "path": "binding.fwd_from_host: pinned host -> device copies of Q, K, V, attn_fwd "
-                   "(C ABI), device -> pinned host copies of O and LSE, pipelined in chunks of 8 "
-                   "heads over an upload stream, the compute stream and a download stream; the "
-                   "host link (~210 GB/s each way on this box) bounds it"}
+           "path": "attn_fwd_from_host (one C-ABI call per step, through binding.fwd_from_host): "
+                   "pinned host -> device copies of Q, K, V, the forward, device -> pinned host "
+                   "copies of O and LSE, pipelined in chunks of 8 heads over an upload stream, "
+                   "the compute stream and a download stream; the host link (~210 GB/s each way "
+                   "on this box) bounds it"}
     del q_p, k_p, v_p, o_p, lse_p
 
     others = []

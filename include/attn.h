@@ -128,6 +128,31 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int attn_fwd_ex(const attn_params* p, cudaStream_t stream);
 
 /*
+ * End-to-end forward from host memory: copies Q, K and V from the host
+ * buffers into the device buffers of `p` (p->q, p->k, p->v, which must not
+ * be in use by other work), computes O and LSE into p->o and p->lse as
+ * attn_fwd_ex does, and copies them back into o_host and lse_host.  The
+ * work is cut into chunks of whole K/V head groups (chunk_heads query heads,
+ * rounded to whole groups) of one batch entry -- every (b, h) slice is
+ * independent -- and the chunks are pipelined over three caller-owned
+ * streams: uploads on upload_stream, the kernels on `stream` once their
+ * chunk has landed, downloads on download_stream once it is computed; the
+ * side streams first wait for the work already queued on `stream`, and
+ * `stream` waits for the last download before this returns, so the host
+ * buffers hold the result once `stream` has completed.  Host buffers should
+ * be page-locked for the copies to overlap.  Layouts as in attn_params
+ * (bf16 Q, K, V, O; f32 LSE; same shapes on host and device).  Nothing is
+ * allocated on the device; the call creates and releases timing-free events
+ * (two per chunk, two more per call).  Returns the argument checks of attn_fwd_ex, ATTN_ERR_INVALID for a
+ * null host pointer or chunk_heads < 1, ATTN_ERR_UNSUPPORTED for FP8 Q/K, and
+ * ATTN_ERR_CUDA if a copy, event or launch fails.
+ */
+int attn_fwd_from_host(const attn_params* p, const void* q_host, const void* k_host,
+                       const void* v_host, void* o_host, float* lse_host, int chunk_heads,
+                       cudaStream_t stream, cudaStream_t upload_stream,
+                       cudaStream_t download_stream);
+
+/*
  * Bytes of workspace attn_fwd_splitkv needs: float32 partial outputs
  * [B][H][num_splits][Nq][d] followed (at a 256-byte boundary) by float32
  * partial log-sum-exps [B][H][num_splits][Nq].  `d` is the width of the

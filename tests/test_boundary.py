@@ -164,6 +164,27 @@ def test_noalloc_rejects(lib):
     assert f(*big, 128, 0, 0.125, 128, None) == binding.ATTN_ERR_WORKSPACE
 
 
+def test_from_host_rejects(lib):
+    """The host-buffer entry point applies the forward's checks and its own
+    (host pointers, chunk size, FP8) before any CUDA call."""
+    f = lib.attn_fwd_from_host
+    host = ctypes.create_string_buffer(64)
+    hp = ctypes.addressof(host)
+    p = _params()
+    assert f(ctypes.byref(p), hp, hp, hp, hp, hp, 0, None, None, None) == binding.ATTN_ERR_INVALID
+    assert f(ctypes.byref(p), 0, hp, hp, hp, hp, 8, None, None, None) == binding.ATTN_ERR_INVALID
+    assert f(ctypes.byref(p), hp, hp, hp, hp, 0, 8, None, None, None) == binding.ATTN_ERR_INVALID
+    bad = _params(d=80)
+    assert f(ctypes.byref(bad), hp, hp, hp, hp, hp, 8, None, None, None) == \
+        binding.ATTN_ERR_UNSUPPORTED
+    fp8 = _params(d=128, qk_dtype=1, q_descale=1.0, k_descale=1.0)
+    assert f(ctypes.byref(fp8), hp, hp, hp, hp, hp, 8, None, None, None) == \
+        binding.ATTN_ERR_UNSUPPORTED
+    mis = _params(q=MIS)
+    assert f(ctypes.byref(mis), hp, hp, hp, hp, hp, 8, None, None, None) == binding.ATTN_ERR_ALIGN
+    assert f(None, hp, hp, hp, hp, hp, 8, None, None, None) == binding.ATTN_ERR_INVALID
+
+
 def test_combine_rejects(lib):
     c = lib.attn_combine
     assert c(0, A16, A16, A16, 1, 1, 1, 64, 4, None) == binding.ATTN_ERR_INVALID
