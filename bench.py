@@ -192,6 +192,38 @@ def event_time(fn, steps: int, stream) -> float:
     return start.elapsed_time(end) / steps
 
 
+def copy_only_step(stream, uploads, downloads, h2d: int, d2h: int, reps: int = 5) -> dict:
+    """The end-to-end step's host<->device copies with no compute: uploads
+    (device <- pinned host) alone, downloads (pinned host <- device) alone, and
+    both at once on two streams.  `both_ms` is a floor for the end-to-end step
+    (the copies have to happen; the forward can at best hide under them)."""
+    side = torch.cuda.Stream()
+
+    def up():
+        for dst, src in uploads:
+            dst.copy_(src, non_blocking=True)
+
+    def down():
+        for dst, src in downloads:
+            dst.copy_(src, non_blocking=True)
+
+    def both():
+        side.wait_stream(torch.cuda.current_stream())
+        up()
+        with torch.cuda.stream(side):
+            down()
+        torch.cuda.current_stream().wait_stream(side)
+
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, fn in (("h2d", up), ("d2h", down), ("both", both)):
+            fn()
+            out[name + "_ms"] = event_time(fn, reps, stream)
+    out["h2d_gbs"] = h2d / out["h2d_ms"] / 1e6
+    out["d2h_gbs"] = d2h / out["d2h_ms"] / 1e6
+    return out
+
+
 def event_time_each(fn, steps: int, stream, scratch: torch.Tensor | None = None) -> list:
     """ms of each of `steps` calls, every call between its own CUDA events on
     `stream`; with `scratch` (a buffer larger than L2), L2 is flushed by
@@ -575,8 +607,12 @@ def main():
     launches += e2e_steps * w.B * -(-w.H // E2E_CHUNK_HEADS)  # one attn_fwd per chunk
     h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p))
     d2h = o_p.numel() * o_p.element_size() + lse_p.numel() * lse_p.element_size()
+    link = copy_only_step(stream, [(q, q_p), (k, k_p), (v, v_p)], [(o_p, o), (lse_p, lse)],
+                          h2d, d2h)
+    link["frac"] = link["both_ms"] / e2e_ms
     e2e = {"value": world * flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOPS",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "copy_only": link,
            "path": "attn_fwd_from_host (one C-ABI call per step, through binding.fwd_from_host): "
                    "pinned host -> device copies of Q, K, V, the forward, device -> pinned host "
                    "copies of O and LSE, pipelined in chunks of 8 heads over an upload stream, "
