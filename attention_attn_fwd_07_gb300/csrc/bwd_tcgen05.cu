@@ -243,21 +243,21 @@ __device__ __forceinline__ void epilogue_sync(const Ctx& c, int warp) {
 // Row statistics of one 128-query tile as the exponent offsets the
 // elementwise warps use: nl2[i] = -LSE_i*log2(e) (-inf where the row has no
 // admissible key or lies past Nq, so P = 0 there) and nd[i] = -Delta_i.
-// Elementwise thread t < 128 writes nl2[t], thread 128 + t writes nd[t].
-__device__ __forceinline__ void load_stats(const BwdParams& p, int64_t row_base, int64_t q0,
-                                           int t, float* nl2, float* nd) {
-  const int r = t & (T - 1);
-  const int64_t i = q0 + r;
+// Elementwise thread t < 128 supplies nl2[t], thread 128 + t supplies nd[t]:
+// fetch_stat reads the thread's value from global memory (issued early, used
+// late), put_stat stores it into the tile's statistics buffer [nl2 | nd].
+__device__ __forceinline__ float fetch_stat(const BwdParams& p, int64_t row_base, int64_t q0,
+                                            int t) {
+  const int64_t i = q0 + (t & (T - 1));
   if (t < T) {
-    float l2 = -INFINITY;
-    if (i < p.Nq) {
-      const float lse = p.lse[row_base + i];
-      l2 = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
-    }
-    nl2[r] = l2;
-  } else {
-    nd[r] = i < p.Nq ? -p.delta[row_base + i] : 0.0f;
+    if (i >= p.Nq) return -INFINITY;
+    const float lse = p.lse[row_base + i];
+    return (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
   }
+  return i < p.Nq ? -p.delta[row_base + i] : 0.0f;
+}
+__device__ __forceinline__ void put_stat(float* stats, int t, float v) {
+  stats[(t < T ? 0 : T) + (t & (T - 1))] = v;
 }
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t (&v)[32],
@@ -481,17 +481,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f2_pack(p.sc_log2, p.sc_log2);
     const bool row_live = j < p.Nk;
     bool ok = true;
+    // Each thread supplies one statistic per tile; the eight warps meet on
+    // a (bounded) mbarrier per tile, double-buffered by tile parity.  The
+    // statistic of tile n + 1 is read from global memory at the start of
+    // tile n and stored after tile n's phase B, so its latency hides behind
+    // the tile's work.  Slot (n + 1) % 2 last served tile n - 1, whose every
+    // reader arrived for tile n (after its phase B of n - 1) before this
+    // thread got past tile n's wait.
+    if (n_items > 0) {
+      int64_t bh, q0;
+      item_rows(0, bh, q0);
+      put_stat(stat_buf, threadIdx.x, fetch_stat(p, bh * p.Nq, q0, threadIdx.x));
+      mbar_arrive(c.bar(kBarStat));  // release: this thread's statistic is written
+    }
     for (int n = 0; n < n_items; ++n) {
       int64_t bh, q0;
       item_rows(n, bh, q0);
       float* nl2 = stat_buf + (n & 1) * 2 * T;
       float* nd = nl2 + T;
-      // Each thread writes one statistic; the eight warps meet on a
-      // (bounded) mbarrier per tile, double-buffered by tile parity.
-      load_stats(p, bh * p.Nq, q0, threadIdx.x, nl2, nd);
-      mbar_arrive(c.bar(kBarStat + (n & 1)));  // release: this thread's statistic is written
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarStat + (n & 1)), (n >> 1) & 1));
       if (!ok) break;
+      float stat_next = 0.0f;
+      if (n + 1 < n_items) {
+        int64_t bh1, q01;
+        item_rows(n + 1, bh1, q01);
+        stat_next = fetch_stat(p, bh1 * p.Nq, q01, threadIdx.x);
+      }
       // Key j is visible to query i = q0 + col iff j < Nk and (not causal or
       // j <= i + off), i.e. col >= thr.  Tiles where no lane masks any of
       // its columns take the unmasked path.
@@ -570,6 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarDS));
+      if (n + 1 < n_items) {
+        put_stat(stat_buf + ((n + 1) & 1) * 2 * T, threadIdx.x, stat_next);
+        mbar_arrive(c.bar(kBarStat + ((n + 1) & 1)));
+      }
     }
     if (ok && n_items > 0) {
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarAcc), 0));
