@@ -243,20 +243,23 @@ __device__ __forceinline__ void epilogue_sync(const Ctx& c, int warp) {
 // Row statistics of one 128-query tile as the exponent offsets the
 // elementwise warps use: nl2[i] = -LSE_i*log2(e) (-inf where the row has no
 // admissible key or lies past Nq, so P = 0 there) and nd[i] = -Delta_i.
-// Elementwise thread t < 128 supplies nl2[t], thread 128 + t supplies nd[t]:
-// fetch_stat reads the thread's value from global memory (issued early, used
-// late), put_stat stores it into the tile's statistics buffer [nl2 | nd].
+// Elementwise thread t < 128 supplies nl2[t], thread 128 + t supplies nd[t].
+// fetch_stat only loads the raw LSE or Delta (an in-bounds row: past Nq it
+// reads row Nq - 1), so nothing waits for the load until put_stat turns the
+// value into the offset and stores it into the tile's buffer [nl2 | nd].
 __device__ __forceinline__ float fetch_stat(const BwdParams& p, int64_t row_base, int64_t q0,
                                             int t) {
-  const int64_t i = q0 + (t & (T - 1));
-  if (t < T) {
-    if (i >= p.Nq) return -INFINITY;
-    const float lse = p.lse[row_base + i];
-    return (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
-  }
-  return i < p.Nq ? -p.delta[row_base + i] : 0.0f;
+  const int64_t i = min(q0 + (t & (T - 1)), p.Nq - 1);
+  return (t < T ? p.lse : p.delta)[row_base + i];
 }
-__device__ __forceinline__ void put_stat(float* stats, int t, float v) {
+__device__ __forceinline__ void put_stat(const BwdParams& p, float* stats, int64_t q0, int t,
+                                         float raw) {
+  const bool live = q0 + (t & (T - 1)) < p.Nq;
+  float v;
+  if (t < T)
+    v = (!live || raw == -INFINITY) ? -INFINITY : -raw * kLog2e;
+  else
+    v = live ? -raw : 0.0f;
   stats[(t < T ? 0 : T) + (t & (T - 1))] = v;
 }
 
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_items > 0) {
       int64_t bh, q0;
       item_rows(0, bh, q0);
-      put_stat(stat_buf, threadIdx.x, fetch_stat(p, bh * p.Nq, q0, threadIdx.x));
+      put_stat(p, stat_buf, q0, threadIdx.x, fetch_stat(p, bh * p.Nq, q0, threadIdx.x));
       mbar_arrive(c.bar(kBarStat));  // release: this thread's statistic is written
     }
     for (int n = 0; n < n_items; ++n) {
@@ -502,10 +505,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait(c.bar(kBarStat + (n & 1)), (n >> 1) & 1));
       if (!ok) break;
       float stat_next = 0.0f;
+      int64_t q_next = 0;
       if (n + 1 < n_items) {
-        int64_t bh1, q01;
-        item_rows(n + 1, bh1, q01);
-        stat_next = fetch_stat(p, bh1 * p.Nq, q01, threadIdx.x);
+        int64_t bh1;
+        item_rows(n + 1, bh1, q_next);
+        stat_next = fetch_stat(p, bh1 * p.Nq, q_next, threadIdx.x);
       }
       // Key j is visible to query i = q0 + col iff j < Nk and (not causal or
       // j <= i + off), i.e. col >= thr.  Tiles where no lane masks any of
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(kBarDS));
       if (n + 1 < n_items) {
-        put_stat(stat_buf + ((n + 1) & 1) * 2 * T, threadIdx.x, stat_next);
+        put_stat(p, stat_buf + ((n + 1) & 1) * 2 * T, q_next, threadIdx.x, stat_next);
         mbar_arrive(c.bar(kBarStat + ((n + 1) & 1)));
       }
     }
