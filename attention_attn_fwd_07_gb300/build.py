@@ -20,7 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_gb300.so")
 SOURCES = ["api.cu", "fwd_tcgen05.cu", "splitkv.cu", "noalloc.cu", "bwd_tcgen05.cu",
            "bwd_tcgen05_d64.cu",
-           "bwd_tcgen05_d64_v128.cu", "bwd_tcgen05_d128_v64.cu", "splitkv_tc.cu"]
+           "bwd_tcgen05_d64_v128.cu", "bwd_tcgen05_d128_v64.cu", "bwd_tcgen05_d96.cu",
+           "splitkv_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

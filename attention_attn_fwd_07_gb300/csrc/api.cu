@@ -407,10 +407,12 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   if (p->query_offset < -kMaxOffset || p->query_offset > kMaxOffset) return ATTN_ERR_INVALID;
   if (p->query_offset < 0 && !(p->flags & ATTN_FLAG_ALLOW_NEG_OFFSET)) return ATTN_ERR_INVALID;
   if (p->Hkv < 0 || p->Hkv > p->H || (p->Hkv > 0 && p->H % p->Hkv != 0)) return ATTN_ERR_INVALID;
-  if (p->d != 64 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 96 && p->d != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->value_dim < 0) return ATTN_ERR_INVALID;
   const int64_t dv = p->value_dim > 0 ? p->value_dim : p->d;
-  if (dv != 64 && dv != 128) return ATTN_ERR_UNSUPPORTED;
+  // d and dv in {64, 128} in any pair; 96 with 96 only.
+  if ((p->d == 96) != (dv == 96) || (dv != 64 && dv != 96 && dv != 128))
+    return ATTN_ERR_UNSUPPORTED;
   if (p->B > kMaxDim || p->H > kMaxDim || p->B * p->H > kMaxDim || p->Nq > kMaxDim ||
       p->Nk > kMaxDim)
     return ATTN_ERR_UNSUPPORTED;
@@ -455,7 +457,9 @@ extern "C" int attn_bwd(const attn_bwd_params* p, void* workspace, size_t worksp
   a.scale = p->scale;
   a.timeout_ns = 1000ull * (p->wait_timeout_us ? p->wait_timeout_us : 1000000u);
   cudaError_t err;
-  if (p->d == 64)
+  if (p->d == 96)
+    err = launch_bwd<96, 96>(a, tq, tk, tv, tdo, stream);
+  else if (p->d == 64)
     err = dv == 64 ? launch_bwd<64, 64>(a, tq, tk, tv, tdo, stream)
                    : launch_bwd<64, 128>(a, tq, tk, tv, tdo, stream);
   else

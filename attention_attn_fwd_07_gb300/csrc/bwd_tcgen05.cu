@@ -54,7 +54,8 @@ namespace {
 
 constexpr int D = ATTN_BWD_HEAD_DIM;       // head dim of Q and K
 constexpr int DV = ATTN_BWD_VALUE_DIM;     // head dim of V, O and dO
-static_assert((D == 64 || D == 128) && (DV == 64 || DV == 128), "head dims 64 and 128");
+static_assert(((D == 64 || D == 128) && (DV == 64 || DV == 128)) || (D == 96 && DV == 96),
+              "head dims 64 and 128 (any pair), or 96 with 96");
 constexpr int T = 128;                    // rows per query tile and per key tile
 constexpr int kEwWarps = 8;
 constexpr int kEwThreads = kEwWarps * 32;
@@ -62,8 +63,12 @@ constexpr int kThreads = kEwThreads + 64;
 constexpr int kWarpMma = 8;
 constexpr int kWarpLoad = 9;
 constexpr uint32_t kAtomBytes = 128u * 128u;  // [128 rows][64 bf16] swizzled box
-constexpr uint32_t kQKTileBytes = T * D * 2;  // one [128][d] bf16 tile (d / 64 atoms): Q, K
-constexpr uint32_t kVTileBytes = T * DV * 2;  // one [128][dv] bf16 tile: V, dO
+// One [128][d] bf16 tile (Q, K) takes ceil(d / 64) atoms, one [128][dv] tile
+// (V, dO) ceil(dv / 64); at 96 the second atom's columns 96-127 are the
+// tensor map's zero fill, never read by an MMA.
+constexpr int kDAtoms = (D + 63) / 64, kDVAtoms = (DV + 63) / 64;
+constexpr uint32_t kQKTileBytes = kDAtoms * kAtomBytes;
+constexpr uint32_t kVTileBytes = kDVAtoms * kAtomBytes;
 constexpr int kStagesA = 3;  // ring A (Q tiles in the dK/dV kernel, K tiles in the dQ kernel)
 constexpr int kStagesB = 2;  // ring B (dO tiles, respectively V tiles)
 constexpr uint32_t kIdescSS = idesc_bf16_f32(T, T, 0);  // both operands K-major
@@ -159,9 +164,11 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
 // from one elect.sync.
 template <int W>
 __device__ __forceinline__ void mma_ss_tiles_w(uint32_t d_tmem, uint32_t a_tile, uint32_t b_tile) {
-  static_assert(W == 64 || W == 128, "tile widths 64 and 128");
+  static_assert(W == 64 || W == 96 || W == 128, "tile widths 64, 96 and 128");
   if constexpr (W == 128)
     mma_ss_run8_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
+  else if constexpr (W == 96)
+    mma_ss_run6_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
   else
     mma_ss_run4_w(d_tmem, desc_kmajor(a_tile, 0), desc_kmajor(b_tile, 0), kIdescSS, 0u);
 }
@@ -174,11 +181,11 @@ __device__ __forceinline__ void mma_ts_tile_w(uint32_t d_tmem, uint32_t a_tmem, 
   mma_ts_run8_halves_w(d_tmem, a_tmem, desc_mnmajor(b_tile, 0), idesc, accumulate ? 1u : 0u);
 }
 
-// One [128][W] bf16 tile (W / 64 swizzle atoms).
+// One [128][W] bf16 tile (ceil(W / 64) swizzle atoms).
 template <int W>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                           int row, int64_t z) {
-  for (int a = 0; a < W / 64; ++a)
+  for (int a = 0; a < (W + 63) / 64; ++a)
     tma_load_3d(dst + a * kAtomBytes, map, bar, a * 64, row, static_cast<int>(z));
 }
 
@@ -292,6 +299,12 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
     const uint2 a = *reinterpret_cast<const uint2*>(o + row * DV + 4 * lane);
     const uint2 b = *reinterpret_cast<const uint2*>(dout + row * DV + 4 * lane);
     acc = lo(a.x) * lo(b.x) + hi(a.x) * hi(b.x) + lo(a.y) * lo(b.y) + hi(a.y) * hi(b.y);
+  } else if constexpr (DV == 96) {  // three elements per lane, 32 apart
+    acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 3; ++e)
+      acc += __bfloat162float(o[row * DV + 32 * e + lane]) *
+             __bfloat162float(dout[row * DV + 32 * e + lane]);
   } else {  // two elements per lane
     const uint32_t a = *reinterpret_cast<const uint32_t*>(o + row * DV + 2 * lane);
     const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + row * DV + 2 * lane);
@@ -599,19 +612,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
-      // Each thread stores half of its row's d columns of dK and half of its
-      // dv columns of dV.
+      // Each thread stores half of its row's 32-column chunks of dK (chunk
+      // cc with cc % 2 = half) and half of those of dV.
       const int64_t kv_row = bkv * p.Nk + j;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const uint32_t col = static_cast<uint32_t>((D / 2) * half + 32 * cc);
+      for (int cc = half; cc < D / 32; cc += 2) {
+        const uint32_t col = static_cast<uint32_t>(32 * cc);
         uint32_t kd[32] = {};
         if (n_items > 0) tmem_ld_x32(tdK + lane_off + col, kd);
         if (row_live) store_row_bf16(p.dk + kv_row * D + col, kd, p.scale, n_items == 0);
       }
 #pragma unroll 1
-      for (int cc = 0; cc < DV / 64; ++cc) {
-        const uint32_t col = static_cast<uint32_t>((DV / 2) * half + 32 * cc);
+      for (int cc = half; cc < DV / 32; cc += 2) {
+        const uint32_t col = static_cast<uint32_t>(32 * cc);
         uint32_t vd[32] = {};
         if (n_items > 0) tmem_ld_x32(tdV + lane_off + col, vd);
         if (row_live) store_row_bf16(p.dv + kv_row * DV + col, vd, 1.0f, n_items == 0);
@@ -815,11 +828,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) tc_fence_after();
     }
     if (ok) {
-      // Each thread stores half of its row's d columns.
+      // Each thread stores half of its row's 32-column chunks (chunk cc with
+      // cc % 2 = half).
       const bool valid = i < p.Nq;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const uint32_t col = static_cast<uint32_t>((D / 2) * half + 32 * cc);
+      for (int cc = half; cc < D / 32; cc += 2) {
+        const uint32_t col = static_cast<uint32_t>(32 * cc);
         uint32_t qd[32] = {};
         if (n_kt > 0) tmem_ld_x32(tdQ + lane_off + col, qd);
         // A row with no admissible key stores +0 exactly (its dS is +-0).

@@ -85,7 +85,7 @@ struct BwdArgs {
 
 // Backward launches for key head dim D and value head dim DV, one
 // translation unit each (bwd_tcgen05.cu: 128/128, bwd_tcgen05_d64.cu: 64/64,
-// bwd_tcgen05_d64_v128.cu, bwd_tcgen05_d128_v64.cu).
+// bwd_tcgen05_d64_v128.cu, bwd_tcgen05_d128_v64.cu, bwd_tcgen05_d96.cu: 96/96).
 template <int D, int DV>
 cudaError_t launch_bwd(const BwdArgs& a, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, cudaStream_t stream);
@@ -97,6 +97,7 @@ ATTN_DECLARE_BWD(64, 64)
 ATTN_DECLARE_BWD(128, 128)
 ATTN_DECLARE_BWD(64, 128)
 ATTN_DECLARE_BWD(128, 64)
+ATTN_DECLARE_BWD(96, 96)
 #undef ATTN_DECLARE_BWD
 
 // Split-KV partial on the tensor cores for rows that share K/V heads

@@ -240,8 +240,9 @@ size_t attn_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq);
  * row can see get zero dK and dV.  Grouped K/V heads sum their group's
  * contributions.  Three launches on `stream` (row corrections, a dK/dV kernel
  * per 128-key tile, a dQ kernel per 128-query tile); no atomics, so the
- * result is deterministic.  d and dv in {64, 128} (ATTN_ERR_UNSUPPORTED
- * otherwise; dv may differ from d).
+ * result is deterministic.  d and dv in {64, 128} (dv may differ from d), or
+ * d = dv = 96; ATTN_ERR_UNSUPPORTED otherwise (head dim 256 has no
+ * backward).
  * `workspace` (device, 16-byte aligned, caller-owned) must hold
  * attn_bwd_workspace_bytes(B, H, Nq) bytes.
  */

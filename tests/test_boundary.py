@@ -231,7 +231,9 @@ def _bwd_params(**kw):
     (dict(Hkv=3), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(Hkv=4), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(query_offset=-1), 1 << 20, binding.ATTN_ERR_INVALID),
-    (dict(d=96), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96, value_dim=64), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96, value_dim=128), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
     (dict(value_dim=-1), 1 << 20, binding.ATTN_ERR_INVALID),
     (dict(value_dim=96), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),
     (dict(value_dim=256), 1 << 20, binding.ATTN_ERR_UNSUPPORTED),

@@ -78,7 +78,7 @@ def check_case(B, H, Hkv, Nq, Nk, causal, off, seed, what, d=128, dv=0):
             compare_grad(dv, rv, f"{what} dV", zk))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", [1, 100, 128, 129, 333])
 def test_bwd_square(n, causal, d):
@@ -92,7 +92,7 @@ def test_bwd_rectangular(nq, nk, causal):
     check_case(1, 2, 2, nq, nk, causal, off, 2100 + nq + nk, f"bwd {nq}x{nk} off={off}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("hkv", [1, 2, 4])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bwd_gqa(hkv, causal, d):
@@ -100,7 +100,7 @@ def test_bwd_gqa(hkv, causal, d):
                f"bwd GQA Hkv={hkv} d={d} causal={causal}", d=d)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 96, 128])
 @pytest.mark.parametrize("off", [-150, -1, 5, 400])
 def test_bwd_offsets(off, d):
     # off < 0: the first -off rows see no key (dQ = 0) and the last keys no
@@ -129,14 +129,31 @@ def check_whole_head(w, q, k, v, dout, dq, dk, dv, b, h):
         compare_grad(g[b:b + 1, h:h + 1], r, f"{w.name}: whole head b={b} h={h} {name}")
 
 
-def test_bwd_rejects_d96():
-    w = W.Workload("d96", 1, 1, 64, 64, 96, False, 7)
-    q, k, v = (t.to(DEV) for t in W.make_qkv(w))
-    o = torch.zeros_like(q)
-    lse = torch.zeros((1, 1, 64), dtype=torch.float32, device=DEV)
-    with pytest.raises(binding.AttnError) as e:
-        binding.attn_bwd(q, k, v, o, lse, torch.zeros_like(q), False, w.scale)
-    assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
+def test_bwd_rejects_unsupported_head_dims():
+    """Head dim 96 runs with value dim 96 only; 256 has no backward."""
+    for d, dv in ((96, 64), (64, 96), (256, 256)):
+        w = W.Workload(f"d{d} dv{dv}", 1, 1, 64, 64, d, False, 7, dv=dv)
+        q, k, v = (t.to(DEV) for t in W.make_qkv(w))
+        o = torch.zeros_like(q[..., :1].expand(*q.shape[:3], v.shape[-1])).contiguous()
+        lse = torch.zeros((1, 1, 64), dtype=torch.float32, device=DEV)
+        with pytest.raises(binding.AttnError) as e:
+            binding.attn_bwd(q, k, v, o, lse, torch.zeros_like(o), False, w.scale)
+        assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_d96_long_prefill_whole_head():
+    """B2 H32 N8192 d96 causal (the d = 96 long prefill): the last (b, h)
+    slice whole, element by element on dQ, dK and dV, and dK, dV of every
+    slice through the softmax identities."""
+    w = W.LONG_PREFILL_D96
+    q, k, v = W.make_qkv(w, device=DEV)
+    dout = W.make_dout(w, device=DEV)
+    dq, dk, dv = run_bwd(q, k, v, dout, True, w.scale)
+    check_whole_head(w, q, k, v, dout, dq, dk, dv, w.B - 1, w.H - 1)
+    sum_dk, sum_dv = dk.double().sum(dim=2), dv.double().sum(dim=2)
+    sum_do = dout.double().sum(dim=2)
+    assert (sum_dk.abs() <= 1e-2 * dk.double().abs().sum(dim=2) + 1e-3).all()
+    assert ((sum_dv - sum_do).abs() <= 1e-2 * dv.double().abs().sum(dim=2) + 1e-3).all()
 
 
 def test_bwd_d64_prefill_sampled():
