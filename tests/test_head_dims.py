@@ -173,14 +173,15 @@ def test_decode_d256_full_size():
 
 def test_remaining_refusals():
     """Head dims outside {64, 96, 128, 256}, value dims of their own at 96
-    and 256, FP8 at 96/256 and the backward at 96/256 stay unsupported."""
+    and 256, FP8 at 96/256 and the backward at 256 stay unsupported (the
+    backward at 96 is tested in test_bwd.py)."""
     for d in (32, 80, 192):
         w = W.Workload("bad", 1, 1, 64, 64, d, False, 7)
         q, k, v = (t.to(DEV) for t in W.make_qkv(w))
         with pytest.raises(binding.AttnError) as e:
             binding.attn_fwd(q, k, v, False, w.scale)
         assert e.value.status == binding.ATTN_ERR_UNSUPPORTED
-    for d in DIMS:
+    for d in (256,):
         w = W.Workload("bwd", 1, 1, 64, 64, d, False, 7)
         q, k, v = (t.to(DEV) for t in W.make_qkv(w))
         o, lse = binding.attn_fwd(q, k, v, False, w.scale)
