@@ -249,6 +249,29 @@ def launch_stats(times_ms: list) -> dict:
             "p90": float(np.percentile(a, 90)), "n": int(a.size)}
 
 
+def graph_time(fn, calls: int, stream, reps: int = 5) -> float | None:
+    """ms per call of `calls` back-to-back calls of fn captured in one CUDA
+    graph and replayed `reps` times (launch overhead out of the picture);
+    None if the capture fails."""
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()  # warm: any one-time host work happens outside the capture
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(calls):
+                    fn()
+        with torch.cuda.stream(stream):  # replay on the stream the events are on
+            graph.replay()
+            torch.cuda.synchronize()
+            ms = event_time(graph.replay, reps, stream) / calls
+        del graph
+        return ms
+    except Exception:  # capture refused (a call not capturable here): no figure
+        torch.cuda.synchronize()
+        return None
+
+
 def event_time_flushed(fn, steps: int, stream, scratch: torch.Tensor) -> tuple:
     """Average ms per call with L2 flushed before each call, and the per-call
     distribution."""
@@ -666,6 +689,15 @@ def main():
                 others[-1]["launch_ms"] = flushed_dist
                 others[-1]["value_from"] = ("median of per-call times (mean "
                                             f"{mean_ms:.4f} ms over the same calls)")
+                gms = graph_time(st, 100, stream)
+                if gms is not None:
+                    launches += 601  # a warm-up call, one check replay, five timed replays of 100
+                    others[-1]["graph_100_calls"] = {
+                        "value": world * prefill_flops(wo) / (gms / 1e3) / 1e12,
+                        "ms_per_call": gms,
+                        "note": "100 calls captured in one CUDA graph, replayed back to back; "
+                                "inputs stay L2-resident between calls (no flush), so this "
+                                "is the launch-overhead-free rate, not the line's value"}
             if wo.d in (64, 96):  # the d = 64 and d = 96 backwards on the same inputs
                 rb = run_backward(wo, qq, kk, vv, oo, ll, dev, stream, args, pk, pk_src, world,
                                   max_over_ranks_)
