@@ -241,21 +241,37 @@ __device__ __forceinline__ Item decode_item(int64_t idx, const KParams& p) {
     const uint32_t n_items = static_cast<uint32_t>(p.n_bh) * nq32;
     const uint32_t a = (idx32 / chunk) * chunk;        // chunk [a, e) of the (b, h)-major list
     const uint32_t e = min(a + chunk, n_items);
-    const int64_t h_first = a / nq32, h_last = (e - 1) / nq32;
-    const int64_t a0 = a % nq32, e0 = (e - 1) % nq32;  // first block of h_first, last of h_last
+    const uint32_t h_first = a / nq32, h_last = (e - 1) / nq32;
+    const uint32_t a0 = a % nq32, e0 = (e - 1) % nq32;  // first block of h_first, last of h_last
     // Rank r inside the chunk: query blocks from the last down, the chunk's
-    // heads holding that block in (b, h) order.
-    int64_t r = idx32 - a;
-    for (qb = nq - 1;; --qb) {
-      const int64_t lo = qb >= a0 ? h_first : h_first + 1;
-      const int64_t hi = qb <= e0 ? h_last : h_last - 1;
-      const int64_t cnt = hi >= lo ? hi - lo + 1 : 0;
-      if (r < cnt || qb == 0) {
-        it.bh = lo + r;
-        break;
-      }
-      r -= cnt;
+    // heads holding that block in (b, h) order.  Block qb is held by the
+    // chunk's hc heads except h_first (when qb < a0) and h_last (when
+    // qb > e0), so the heads per block are constant on three ranges of
+    // blocks, from the top: [u1, nq) with hc - 1, [u2, u1) with c2 (all hc
+    // on [a0, e0], or hc - 2 between e0 and a0), [0, u2) with hc - 1.  (A
+    // chunk inside one head has only the middle range.)
+    const uint32_t hc = h_last - h_first + 1;
+    const uint32_t u1 = max(a0, e0 + 1);
+    const bool inner = a0 <= e0;
+    const uint32_t u2 = inner ? a0 : e0 + 1;
+    const uint32_t c2 = inner ? hc : hc - 2;
+    const uint32_t lo2 = inner ? h_first : h_first + 1;
+    const uint32_t c1 = hc - 1;
+    const uint32_t n1 = (nq32 - u1) * c1, n2 = (u1 - u2) * c2;
+    uint32_t r = idx32 - a, h, q;
+    if (r < n1) {
+      h = h_first + r % c1;
+      q = nq32 - 1 - r / c1;
+    } else if ((r -= n1) < n2) {
+      h = lo2 + r % c2;
+      q = u1 - 1 - r / c2;
+    } else {
+      r -= n2;
+      h = h_first + 1 + r % c1;
+      q = u2 - 1 - r / c1;
     }
+    it.bh = h;
+    qb = q;
   } else {
     it.bh = idx32 / nq32;
     qb = idx32 % nq32;
@@ -986,10 +1002,12 @@ __global__ void __launch_bounds__(threads_for(1), 2)
     int64_t sc = 0;  // score tiles of this query tile handled so far
     int o_uses = 0;  // items in which this query tile had keys (O barrier phases)
     bool ok = true;
-    for (int64_t k = 0; ok; ++k) {
-      const int64_t idx = item_of(k, cta, G, n_items);
-      if (idx < 0) break;
-      const Item it = decode_item<NT>(idx, p);
+    // The next item is decoded while the last P V of the current one runs
+    // (its integer divisions are otherwise on the softmax's critical path).
+    int64_t idx = item_of(0, cta, G, n_items);
+    Item it = {};
+    if (idx >= 0) it = decode_item<NT>(idx, p);
+    for (int64_t k = 0; ok && idx >= 0; ++k) {
       const int64_t row0 = it.q0 + x * BM;
       const int64_t row = row0 + row_in_tile;
       const int n = it.ntile[x];
@@ -1120,6 +1138,9 @@ __global__ void __launch_bounds__(threads_for(1), 2)
         l += sum_lo + sum_hi;
       }
       if (!ok) break;
+      const int64_t next_idx = item_of(k + 1, cta, G, n_items);
+      Item next = {};
+      if (next_idx >= 0) next = decode_item<NT>(next_idx, p);
       if (n > 0) {
         ok = __all_sync(0xffffffffu, wait(bar(C::kBarO + x), static_cast<uint32_t>(o_uses & 1)));
         if (!ok) break;
@@ -1155,6 +1176,8 @@ __global__ void __launch_bounds__(threads_for(1), 2)
             empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f;
       sc += n;
       o_uses += n > 0 ? 1 : 0;
+      idx = next_idx;
+      it = next;
     }
   }
 
