@@ -249,22 +249,27 @@ def launch_stats(times_ms: list) -> dict:
             "p90": float(np.percentile(a, 90)), "n": int(a.size)}
 
 
-def graph_time(fn, calls: int, stream, reps: int = 5) -> float | None:
-    """ms per call of `calls` back-to-back calls of fn captured in one CUDA
-    graph and replayed `reps` times (launch overhead out of the picture);
-    None if the capture fails."""
+def graph_time(launch_on, calls: int, reps: int = 5) -> float | None:
+    """ms per call of `calls` back-to-back calls captured in one CUDA graph
+    and replayed `reps` times (launch overhead out of the picture);
+    launch_on(stream) issues one call on that stream.  Capture and replay
+    run on a stream of their own (the legacy default stream cannot be
+    captured); None if the capture fails."""
+    side = torch.cuda.Stream()
+    fn = lambda: launch_on(side)  # noqa: E731
     try:
+        torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
+        with torch.cuda.stream(side):
             fn()  # warm: any one-time host work happens outside the capture
             torch.cuda.synchronize()
-            with torch.cuda.graph(graph, stream=stream):
+            with torch.cuda.graph(graph, stream=side):
                 for _ in range(calls):
                     fn()
-        with torch.cuda.stream(stream):  # replay on the stream the events are on
+        with torch.cuda.stream(side):  # replay on the stream the events are on
             graph.replay()
             torch.cuda.synchronize()
-            ms = event_time(graph.replay, reps, stream) / calls
+            ms = event_time(graph.replay, reps, side) / calls
         del graph
         return ms
     except Exception:  # capture refused (a call not capturable here): no figure
@@ -689,7 +694,9 @@ def main():
                 others[-1]["launch_ms"] = flushed_dist
                 others[-1]["value_from"] = ("median of per-call times (mean "
                                             f"{mean_ms:.4f} ms over the same calls)")
-                gms = graph_time(st, 100, stream)
+                gms = graph_time(
+                    lambda s, qq=qq, kk=kk, vv=vv, oo=oo, ll=ll, wo=wo: binding.attn_fwd(
+                        qq, kk, vv, wo.causal, wo.scale, o=oo, lse=ll, stream=s), 100)
                 if gms is not None:
                     launches += 601  # a warm-up call, one check replay, five timed replays of 100
                     others[-1]["graph_100_calls"] = {

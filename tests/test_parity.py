@@ -323,6 +323,25 @@ def test_prefill_full_size():
     compare(o, lse, o_ref, lse_ref, w.name)
 
 
+def test_persistent_chunks_straddling_heads():
+    """d = 64 causal at B1 H96 N5120: the persistent kernel's causal
+    scheduling chunks (on a 152-SM GB300: three of 1216 items and one of
+    192, over heads of 40 query blocks) start and end inside heads, and the
+    third starts at block 32 of its first head and ends at block 7 of its
+    last, so the work-item decode takes every one of its block ranges.  One
+    seeded row of every (head, 128-row query block) item, so a missed or
+    doubled item shows, plus one whole head."""
+    w = W.Workload("chunks B1 H96 N5120 d64 causal", 1, 96, 5120, 5120, 64, True, 1200)
+    q, k, v = W.make_qkv(w)
+    o, lse = run_fwd(*to_dev(q, k, v), w.causal, w.scale)
+    rng = np.random.default_rng(1200)
+    n_blocks = w.Nq // 128
+    rows = {bh * w.Nq + qb * 128 + int(rng.integers(0, 128))
+            for bh in range(w.B * w.H) for qb in range(n_blocks)}
+    rows |= set(range(61 * w.Nq, 62 * w.Nq))
+    _sampled(w, o, lse, q, k, v, np.array(sorted(rows), dtype=np.int64))
+
+
 @pytest.mark.parametrize("wl", [W.LONG_PREFILL_CAUSAL, W.LONG_PREFILL_NONCAUSAL],
                          ids=["causal", "noncausal"])
 def test_long_prefill_full_size(wl):
